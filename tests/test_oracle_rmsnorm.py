@@ -1,0 +1,102 @@
+"""Oracle pins: residual add + RMSNorm.
+
+* fused == unfused, bitwise (two separately written code paths);
+* zero input, constant input, tiny input (eps inside the root), each against
+  the definition y = h / sqrt(mean(h^2) + eps) * gamma evaluated in float64;
+* random inputs within 2 fp16 ulp of the float64 definition;
+* the blocked sum-of-squares order on a hand-derived case.
+"""
+import numpy as np
+import pytest
+
+F16 = np.float16
+EPS = 1e-6
+
+
+def _ref64(h, gamma, eps=EPS):
+    h = h.astype(np.float64)
+    return h / np.sqrt(np.mean(h * h) + eps) * gamma.astype(np.float64)
+
+
+def _ulp16(v):
+    v = np.abs(v.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(v, 2.0 ** -14)))
+    return 2.0 ** (e - 10)
+
+
+@pytest.mark.parametrize("K", [32, 96, 1024, 2048, 5376, 50])
+def test_fused_equals_unfused(orc, K):
+    rng = np.random.default_rng(K)
+    M = 3
+    x = rng.standard_normal((M, K)).astype(F16)
+    r = rng.standard_normal((M, K)).astype(F16)
+    g = (1 + 0.1 * rng.standard_normal(K)).astype(F16)
+    hf, yf = orc.fused_residual_rmsnorm(x, r, g, EPS)
+    for m in range(M):
+        hu = orc.residual_add(x[m], r[m])
+        yu = orc.rmsnorm(hu, g, EPS, order=0)
+        assert np.array_equal(hf[m], hu)
+        assert np.array_equal(yf[m], yu)
+
+
+def test_zero_input(orc):
+    K = 256
+    z = np.zeros(K, F16)
+    g = np.full(K, 1.5, F16)
+    h, y = orc.fused_residual_rmsnorm(z, z, g, EPS)
+    assert np.all(y == 0) and np.all(h == 0)
+    x = np.linspace(-3, 3, K).astype(F16)
+    h, y = orc.fused_residual_rmsnorm(x, -x, g, EPS)      # x + (-x) = 0 exactly
+    assert np.all(y.view(F16).astype(np.float32) == 0)
+
+
+@pytest.mark.parametrize("a", [3.0, -0.75, 100.0, 2.0 ** -12])
+def test_constant_input(orc, a):
+    K = 512
+    h = np.full(K, a, F16)
+    g = np.linspace(0.8, 1.2, K).astype(F16)
+    y = orc.rmsnorm(h, g, EPS).view(F16)
+    ref = _ref64(h, g)
+    assert np.all(np.abs(y.astype(np.float64) - ref) <= _ulp16(ref))
+
+
+def test_eps_inside_root(orc):
+    # h = 2^-12: mean(h^2) = 2^-24 ~ 6e-8 is small next to eps = 1e-6, so
+    # y = 2^-12 / sqrt(2^-24 + 1e-6) = 0.2372...; without eps it would be 1.0,
+    # with eps outside the root 0.996.
+    K = 64
+    h = np.full(K, 2.0 ** -12, F16)
+    g = np.ones(K, F16)
+    y = orc.rmsnorm(h, g, EPS).view(F16).astype(np.float64)
+    assert np.all(np.abs(y - 0.23717) < 2e-4)
+
+
+def test_gamma_used_as_is(orc):
+    # h = 3 everywhere, gamma = 0.5 -> y = 0.5 (a (1 + gamma) form would give 0.75)
+    K = 32
+    y = orc.rmsnorm(np.full(K, 3.0, F16), np.full(K, 0.5, F16), EPS).view(F16)
+    assert np.all(y == F16(0.5))
+
+
+@pytest.mark.parametrize("K", [1024, 2048, 5376])
+def test_random_within_2ulp(orc, K):
+    rng = np.random.default_rng(K + 1)
+    x = rng.standard_normal(K).astype(F16)
+    r = rng.standard_normal(K).astype(F16)
+    g = (1 + 0.1 * rng.standard_normal(K)).astype(F16)
+    hb, yb = orc.fused_residual_rmsnorm(x, r, g, EPS)
+    hh = hb[0].view(F16)
+    assert np.all(hh == (x.astype(np.float32) + r.astype(np.float32)).astype(F16))
+    ref = _ref64(hh, g)
+    y = yb[0].view(F16).astype(np.float64)
+    assert np.all(np.abs(y - ref) <= 2 * _ulp16(ref))
+
+
+def test_sumsq_block_order(orc):
+    # h0 = 2048 (h0^2 = 2^22), h1..31 = 2^-7 (squares 2^-14), h32..63 = 0.25
+    # (squares 2^-4).  fp32 spacing at 2^22 is 0.5, so every small square is
+    # absorbed by a serial chain: 2^22.  Blocked: block 0 -> 2^22, block 1 -> 2
+    # exactly, total 2^22 + 2.
+    h = np.array([2048.0] + [2.0 ** -7] * 31 + [0.25] * 32, F16)
+    assert orc.sumsq(h, order=0) == 2.0 ** 22 + 2
+    assert orc.sumsq(h, order=1) == 2.0 ** 22
