@@ -1,0 +1,217 @@
+// qmv_abi.cu -- the C ABI declared in include/qmv.h: argument validation on
+// the host, pack descriptors, and dispatch to the kernels.  Nothing here
+// computes on the host: every step of the matvec runs in the kernels.
+#include <new>
+
+#include "qmv_internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return QMV_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool pack_ok(const qmv_pack* p) { return p && p->magic == QMV_PACK_MAGIC; }
+
+bool shape_ok(int K, int bits) {
+  if (K < 32 || K % 32 != 0) return false;
+  return ((int64_t)K * bits) % 128 == 0;   // a row is a whole number of 16-byte units
+}
+
+}  // namespace
+
+namespace qmv {
+
+const DevInfo& dev_info() {
+  static thread_local int cached_dev = -1;
+  static thread_local DevInfo info{152, 227 * 1024};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return info;
+  if (dev != cached_dev) {
+    int sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+      info.sms = sms;
+    if (cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+        smem > 0)
+      info.max_smem_optin = smem;
+    cached_dev = dev;
+  }
+  return info;
+}
+
+}  // namespace qmv
+
+extern "C" {
+
+int qmv_create_pack(qmv_pack** out, int N, int K, int bits, int group, size_t* codes_bytes,
+                    size_t* scales_bytes) {
+  if (!out) return QMV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (bits != 2 && bits != 4 && bits != 8) return QMV_ERR_INVALID_ARG;
+  if (N < 1 || !shape_ok(K, bits)) return QMV_ERR_SHAPE;
+  if (group != 32 && group != K) return QMV_ERR_INVALID_ARG;
+  qmv_pack* p = new (std::nothrow) qmv_pack;
+  if (!p) return QMV_ERR_INVALID_ARG;
+  memset(p, 0, sizeof(*p));
+  p->magic = QMV_PACK_MAGIC;
+  p->N = N;
+  p->K = K;
+  p->bits = bits;
+  p->group = group;
+  p->G = K / group;
+  p->codes_bytes = (size_t)N * (size_t)K * (size_t)bits / 8;
+  p->scales_bytes = (size_t)N * (size_t)p->G * 2;
+  if (codes_bytes) *codes_bytes = p->codes_bytes;
+  if (scales_bytes) *scales_bytes = p->scales_bytes;
+  *out = p;
+  return QMV_OK;
+}
+
+int qmv_pack_weights(qmv_pack* p, const int8_t* d_codes_in, const uint16_t* d_scales_in,
+                     void* d_codes, void* d_scales, void* stream) {
+  if (!pack_ok(p) || !d_codes_in || !d_scales_in || !d_codes || !d_scales)
+    return QMV_ERR_INVALID_ARG;
+  if (!aligned(d_codes_in, 16) || !aligned(d_codes, 16) || !aligned(d_scales, 16) ||
+      !aligned(d_scales_in, 2))
+    return QMV_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t nwords = (int64_t)p->codes_bytes / 4;
+  cudaError_t e = qmv::launch_pack(p->bits, d_codes_in, (uint32_t*)d_codes, nwords, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemcpyAsync(d_scales, d_scales_in, p->scales_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  p->d_codes = (const uint32_t*)d_codes;
+  p->d_scales = (const uint16_t*)d_scales;
+  p->bound = 1;
+  return QMV_OK;
+}
+
+static int check_common(const qmv_pack* p, int M, const void* x, void* y, int y_dtype, int mode) {
+  if (!pack_ok(p) || !x || !y) return QMV_ERR_INVALID_ARG;
+  if (!p->bound) return QMV_ERR_INVALID_ARG;
+  if (M < 1 || M > 4096) return QMV_ERR_INVALID_ARG;
+  if (y_dtype != QMV_F32 && y_dtype != QMV_F16) return QMV_ERR_INVALID_ARG;
+  if (mode != QMV_FAST && mode != QMV_EXACT) return QMV_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 4)) return QMV_ERR_ALIGNMENT;
+  return QMV_OK;
+}
+
+static qmv::GemvArgs base_args(const qmv_pack* p, int M, const void* x, void* y, int y_dtype) {
+  qmv::GemvArgs a;
+  memset(&a, 0, sizeof(a));
+  a.codes = (const uint4*)p->d_codes;
+  a.scales = (const __half*)p->d_scales;
+  a.N = p->N;
+  a.K = p->K;
+  a.G = p->G;
+  a.row_u4 = (int)((int64_t)p->K * p->bits / 128);
+  a.perrow = (p->group == p->K && p->K != 32) ? 1 : 0;
+  a.x = (const __half*)x;
+  a.y = y;
+  a.y_f16 = (y_dtype == QMV_F16);
+  a.M = M;
+  return a;
+}
+
+// M columns through the CUDA-core kernels, 32 columns per launch above 32.
+static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s) {
+  cudaError_t err = cudaSuccess;
+  int rc;
+  if (a.M == 1) {
+    rc = qmv::launch_gemv_m1(a, bits, s, &err);
+    return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
+  }
+  const int M = a.M;
+  const size_t ysz = a.y_f16 ? 2 : 4;
+  for (int m0 = 0; m0 < M; m0 += 32) {
+    qmv::GemvArgs b = a;
+    b.M = (M - m0 < 32) ? (M - m0) : 32;
+    b.x = a.x + (int64_t)m0 * a.K;
+    if (a.r) b.r = a.r + (int64_t)m0 * a.K;
+    if (a.h_out) b.h_out = a.h_out + (int64_t)m0 * a.K;
+    b.y = (char*)a.y + (size_t)m0 * (size_t)a.N * ysz;
+    rc = qmv::launch_gemm_small(b, bits, s, &err);
+    if (rc != QMV_OK) return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
+  }
+  return QMV_OK;
+}
+
+int qmv_gemv(const qmv_pack* p, int M, int N, int K, int bits, int group, const void* x, void* y,
+             int y_dtype, int mode, void* stream) {
+  int rc = check_common(p, M, x, y, y_dtype, mode);
+  if (rc != QMV_OK) return rc;
+  if (N != p->N || K != p->K || bits != p->bits || group != p->group) return QMV_ERR_SHAPE;
+  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream);
+}
+
+int qmv_chunk_gemm(const qmv_pack* p, int M, const void* x, void* y, int y_dtype, int mode,
+                   void* stream) {
+  int rc = check_common(p, M, x, y, y_dtype, mode);
+  if (rc != QMV_OK) return rc;
+  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream);
+}
+
+int qmv_fused_rmsnorm_gemv(const qmv_pack* p, int M, const void* x, const void* residual,
+                           const void* gamma, float eps, void* h_out, void* y, int y_dtype,
+                           int mode, void* stream) {
+  int rc = check_common(p, M, x, y, y_dtype, mode);
+  if (rc != QMV_OK) return rc;
+  if (!residual || !gamma) return QMV_ERR_INVALID_ARG;
+  if (M > 32) return QMV_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f)) return QMV_ERR_INVALID_ARG;
+  if (!aligned(residual, 16) || !aligned(gamma, 16) || (h_out && !aligned(h_out, 16)))
+    return QMV_ERR_ALIGNMENT;
+  qmv::GemvArgs a = base_args(p, M, x, y, y_dtype);
+  a.fused = 1;
+  a.r = (const __half*)residual;
+  a.gamma = (const __half*)gamma;
+  a.eps = eps;
+  a.h_out = (__half*)h_out;
+  return run_cuda_core(a, p->bits, (cudaStream_t)stream);
+}
+
+int qmv_unpack_codes(const qmv_pack* p, int8_t* d_codes_out, void* stream) {
+  if (!pack_ok(p) || !p->bound || !d_codes_out) return QMV_ERR_INVALID_ARG;
+  if (!aligned(d_codes_out, 16)) return QMV_ERR_ALIGNMENT;
+  cudaError_t e = qmv::launch_unpack(p->bits, p->d_codes, d_codes_out,
+                                     (int64_t)p->codes_bytes / 4, (cudaStream_t)stream);
+  return e == cudaSuccess ? QMV_OK : cuda_fail(e);
+}
+
+int qmv_pack_info(const qmv_pack* p, int* N, int* K, int* bits, int* group) {
+  if (!pack_ok(p)) return QMV_ERR_INVALID_ARG;
+  if (N) *N = p->N;
+  if (K) *K = p->K;
+  if (bits) *bits = p->bits;
+  if (group) *group = p->group;
+  return QMV_OK;
+}
+
+int qmv_destroy_pack(qmv_pack* p) {
+  if (!pack_ok(p)) return QMV_ERR_INVALID_ARG;
+  p->magic = 0;
+  delete p;
+  return QMV_OK;
+}
+
+const char* qmv_status_string(int status) {
+  switch (status) {
+    case QMV_OK: return "ok";
+    case QMV_ERR_INVALID_ARG: return "invalid argument";
+    case QMV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case QMV_ERR_ALIGNMENT: return "pointer not aligned as required";
+    case QMV_ERR_SHAPE: return "shape does not match the pack or the layout rules";
+    case QMV_ERR_CUDA: return "CUDA error (see qmv_last_cuda_error)";
+    case QMV_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int qmv_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

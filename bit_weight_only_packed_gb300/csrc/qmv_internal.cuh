@@ -1,0 +1,55 @@
+// qmv_internal.cuh -- declarations shared by the library's translation units.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "qmv.h"
+#include "qmv_decode.cuh"
+
+#define QMV_PACK_MAGIC 0x514D5650u
+
+struct qmv_pack {
+  uint32_t magic;
+  int N, K, bits, group;
+  int G;                      // scales per row: K / group
+  size_t codes_bytes, scales_bytes;
+  const uint32_t* d_codes;    // bound by qmv_pack_weights
+  const uint16_t* d_scales;
+  int bound;
+};
+
+namespace qmv {
+
+// Arguments of one matvec launch (all device pointers).
+struct GemvArgs {
+  const uint4* codes;         // [N][row_u4] 16-byte units
+  const __half* scales;       // [N][G]
+  int N, K, G, row_u4;        // G = scales per row
+  int perrow;                 // one scale per row (group == K)
+  const __half* x;            // [M][K] activations (the normalised input when fused)
+  const __half* r;            // [M][K] residual (fused only)
+  const __half* gamma;        // [K] (fused only)
+  float eps;
+  __half* h_out;              // [M][K] nullable (fused only)
+  void* y;                    // [M][N] fp32 or fp16
+  int y_f16;
+  int M;                      // columns (tokens)
+  int fused;
+};
+
+struct DevInfo {
+  int sms;
+  int max_smem_optin;
+};
+const DevInfo& dev_info();   // of the current device (cached)
+
+cudaError_t launch_pack(int bits, const int8_t* in, uint32_t* out, int64_t nwords, cudaStream_t s);
+cudaError_t launch_unpack(int bits, const uint32_t* in, int8_t* out, int64_t nwords, cudaStream_t s);
+
+// Return a qmv_status; on QMV_ERR_CUDA, *err holds the CUDA error.
+int launch_gemv_m1(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+int launch_gemm_small(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+
+}  // namespace qmv

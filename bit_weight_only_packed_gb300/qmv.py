@@ -1,0 +1,194 @@
+"""Thin ctypes binding of the C ABI in include/qmv.h (libqmv.so).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the ABI.  torch is used for device memory and streams.  If the
+native library is missing the import of this module raises (there is no
+fallback of any kind).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libqmv.so")
+
+QMV_OK = 0
+QMV_ERR_INVALID_ARG = -1
+QMV_ERR_UNSUPPORTED = -2
+QMV_ERR_ALIGNMENT = -3
+QMV_ERR_SHAPE = -4
+QMV_ERR_CUDA = -5
+QMV_ERR_TIMEOUT = -6
+QMV_F32, QMV_F16 = 0, 1
+QMV_FAST, QMV_EXACT = 0, 1
+
+# every entry point declared in include/qmv.h, with its ctypes signature
+_P, _I, _F, _SZP = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.POINTER(ctypes.c_size_t)
+SIGNATURES = {
+    "qmv_create_pack": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _SZP, _SZP]),
+    "qmv_pack_weights": (_I, [_P, _P, _P, _P, _P, _P]),
+    "qmv_gemv": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P]),
+    "qmv_fused_rmsnorm_gemv": (_I, [_P, _I, _P, _P, _P, _F, _P, _P, _I, _I, _P]),
+    "qmv_chunk_gemm": (_I, [_P, _I, _P, _P, _I, _I, _P]),
+    "qmv_unpack_codes": (_I, [_P, _P, _P]),
+    "qmv_pack_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
+                           ctypes.POINTER(_I)]),
+    "qmv_destroy_pack": (_I, [_P]),
+    "qmv_status_string": (ctypes.c_char_p, [_I]),
+    "qmv_last_cuda_error": (_I, []),
+}
+
+
+class QmvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = _lib.qmv_status_string(status).decode()
+        if status == QMV_ERR_CUDA:
+            msg += f" (cudaError {_lib.qmv_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg} [{status}]")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libqmv.so is not built ({LIB_PATH}); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(fn: str, rc: int):
+    if rc != QMV_OK:
+        raise QmvError(fn, rc)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+class Pack:
+    """A packed weight matrix: the host descriptor plus the device buffers
+    (allocated with torch) that hold the packed codes and scales."""
+
+    def __init__(self, N: int, K: int, bits: int, group: int):
+        h = _P()
+        cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+        _check("qmv_create_pack", _lib.qmv_create_pack(ctypes.byref(h), N, K, bits, group,
+                                                        ctypes.byref(cb), ctypes.byref(sb)))
+        self.handle = h
+        self.N, self.K, self.bits, self.group = N, K, bits, group
+        self.codes_bytes, self.scales_bytes = cb.value, sb.value
+        self.words = None
+        self.scales = None
+
+    @property
+    def packed_bytes(self) -> int:
+        return self.codes_bytes + self.scales_bytes
+
+    def pack_weights(self, codes: torch.Tensor, scales: torch.Tensor, stream=None, device=None):
+        """codes: device int8 [N, K] signed codes; scales: device fp16 [N, K/group]."""
+        dev = codes.device if device is None else device
+        self.words = torch.empty(self.codes_bytes // 4, dtype=torch.int32, device=dev)
+        self.scales = torch.empty(self.scales_bytes // 2, dtype=torch.float16, device=dev)
+        qmv_pack_weights(self, codes, scales, self.words, self.scales, stream)
+        return self
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            _lib.qmv_destroy_pack(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def qmv_create_pack(N: int, K: int, bits: int, group: int) -> Pack:
+    return Pack(N, K, bits, group)
+
+
+def qmv_pack_weights(p: Pack, codes, scales, d_codes, d_scales, stream=None):
+    _check("qmv_pack_weights", _lib.qmv_pack_weights(
+        p.handle, _dptr(codes), _dptr(scales), _dptr(d_codes), _dptr(d_scales), _stream(stream)))
+
+
+def _out(y, M, N, y_dtype, like):
+    if y is None:
+        dt = torch.float16 if y_dtype == QMV_F16 else torch.float32
+        y = torch.empty((M, N), dtype=dt, device=like.device)
+    return y
+
+
+def qmv_gemv(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None, M=None):
+    M = x.shape[0] if (M is None and x.dim() == 2) else (M or 1)
+    y = _out(y, M, p.N, y_dtype, x)
+    _check("qmv_gemv", _lib.qmv_gemv(p.handle, M, p.N, p.K, p.bits, p.group, _dptr(x), _dptr(y),
+                                     y_dtype, mode, _stream(stream)))
+    return y
+
+
+def qmv_chunk_gemm(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None):
+    M = x.shape[0]
+    y = _out(y, M, p.N, y_dtype, x)
+    _check("qmv_chunk_gemm", _lib.qmv_chunk_gemm(p.handle, M, _dptr(x), _dptr(y), y_dtype, mode,
+                                                 _stream(stream)))
+    return y
+
+
+def qmv_fused_rmsnorm_gemv(p: Pack, x, residual, gamma, eps=1e-6, h_out=None, y=None,
+                           y_dtype=QMV_F32, mode=QMV_FAST, stream=None):
+    M = x.shape[0] if x.dim() == 2 else 1
+    y = _out(y, M, p.N, y_dtype, x)
+    _check("qmv_fused_rmsnorm_gemv", _lib.qmv_fused_rmsnorm_gemv(
+        p.handle, M, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out), _dptr(y),
+        y_dtype, mode, _stream(stream)))
+    return y
+
+
+def qmv_unpack_codes(p: Pack, out=None, stream=None):
+    if out is None:
+        out = torch.empty((p.N, p.K), dtype=torch.int8, device=p.words.device)
+    _check("qmv_unpack_codes", _lib.qmv_unpack_codes(p.handle, _dptr(out), _stream(stream)))
+    return out
+
+
+def qmv_pack_info(p: Pack):
+    n, k, b, g = _I(), _I(), _I(), _I()
+    _check("qmv_pack_info", _lib.qmv_pack_info(p.handle, ctypes.byref(n), ctypes.byref(k),
+                                               ctypes.byref(b), ctypes.byref(g)))
+    return n.value, k.value, b.value, g.value
+
+
+def qmv_status_string(status: int) -> str:
+    return _lib.qmv_status_string(status).decode()
+
+
+def qmv_last_cuda_error() -> int:
+    return _lib.qmv_last_cuda_error()

@@ -1,0 +1,178 @@
+/*
+ * qmv.h -- C ABI of the weight-only mixed-bit packed matvec library (GB300,
+ * sm_103a).
+ *
+ * y = W . x for weights stored as packed low-bit codes with fp16 scales,
+ * fp16 activations and fp32 accumulation, with an optional residual-add +
+ * RMSNorm folded into the matvec.  The method follows these pages:
+ *   [A19]  "Gemma4 raw-Metal loop on A19 -- findings + the remaining (parked)
+ *          levers", section "What moved the needle": int2 codes, 16 per 32-bit
+ *          word, exact products, fp32 sums in code order; q/k/v and gate/up
+ *          fused into single dispatches; residual-add + RMSNorm folded into
+ *          the next matvec's prologue; int8 weights loaded as vectors.
+ *   [PLAY] "raw-metal-loop-playbook", prefill-regimes table: chunks of M
+ *          tokens read the weights once per M tokens; M = 8/16 tiles keep each
+ *          output scalar's K-dot in the M = 1 order; M = 64/128 tiles use the
+ *          matrix units and change the order.
+ *
+ * Conventions (all entry points):
+ *   - Every pointer named d_* or described as "device" is a CUDA device
+ *     pointer owned by the caller.  The library allocates no device memory.
+ *   - fp16 values are IEEE binary16 bit patterns (uint16_t / __half).
+ *   - Matrices are row-major with no padding.  Activations are M x K (row m is
+ *     column m of the matvec, i.e. token m); outputs are M x N.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on it; nothing synchronises.
+ *   - Every call returns a qmv_status.  Arguments are validated on the host;
+ *     no call aborts, throws across the ABI or traps on the device.  A failed
+ *     launch returns QMV_ERR_CUDA and qmv_last_cuda_error() gives the raw
+ *     cudaError_t (thread-local).
+ *   - Packs are immutable after qmv_pack_weights, so concurrent calls that
+ *     share a pack are safe.
+ *
+ * Packed layout (the bit order is a reading: the pages give only "16 codes
+ * per word"): row n of codes is K*bits/32 little-endian uint32 words; code k
+ * sits in word floor(k*bits/32) at bit offset bits*(k mod (32/bits)); the
+ * field holds u = v + 2^(bits-1) for the signed code v, so int2 fields
+ * 0,1,2,3 decode to -2,-1,0,1.  Scales are fp16 [N][K/group].
+ *
+ * Accumulation order (both modes of the CUDA-core paths, M <= 32): for each
+ * output scalar, each block of 32 consecutive codes is summed serially in k
+ * in fp32 (products are exact); with group 32 the block sum is multiplied by
+ * its scale (rounded) and added to the accumulator (rounded), blocks in
+ * order; with one scale per row (group == K) the block sums are added
+ * serially and the total is multiplied by the scale once.  This is the
+ * oracle's order, so QMV_EXACT results are bit-identical to it, and every
+ * column of an M-tile is bit-identical to the M = 1 result.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QMV_API __attribute__((visibility("default")))
+#else
+#define QMV_API
+#endif
+
+typedef struct qmv_pack qmv_pack;   /* opaque host descriptor; owns no device memory */
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_ERR_INVALID_ARG = -1,   /* null pointer, bad enum value, M out of range */
+    QMV_ERR_UNSUPPORTED = -2,   /* valid but not implemented (e.g. a tile shape) */
+    QMV_ERR_ALIGNMENT = -3,     /* a pointer is not aligned as documented */
+    QMV_ERR_SHAPE = -4,         /* N/K/bits/group disagree with the pack or layout rules */
+    QMV_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
+    QMV_ERR_TIMEOUT = -6        /* a bounded device-side wait ran out */
+} qmv_status;
+
+typedef enum { QMV_F32 = 0, QMV_F16 = 1 } qmv_dtype;      /* output element type */
+typedef enum { QMV_FAST = 0, QMV_EXACT = 1 } qmv_mode;    /* accumulation mode */
+
+/*
+ * qmv_create_pack -- describe a packed weight matrix.  [A19] int2 item:
+ * 16 codes per word; int4 and int8 use the same offset-binary rule.
+ *   N, K   output and input features; K*bits/8 must be a multiple of 16
+ *          (K % 64 == 0 for int2, K % 32 == 0 for int4 and int8).
+ *   bits   2, 4 or 8.
+ *   group  32 (one fp16 scale per 32 consecutive k of a row) or K (one
+ *          scale per row).
+ *   codes_bytes, scales_bytes  (out, nullable) bytes the caller must allocate
+ *          for the packed codes (N*K*bits/8) and the scales (N*(K/group)*2).
+ * Errors: QMV_ERR_INVALID_ARG (out is NULL, bits/group not allowed),
+ * QMV_ERR_SHAPE (N < 1, K not allowed).  Host only; touches no device.
+ */
+QMV_API int qmv_create_pack(qmv_pack **out, int N, int K, int bits, int group,
+                    size_t *codes_bytes, size_t *scales_bytes);
+
+/*
+ * qmv_pack_weights -- pack signed codes on the device and bind the pack to
+ * the caller's buffers.  [A19] int2 item (16 codes per 32-bit word).
+ *   d_codes_in   device int8 [N][K], signed codes in [-2^(bits-1), 2^(bits-1)-1].
+ *                A code out of range is masked to its low `bits` bits.
+ *   d_scales_in  device fp16 [N][K/group].
+ *   d_codes      device, codes_bytes, 16-byte aligned: receives the words.
+ *   d_scales     device, scales_bytes, 16-byte aligned: receives a copy of
+ *                the scales.
+ * The pack keeps d_codes/d_scales; they must outlive every later call that
+ * uses the pack.  Errors: INVALID_ARG (NULL), ALIGNMENT, CUDA.
+ */
+QMV_API int qmv_pack_weights(qmv_pack *p, const int8_t *d_codes_in, const uint16_t *d_scales_in,
+                     void *d_codes, void *d_scales, void *stream);
+
+/*
+ * qmv_gemv -- y = x . W^T for M columns: y[m][n] = sum_g (sum_{k in g}
+ * x[m][k] * v[n][k]) * s[n][g] in the order stated at the top of this file.
+ * [A19] int2 item (exact products, fp32 in code order); [PLAY] K-order-fixed
+ * row for M <= 16 and matrix-unit row for M >= 64.
+ *   M            1 .. 4096.  M <= 32 runs the CUDA-core kernels (bit-exact
+ *                in both modes); M > 32 with QMV_FAST runs tcgen05 tensor-core
+ *                tiles (fp32 accumulate, hardware order); M > 32 with
+ *                QMV_EXACT runs the CUDA-core kernels 32 columns at a time.
+ *   N, K, bits, group  must equal the pack's (QMV_ERR_SHAPE otherwise).
+ *   x            device fp16 [M][K], 16-byte aligned.
+ *   y            device [M][N] of y_dtype (fp32, or fp16 = RNE of the fp32
+ *                result), 4-byte aligned.
+ *   mode         QMV_FAST or QMV_EXACT.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, CUDA.
+ */
+QMV_API int qmv_gemv(const qmv_pack *p, int M, int N, int K, int bits, int group,
+             const void *x, void *y, int y_dtype, int mode, void *stream);
+
+/*
+ * qmv_fused_rmsnorm_gemv -- residual add + RMSNorm folded into the matvec
+ * prologue ([A19] dispatch-count fusion item).  For each column m:
+ *   h = fp16(x + residual); ss = sum of h*h (serial in blocks of 32, then
+ *   serial over blocks); inv = 1/sqrt(ss/K + eps) (IEEE fp32 ops);
+ *   y16 = fp16((h * inv) * gamma); then y = matvec(y16) as qmv_gemv.
+ *   x, residual  device fp16 [M][K]; gamma device fp16 [K]; 16-byte aligned.
+ *   h_out        nullable device fp16 [M][K]: receives h (the next residual).
+ *   M            1 .. 32.
+ * Errors: as qmv_gemv; M > 32 gives QMV_ERR_UNSUPPORTED.
+ */
+QMV_API int qmv_fused_rmsnorm_gemv(const qmv_pack *p, int M, const void *x, const void *residual,
+                           const void *gamma, float eps, void *h_out, void *y,
+                           int y_dtype, int mode, void *stream);
+
+/*
+ * qmv_chunk_gemm -- a prefill chunk of M tokens against one pack ([PLAY]
+ * prefill-regimes table): the same computation as qmv_gemv with the pack's
+ * own N, K, bits and group.  M = 4, 8, 16 (and any M <= 32) use the
+ * K-order-fixed CUDA-core tiles; M = 64, 128 (any M > 32) in QMV_FAST use
+ * tcgen05 tensor-core tiles.
+ */
+QMV_API int qmv_chunk_gemm(const qmv_pack *p, int M, const void *x, void *y, int y_dtype,
+                   int mode, void *stream);
+
+/*
+ * qmv_unpack_codes -- decode the packed words back to signed int8 codes
+ * [N][K] with the same decode routine the matvec kernels use (a check of
+ * that routine; not on the hot path).  d_codes_out: device int8, N*K bytes.
+ */
+QMV_API int qmv_unpack_codes(const qmv_pack *p, int8_t *d_codes_out, void *stream);
+
+/* qmv_pack_info -- read back a pack's shape (any out pointer may be NULL). */
+QMV_API int qmv_pack_info(const qmv_pack *p, int *N, int *K, int *bits, int *group);
+
+/* qmv_destroy_pack -- free the host descriptor (never the device buffers). */
+QMV_API int qmv_destroy_pack(qmv_pack *p);
+
+/* qmv_status_string -- static text for a status code. */
+QMV_API const char *qmv_status_string(int status);
+
+/* qmv_last_cuda_error -- the raw cudaError_t behind the calling thread's
+ * last QMV_ERR_CUDA (0 if none). */
+QMV_API int qmv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */
