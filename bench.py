@@ -1,0 +1,442 @@
+"""Benchmark: effective HBM GB/s of the weight-only mixed-bit decode matvecs.
+
+Workload (one "step"): one synthetic decode layer at M = 1, d_model 2048 --
+  residual-add + RMSNorm fused into the q/k/v matvec  (int4, 2560 x 2048, group 32)
+  o_proj                                             (int4, 2048 x 2048, group 32)
+  residual-add + RMSNorm fused into gate/up          (int2, 16384 x 2048, group 32)
+  down                                               (int2, 2048 x 8192, group 32)
+= 21,037,056 packed bytes (codes + fp16 scales) per layer, 4 kernel launches.
+`--layers L` distinct layers are resident (default 32, 673 MB, > 5x L2) and
+the steps walk through them in turn, so every step reads its weights from
+HBM (inputs larger than L2; no flush needed).
+
+value = packed bytes of all timed steps / device time (CUDA events on the
+launch stream), i.e. effective GB/s; `tok_per_s_equiv` = layers per second.
+`e2e` is the same metric with the step's activations copied host->device from
+pinned memory and the outputs read back inside the timed region.
+
+`--impl reference` times the CPU oracle (single-threaded C, the definition
+the GPU path is checked against) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+D_MODEL, D_FF = 2048, 8192
+LAYER = [  # name, N, K, bits, group, fused prologue
+    ("qkv", 2560, D_MODEL, 4, 32, True),
+    ("o", D_MODEL, D_MODEL, 4, 32, False),
+    ("gateup", 2 * D_FF, D_MODEL, 2, 32, True),
+    ("down", D_MODEL, D_FF, 2, 32, False),
+]
+DOMINANT = "gateup"
+METRIC = "effective HBM GB/s (% of GB300 peak) and equiv. decode tok/s per weight set"
+SEED = 20261202
+
+
+def packed_bytes(N, K, bits, group):
+    return N * K * bits // 8 + N * (K // group) * 2
+
+
+LAYER_BYTES = sum(packed_bytes(N, K, b, g) for _, N, K, b, g, _ in LAYER)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    import torch
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return rank, ws, local
+
+
+def reduce_max(v: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return v
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    def __init__(self):
+        self.p = None
+        self.path = os.path.join("/tmp", f"qmv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                       "-lms", "100", "-i", str(self.idx())],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    @staticmethod
+    def idx():
+        import torch
+        return torch.cuda.current_device()
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.close()
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+def build_layers(L, dev):
+    import torch
+
+    import synth
+    from bit_weight_only_packed_gb300 import qmv
+    layers = []
+    for li in range(L):
+        lay = {}
+        for name, N, K, bits, group, fused in LAYER:
+            codes = synth.codes(SEED, f"L{li}.{name}", N, K, bits, device=dev)
+            scales = synth.scales(SEED, f"L{li}.{name}", N, K // group, device=dev)
+            lay[name] = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
+            del codes, scales
+        layers.append(lay)
+    torch.cuda.synchronize()
+    return layers
+
+
+def host_inputs():
+    import synth
+    x = synth.normal_f16(SEED, "bench.x", (1, D_MODEL))
+    r = synth.normal_f16(SEED, "bench.r", (1, D_MODEL))
+    g1 = synth.normal_f16(SEED, "bench.g1", (D_MODEL,), mean=1.0, std=0.1)
+    g2 = synth.normal_f16(SEED, "bench.g2", (D_MODEL,), mean=1.0, std=0.1)
+    attn = synth.normal_f16(SEED, "bench.attn", (1, D_MODEL))
+    act = synth.normal_f16(SEED, "bench.act", (1, D_FF))
+    return dict(x=x, r=r, g1=g1, g2=g2, attn=attn, act=act)
+
+
+def run_layer(qmv, lay, b, stream):
+    """One decode layer: 4 launches on `stream`."""
+    qmv.qmv_fused_rmsnorm_gemv(lay["qkv"], b["x"], b["r"], b["g1"], 1e-6, h_out=b["h"],
+                               y=b["y_qkv"], mode=qmv.QMV_FAST, stream=stream)
+    qmv.qmv_gemv(lay["o"], b["attn"], y=b["y_o"], mode=qmv.QMV_FAST, stream=stream)
+    qmv.qmv_fused_rmsnorm_gemv(lay["gateup"], b["attn"], b["h"], b["g2"], 1e-6, h_out=b["h2"],
+                               y=b["y_gu"], mode=qmv.QMV_FAST, stream=stream)
+    qmv.qmv_gemv(lay["down"], b["act"], y=b["y_down"], mode=qmv.QMV_FAST, stream=stream)
+
+
+def gpu_arm(args, rank, world, local):
+    import torch
+
+    from bit_weight_only_packed_gb300 import qmv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    L = args.layers
+    layers = build_layers(L, dev)
+    hin = host_inputs()
+    b = {k: torch.from_numpy(v).to(dev) for k, v in hin.items()}
+    b["h"] = torch.empty(1, D_MODEL, dtype=torch.float16, device=dev)
+    b["h2"] = torch.empty(1, D_MODEL, dtype=torch.float16, device=dev)
+    b["y_qkv"] = torch.empty(1, 2560, device=dev)
+    b["y_o"] = torch.empty(1, D_MODEL, device=dev)
+    b["y_gu"] = torch.empty(1, 2 * D_FF, device=dev)
+    b["y_down"] = torch.empty(1, D_MODEL, device=dev)
+    K, W = args.steps, args.warmup
+
+    # warm-up through the plain API (first calls set kernel attributes)
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            run_layer(qmv, layers[i % L], b, stream)
+    torch.cuda.synchronize()
+
+    # CUDA graphs remove the per-launch host cost: one graph per layer (a
+    # step) and one graph of all L layers (L steps); the dominant kernel
+    # alone over the L layers is a third graph, timed on its own.
+    g_one = []
+    for li in range(L):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run_layer(qmv, layers[li], b, stream)
+        g_one.append(g)
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for li in range(L):
+            run_layer(qmv, layers[li], b, stream)
+    g_dom = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dom, stream=stream):
+        for li in range(L):
+            qmv.qmv_fused_rmsnorm_gemv(layers[li]["gateup"], b["attn"], b["h"], b["g2"], 1e-6,
+                                       h_out=b["h2"], y=b["y_gu"], mode=qmv.QMV_FAST,
+                                       stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g_all.replay()
+            g_dom.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps, device time ----
+    clocks = Clocks()
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(K // L):
+            g_all.replay()
+        for li in range(K % L):
+            g_one[li].replay()
+        t1.record(stream)
+        # the dominant kernel's own launches, same rotation over L layers
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        reps = max(1, K // L)
+        d0.record(stream)
+        for _ in range(reps):
+            g_dom.replay()
+        d1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ck = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    dom_ms = d0.elapsed_time(d1) / (reps * L)
+    ms_max = reduce_max(ms)
+
+    # ---- end to end through the public API: pinned host -> device -> host ----
+    pin = {k: torch.from_numpy(v).pin_memory() for k, v in hin.items()}
+    outs = {k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory()
+            for k in ("y_qkv", "y_o", "y_gu", "y_down", "h2")}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    KE = max(3, K // 2)
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(KE):
+            for k, v in pin.items():
+                b[k].copy_(v, non_blocking=True)
+            run_layer(qmv, layers[i % L], b, stream)
+            for k, v in outs.items():
+                v.copy_(b[k], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1))
+    barrier()
+
+    peak, peak_kind = peaks()
+    gbs = world * LAYER_BYTES * K / (ms_max * 1e-3) / 1e9
+    dom_bytes = packed_bytes(2 * D_FF, D_MODEL, 2, 32)
+    dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            traffic = json.load(open(tr_path)).get("gemv_m1_fused_int2_16384x2048")
+        except Exception:
+            traffic = None
+    out = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_max / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int2/int4 codes, fp16 act, f32 accum",
+        "data": "synthetic (seeded SplitMix64 codes/scales, Box-Muller fp16 activations)",
+        "config": {"workload": "synthetic decode layer, M=1, d_model 2048, d_ff 8192: "
+                               "fused RMSNorm+qkv int4 2560x2048, o int4 2048x2048, "
+                               "fused RMSNorm+gate/up int2 16384x2048, down int2 2048x8192",
+                   "layer_bytes": LAYER_BYTES, "resident_layers": L,
+                   "resident_bytes": LAYER_BYTES * L,
+                   "l2": "inputs larger than L2 (distinct layer weights rotated per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": round(100.0 * gbs / world / peak, 1),
+        "tok_per_s_equiv": round(world * K / (ms_max * 1e-3), 1),
+        "gpu_launches": 4 * K,
+        "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "traffic": traffic,
+                     "kernel": "gemv_m1 fused RMSNorm + int2 gate/up 16384x2048",
+                     "algorithmic_bytes": dom_bytes, "peak_source": peak_kind},
+        "e2e": {"value": round(world * LAYER_BYTES * KE / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": ck,
+    }
+    return out
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_sample(frac_rows: int):
+    """Host inputs of one layer, restricted to every `frac_rows`-th row."""
+    import synth
+    hin = host_inputs()
+    mats = {}
+    for name, N, K, bits, group, fused in LAYER:
+        rows = np.arange(0, N, frac_rows)
+        codes = synth.codes(SEED, f"L0.{name}", N, K, bits, rows=rows).numpy()
+        scales = synth.scales(SEED, f"L0.{name}", N, K // group, rows=rows).numpy()
+        mats[name] = (codes, scales, group, fused, packed_bytes(len(rows), K, bits, group))
+    return hin, mats
+
+
+def oracle_layer(oracle, hin, mats):
+    x, r, g1, g2, attn, act = (hin[k] for k in ("x", "r", "g1", "g2", "attn", "act"))
+    c, s, g, _, _ = mats["qkv"]
+    h, _, _ = oracle.fused_rmsnorm_gemv(c, s, g, x, r, g1)
+    c, s, g, _, _ = mats["o"]
+    oracle.gemv(c, s, g, attn)
+    c, s, g, _, _ = mats["gateup"]
+    oracle.fused_rmsnorm_gemv(c, s, g, attn, h, g2)
+    c, s, g, _, _ = mats["down"]
+    oracle.gemv(c, s, g, act)
+
+
+def cpu_baseline(budget_s: float = 10.0, frac_rows: int = 4):
+    import oracle
+    oracle.build()
+    hin, mats = oracle_sample(frac_rows)
+    sample_bytes = sum(m[4] for m in mats.values())
+    oracle_layer(oracle, hin, mats)          # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_layer(oracle, hin, mats)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= 200:
+            break
+    return {"value": round(sample_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"every {frac_rows}th row of each matrix of one decode layer "
+                      f"({sample_bytes} packed bytes) x {n} passes, fused prologues included, "
+                      f"single-threaded C"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    frac = 16
+    hin, mats = oracle_sample(frac)
+    sample_bytes = sum(m[4] for m in mats.values())
+    for _ in range(args.warmup):
+        oracle_layer(oracle, hin, mats)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_layer(oracle, hin, mats)
+    dt = time.perf_counter() - t0
+    v = round(sample_bytes * args.steps / dt / 1e9, 4)
+    sample = (f"every {frac}th row of each matrix of one decode layer ({sample_bytes} packed bytes) "
+              f"per step, fused prologues included, single-threaded C")
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int2/int4 codes, fp16 act, f32 accum", "data": "synthetic",
+        "config": {"workload": "synthetic decode layer, M=1, d_model 2048, d_ff 8192 (row sample)"},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        out = reference_arm(args, rank, world)
+        if rank == 0:
+            print(json.dumps(out))
+        return
+    rank, world, local = dist_init()
+    out = gpu_arm(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            out["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -429,10 +429,41 @@ __global__ void __launch_bounds__(256) gemm_small_kernel(GemvArgs a) {
 
 // ============================================================ launchers ====
 
+// Per-kernel launch facts, cached per device: the dynamic shared-memory limit
+// set so far and the occupancy for one (threads, smem) shape.  This keeps the
+// host cost of a call to a few lookups after the first call.
+struct KernCache {
+  int dev = -1;
+  size_t smem_set = 48 * 1024;
+  int occ_threads = -1;
+  size_t occ_smem = 0;
+  int occ = 0;
+};
+
 template <typename Kern>
-static cudaError_t ensure_smem(Kern k, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+static cudaError_t prep_kernel(Kern k, KernCache& c, int threads, size_t smem, int* occ) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (c.dev != dev) {
+    c = KernCache();
+    c.dev = dev;
+  }
+  if (smem > c.smem_set) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    c.smem_set = smem;
+  }
+  if (occ) {
+    if (c.occ_threads != threads || c.occ_smem != smem) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, threads, smem);
+      if (e != cudaSuccess) return e;
+      c.occ_threads = threads;
+      c.occ_smem = smem;
+    }
+    *occ = c.occ;
+  }
+  return cudaSuccess;
 }
 
 template <int BITS, bool PERROW, bool FUSED, int MAXT>
@@ -445,10 +476,9 @@ static int run_m1_t(const GemvArgs& a, int C, int RP, cudaStream_t s, cudaError_
   const DevInfo& d = dev_info();
   if (smem > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
   auto kern = gemv_m1_kernel<BITS, PERROW, FUSED, MAXT>;
-  cudaError_t e = ensure_smem(kern, smem);
-  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  static thread_local KernCache cache;
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, T, smem);
+  cudaError_t e = prep_kernel(kern, cache, T, smem, &occ);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   if (occ < 1) return QMV_ERR_UNSUPPORTED;
   int64_t grid = (int64_t)d.sms * occ;
@@ -497,7 +527,8 @@ static int run_small(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   const DevInfo& d = dev_info();
   if (smem > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
   auto kern = gemm_small_kernel<BITS, MT>;
-  cudaError_t e = ensure_smem(kern, smem);
+  static thread_local KernCache cache;
+  cudaError_t e = prep_kernel(kern, cache, 256, smem, nullptr);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   const int64_t grid = ((int64_t)a.N + 31) / 32;
   kern<<<(unsigned)grid, 256, smem, s>>>(a);
