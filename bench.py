@@ -208,6 +208,8 @@ def gpu_arm(args, rank, world, local):
     b["y_down"] = torch.empty(1, D_MODEL, device=dev)
     K, W = args.steps, args.warmup
 
+    # dependent matvecs overlap through programmatic dependent launch
+    qmv.qmv_set_pdl(True)
     # warm-up through the plain API (first calls set kernel attributes)
     with torch.cuda.stream(stream):
         for i in range(W):

@@ -27,6 +27,10 @@ bool shape_ok(int K, int bits) {
 
 namespace qmv {
 
+static thread_local bool g_pdl = false;
+bool pdl_enabled() { return g_pdl; }
+void set_pdl(bool on) { g_pdl = on; }
+
 const DevInfo& dev_info() {
   static thread_local int cached_dev = -1;
   static thread_local DevInfo info{152, 227 * 1024};
@@ -123,7 +127,8 @@ static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
   int rc;
   if (a.M == 1) {
-    rc = qmv::launch_gemv_m1(a, bits, s, &err);
+    rc = qmv::launch_gemv_tma(a, bits, s, &err);
+    if (rc == QMV_ERR_UNSUPPORTED) rc = qmv::launch_gemv_m1(a, bits, s, &err);
     return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
   }
   const int M = a.M;
@@ -213,5 +218,17 @@ const char* qmv_status_string(int status) {
 }
 
 int qmv_last_cuda_error(void) { return g_last_cuda_error; }
+
+int qmv_set_pdl(int enable) {
+  qmv::set_pdl(enable != 0);
+  return QMV_OK;
+}
+
+int qmv_device_error(int* out, int clear) {
+  if (!out) return QMV_ERR_INVALID_ARG;
+  const int e = qmv::read_device_error(clear, out);
+  if (e != 0) return cuda_fail((cudaError_t)e);
+  return QMV_OK;
+}
 
 }  // extern "C"

@@ -51,5 +51,13 @@ cudaError_t launch_unpack(int bits, const uint32_t* in, int8_t* out, int64_t nwo
 // Return a qmv_status; on QMV_ERR_CUDA, *err holds the CUDA error.
 int launch_gemv_m1(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
 int launch_gemm_small(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+// M = 1 through the bulk-copy pipeline; QMV_ERR_UNSUPPORTED if the shape does
+// not fit it (the caller then uses launch_gemv_m1).
+int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+// Programmatic dependent launch of the M = 1 kernels (off by default).
+bool pdl_enabled();
+void set_pdl(bool on);
+// Read (and optionally clear) the device error word set by bounded waits.
+int read_device_error(int clear, int* out);
 
 }  // namespace qmv

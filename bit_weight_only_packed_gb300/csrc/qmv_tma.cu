@@ -1,0 +1,597 @@
+// qmv_tma.cu -- the M = 1 matvec as a warp-specialised pipeline (GB300).
+//
+// What it computes is exactly what the CUDA-core kernels compute (and the
+// oracle): per output row, each 32-code block summed serially in k in fp32
+// with exact products, scaled (group 32), and folded serially over blocks
+// ("Gemma4 raw-Metal loop on A19", section "What moved the needle": int2 at
+// 16 codes per word, exact products, fp32 in code order; the residual-add +
+// RMSNorm fold into the matvec prologue).
+//
+// How:
+//   * Rows are processed in groups of R rows.  A group's codes (and its
+//     group-32 scales) are contiguous in memory, so one producer thread moves
+//     each group into a ring of NS shared-memory stages with two
+//     cp.async.bulk copies completing on the stage's "full" mbarrier.  The
+//     producer runs ahead of the math by up to NS groups (tens of KB in
+//     flight per SM) and starts before the prologue, since weights do not
+//     depend on the activations.
+//   * Compute warps: thread t owns one 64-code item (two 32-code blocks) of
+//     RP rows in parallel, U rows after another, and keeps that item's 64
+//     activations in registers as fp32 pairs (y_k, y_{32+k}).  A code field
+//     is turned into fp32 exactly by one LOP3: (w & (mask << o)) | 0x4B000000
+//     = 2^23 + u*2^o (every field is first brought below bit 16: the low and
+//     high halves of a word use the same o).  One packed sub.rn.f32x2 maps
+//     the pair (block 0, block 1) to v*2^o exactly, and one fma.rn.f32x2 with
+//     the activations pre-scaled by 2^-o advances both blocks' serial sums
+//     (y*2^-o times v*2^o is y*v exactly).  About 2 instructions per code.
+//   * Block sums (scaled) go to a double-buffered fold buffer; a dedicated
+//     fold warp adds them serially per row (one lane per row) and writes y,
+//     so the compute warps never wait at a CTA-wide barrier.
+//   * Every mbarrier wait is bounded; on timeout the kernel records an error
+//     code in the device error word, stops issuing, lets its own copies land
+//     and returns.
+#include "qmv_internal.cuh"
+
+namespace qmv {
+
+__device__ int g_qmv_error = 0;
+
+namespace {
+
+constexpr int NS = 4;                      // ring stages
+constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (~0.5 s each)
+constexpr int ERR_TIMEOUT_FULL = 1, ERR_TIMEOUT_EMPTY = 2, ERR_TIMEOUT_TFULL = 3,
+              ERR_TIMEOUT_TEMPTY = 4;
+
+typedef unsigned long long u64;
+
+__device__ __forceinline__ uint32_t sa(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(tx)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait.  Returns false (after setting the CTA's abort flag and the
+// device error word) if the phase does not complete in SPIN_LIMIT tries, or
+// at once if another warp of the CTA has aborted.
+__device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                       int code) {
+  for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (i > 16) __nanosleep(100);
+  }
+  *abort_flag = 1;
+  atomicCAS(&g_qmv_error, 0, code);
+  return false;
+}
+
+// Bounded wait that ignores the abort flag (used to let copies land).
+__device__ __noinline__ void mbar_drain(uint64_t* b, uint32_t parity) {
+  for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
+    if (mbar_try(b, parity)) return;
+    __nanosleep(100);
+  }
+  atomicCAS(&g_qmv_error, 0, ERR_TIMEOUT_FULL);
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          sa(dst)),
+      "l"(src), "r"(bytes), "r"(sa(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ u64 pk(float a, float b) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ u64 pku(uint32_t a, uint32_t b) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(u64 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+// d = a*b + c on two fp32 lanes, each lane rounded once
+__device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// Store 8 consecutive fp16 activations starting at element e0 (a multiple of
+// 8) as fp32 into the pair layout: element 64*c + 32*h + k goes to
+// y2f[2*(k*C + c) + h].
+template <int BITS>
+__device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32_t (&h8)[4]) {
+  constexpr int CPW = 32 / BITS, HALF = CPW / 2;
+  const int c = e0 >> 6, h = (e0 >> 5) & 1, k0 = e0 & 31;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int k = k0 + e;
+    const int o = BITS * ((k % CPW) % HALF);
+    const __half2 v = u32_as_h2(h8[e >> 1]);
+    const float f = (e & 1) ? __high2float(v) : __low2float(v);
+    y2f[2 * (k * C + c) + h] = __fmul_rn(f, pow2f(-o));
+  }
+}
+
+// v' = ((a & m) | 0x4B000000, (b & m) | 0x4B000000) - off on two fp32 lanes.
+// With m = (2^bits - 1) << o the magic float is 2^23 + u*2^o exactly, and
+// off = 2^23 + 2^(bits-1)*2^o, so v' = (u - 2^(bits-1)) * 2^o = v * 2^o
+// exactly.  Both LOP3s write the halves of one register pair that the paired
+// add reads.
+__device__ __forceinline__ u64 decode2(uint32_t a, uint32_t b, uint32_t m, u64 off) {
+  u64 v;
+  asm("{\n\t.reg .b32 t0, t1;\n\t.reg .b64 t;\n\t"
+      "lop3.b32 t0, %1, %3, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 t1, %2, %3, 0x4B000000, 0xEA;\n\t"
+      "mov.b64 t, {t0, t1};\n\t"
+      "sub.rn.f32x2 %0, t, %4;\n\t}"
+      : "=l"(v)
+      : "r"(a), "r"(b), "r"(m), "l"(off));
+  return v;
+}
+
+// Both blocks of one 64-code item, for U rows at once.  w[u][0 .. 2*WPB-1]:
+// words of block 0 then block 1.  y2s: activation pairs (y'_k, y'_{32+k}) of
+// all items, laid out [k][item] so that consecutive threads read consecutive
+// 8-byte pairs; one pair serves all U rows.  y'_k = y_k * 2^-o(k) where o(k)
+// is the bit offset the code k is decoded at, so y'_k * (v_k * 2^o(k)) =
+// y_k * v_k exactly (powers of two; no underflow for fp16 inputs).  acc[u] =
+// (p0, p1) are the two blocks' serial sums.  Fields in the high 16-bit half
+// of a word are first shifted down by 16, so every field is masked below
+// bit 16.
+template <int BITS, int U>
+__device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32],
+                                          const u64* __restrict__ y2s, int C, int c,
+                                          u64 (&acc)[U]) {
+  constexpr int CPW = 32 / BITS;   // codes per word
+  constexpr int HALF = CPW / 2;    // codes per 16-bit half
+  constexpr int WPB = 32 / CPW;    // words per block
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+#pragma unroll
+  for (int wi = 0; wi < WPB; ++wi) {
+    uint32_t h0[U], h1[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      h0[u] = w[u][wi] >> 16;
+      h1[u] = w[u][WPB + wi] >> 16;
+    }
+#pragma unroll
+    for (int j = 0; j < CPW; ++j) {
+      const int o = BITS * (j % HALF);
+      const float offf = pow2f(23) + (float)(1 << (BITS - 1 + o));
+      const u64 off = pk(offf, offf);
+      const u64 y = y2s[(wi * CPW + j) * C + c];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t a = (j < HALF) ? w[u][wi] : h0[u];
+        const uint32_t b = (j < HALF) ? w[u][WPB + wi] : h1[u];
+        const u64 v = decode2(a, b, MASK << o, off);
+        acc[u] = ffma2(y, v, acc[u]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// Launch plan (host computes it; the kernel reads it).
+struct TmaPlan {
+  int C;             // 64-code items per row
+  int RP;            // rows in parallel (threads per row group = C*RP <= Tc)
+  int R;             // rows per group = RP*U
+  int Tc;            // compute threads (multiple of 32)
+  int row_bytes;     // code bytes per row
+  int sc_row;        // scale bytes per row inside a stage (0 with one scale per row)
+  int stage_bytes;   // R*(row_bytes + sc_row)
+  int ngroups;       // ceil(N / R)
+  int y_off, stage_off, tbuf_off;   // shared-memory offsets (bytes)
+};
+
+__host__ __device__ inline int tma_round16(int x) { return (x + 15) & ~15; }
+
+template <int BITS, bool PERROW, bool FUSED, int U, int MAXT>
+__global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(GemvArgs a, TmaPlan P) {
+  constexpr int IW = 64 * BITS / 32;   // words per item
+  extern __shared__ __align__(128) unsigned char sm[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm);
+  uint64_t* empty = full + NS;
+  uint64_t* tfull = empty + NS;
+  uint64_t* tempty = tfull + 2;
+  volatile int* abort_f = reinterpret_cast<volatile int*>(sm + 96);
+  float* inv_sh = reinterpret_cast<float*>(sm + 100);
+  float* y2f = reinterpret_cast<float*>(sm + P.y_off);   // pairs [k][item] as fp32
+  unsigned char* stages = sm + P.stage_off;
+  float* tbuf = reinterpret_cast<float*>(sm + P.tbuf_off);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = a.K, NB = K / 32, GS = NB + 1, R = P.R;
+  const int my_groups = (blockIdx.x < (unsigned)P.ngroups)
+                            ? (P.ngroups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                            : 0;
+
+  // Programmatic dependent launch (a no-op when the launch did not ask for
+  // it): let the next kernel in the stream be scheduled as soon as SMs free
+  // up; its weight copies then overlap this kernel's tail.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], P.Tc);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], P.Tc);
+      mbar_init(&tempty[b], 32);
+    }
+    *abort_f = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ producer --
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < my_groups; ++i) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY)) break;
+        if (*abort_f) break;
+        const int64_t g = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
+        const int64_t r0 = g * R;
+        const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
+        const uint32_t cb = (uint32_t)rows * P.row_bytes;
+        const uint32_t sb = PERROW ? 0u : (uint32_t)rows * P.sc_row;
+        unsigned char* st = stages + (size_t)s * P.stage_bytes;
+        mbar_arrive_tx(&full[s], cb + sb);
+        bulk_g2s(st, reinterpret_cast<const unsigned char*>(a.codes) + r0 * P.row_bytes, cb, &full[s]);
+        if (!PERROW)
+          bulk_g2s(st + (size_t)R * P.row_bytes,
+                   reinterpret_cast<const unsigned char*>(a.scales) + r0 * P.sc_row, sb, &full[s]);
+        ++issued;
+      }
+      // let every copy this thread issued land before the CTA can exit
+      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
+        mbar_drain(&full[j % NS], (j / NS) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------------------- prologue (warps 1 .. end) --
+  // Activations, residual and gamma may come from the previous kernel, and
+  // the outputs may still be read by it: wait for it to complete (no-op
+  // without a programmatic launch).  The producer above never waits: packed
+  // weights are not written by the kernels a matvec overlaps.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tt = threadIdx.x - 32;        // 0 .. 32 + Tc - 1
+  const int nt = 32 + P.Tc;
+  if (FUSED) {
+    float* bsum = tbuf;                   // the fold buffer is free until the main loop
+    __half* h_out = (blockIdx.x == 0) ? a.h_out : nullptr;
+    for (int b = tt; b < NB; b += nt) {
+      float blk = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 32 * b + 8 * q));
+        const uint4 rv = __ldg(reinterpret_cast<const uint4*>(a.r + 32 * b + 8 * q));
+        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
+        uint32_t hs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half2 xx = u32_as_h2(xs[e]), rr = u32_as_h2(rs[e]);
+          const __half lo = __float2half_rn(__fadd_rn(__low2float(xx), __low2float(rr)));
+          const __half hi = __float2half_rn(__fadd_rn(__high2float(xx), __high2float(rr)));
+          const float fl = __half2float(lo), fh = __half2float(hi);
+          blk = __fmaf_rn(fl, fl, blk);
+          blk = __fmaf_rn(fh, fh, blk);
+          hs[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        }
+        if (h_out)
+          *reinterpret_cast<uint4*>(h_out + 32 * b + 8 * q) = make_uint4(hs[0], hs[1], hs[2], hs[3]);
+      }
+      bsum[b] = blk;
+    }
+    named_bar(1, nt);
+    if (tt == 0) {
+      float ss = 0.0f;
+      for (int b = 0; b < NB; ++b) ss = __fadd_rn(ss, bsum[b]);
+      const float mean = __fdiv_rn(ss, (float)K);
+      *inv_sh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
+    }
+    named_bar(1, nt);
+    const float inv = *inv_sh;
+    for (int v8 = tt; v8 < K / 8; v8 += nt) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 8 * v8));
+      const uint4 rv = __ldg(reinterpret_cast<const uint4*>(a.r + 8 * v8));
+      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + 8 * v8));
+      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w},
+                     gs[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t ys[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __half2 xx = u32_as_h2(xs[e]), rr = u32_as_h2(rs[e]), gg = u32_as_h2(gs[e]);
+        const float hl = __half2float(__float2half_rn(__fadd_rn(__low2float(xx), __low2float(rr))));
+        const float hh = __half2float(__float2half_rn(__fadd_rn(__high2float(xx), __high2float(rr))));
+        const __half yl = __float2half_rn(__fmul_rn(__fmul_rn(hl, inv), __low2float(gg)));
+        const __half yh = __float2half_rn(__fmul_rn(__fmul_rn(hh, inv), __high2float(gg)));
+        ys[e] = (uint32_t)__half_as_ushort(yl) | ((uint32_t)__half_as_ushort(yh) << 16);
+      }
+      store_y8<BITS>(y2f, P.C, 8 * v8, ys);
+    }
+  } else {
+    for (int v8 = tt; v8 < K / 8; v8 += nt) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 8 * v8));
+      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+      store_y8<BITS>(y2f, P.C, 8 * v8, xs);
+    }
+  }
+  named_bar(1, nt);
+
+  // ---------------------------------------------------------- fold warp --
+  if (warp == 1) {
+    for (int i = 0; i < my_groups; ++i) {
+      const int tb = i & 1;
+      if (!mbar_wait(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL)) break;
+      const int64_t r0 = ((int64_t)blockIdx.x + (int64_t)i * gridDim.x) * R;
+      const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
+      if (lane < rows) {
+        const float* tr = tbuf + (size_t)(tb * R + lane) * GS;
+        float acc;
+        if (!PERROW) {
+          acc = 0.0f;
+#pragma unroll 8
+          for (int b = 0; b < NB; ++b) acc = __fadd_rn(acc, tr[b]);
+        } else {
+          float q = tr[0];
+#pragma unroll 8
+          for (int b = 1; b < NB; ++b) q = __fadd_rn(q, tr[b]);
+          acc = __fadd_rn(0.0f, __fmul_rn(q, __half2float(a.scales[r0 + lane])));
+        }
+        if (a.y_f16)
+          reinterpret_cast<__half*>(a.y)[r0 + lane] = __float2half_rn(acc);
+        else
+          reinterpret_cast<float*>(a.y)[r0 + lane] = acc;
+      }
+      mbar_arrive(&tempty[tb]);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------- compute warps --
+  const int tc = threadIdx.x - 64;
+  const bool active = tc < P.C * P.RP;
+  const int c = active ? tc % P.C : 0;
+  const int rp = active ? tc / P.C : 0;
+  const u64* y2s = reinterpret_cast<const u64*>(y2f);
+
+  for (int i = 0; i < my_groups; ++i) {
+    const int s = i % NS;
+    const int tb = i & 1;
+    if (!mbar_wait(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL)) break;
+    if (i >= 2 && !mbar_wait(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY)) break;
+    const int64_t r0 = ((int64_t)blockIdx.x + (int64_t)i * gridDim.x) * R;
+    const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
+    if (active) {
+      const unsigned char* st = stages + (size_t)s * P.stage_bytes;
+      uint32_t w[U][IW];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = rp * U + u;
+        if (r < rows) {
+          const uint4* src = reinterpret_cast<const uint4*>(st + (size_t)r * P.row_bytes + (size_t)c * (IW * 4));
+#pragma unroll
+          for (int q = 0; q < IW / 4; ++q) {
+            const uint4 v = src[q];
+            w[u][4 * q + 0] = v.x;
+            w[u][4 * q + 1] = v.y;
+            w[u][4 * q + 2] = v.z;
+            w[u][4 * q + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < IW; ++q) w[u][q] = 0x00000000u;
+        }
+      }
+      u64 acc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = 0ull;
+      item_dots<BITS, U>(w, y2s, P.C, c, acc);
+      const __half* scs = reinterpret_cast<const __half*>(st + (size_t)R * P.row_bytes);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = rp * U + u;
+        if (r < rows) {
+          float p0, p1;
+          upk(acc[u], p0, p1);
+          float* dst = tbuf + (size_t)(tb * R + r) * GS + 2 * c;
+          if (PERROW) {
+            dst[0] = p0;
+            dst[1] = p1;
+          } else {
+            const __half2 s2 = *reinterpret_cast<const __half2*>(scs + (size_t)r * NB + 2 * c);
+            dst[0] = __fmul_rn(p0, __low2float(s2));
+            dst[1] = __fmul_rn(p1, __high2float(s2));
+          }
+        }
+      }
+    }
+    mbar_arrive(&empty[s]);
+    mbar_arrive(&tfull[tb]);
+  }
+}
+
+// ------------------------------------------------------------- launcher --
+
+static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int umax, int sms,
+                     TmaPlan* P) {
+  if (K % 256 != 0) return false;
+  const int C = K / 64;
+  if (C > 512) return false;
+  int RP = tc_target / C;
+  if (RP < 1) RP = 1;
+  if (RP > 32) RP = 32;
+  int Tc = ((C * RP + 31) / 32) * 32;
+  if (Tc > 512) return false;
+  const int row_bytes = K * bits / 8;
+  const int sc_row = perrow ? 0 : (K / 32) * 2;
+  // U rows per thread: as many as fit a ~20 KB stage (so that 4 stages plus
+  // the activation table leave room for 2 CTAs per SM), but few enough that
+  // there are at least 3 row groups per CTA slot (load balance on small N).
+  // (Two rows per thread at least: one row leaves a single serial FMA chain
+  // per thread, which is latency-bound.)
+  int U = (Tc > 256 && umax > 2) ? 2 : umax;
+  while (U > 2 && (RP * U > 32 || RP * U * (row_bytes + sc_row) > 20 * 1024)) U /= 2;
+  while (U > 2 && ((int64_t)N + RP * U - 1) / (RP * U) < 3LL * 2 * sms) U /= 2;
+  while (U > 1 && (RP * U > 32 || RP * U * (row_bytes + sc_row) > 40 * 1024)) U /= 2;
+  if (RP * U > 32) return false;
+  P->C = C;
+  P->RP = RP;
+  P->R = RP * U;
+  P->Tc = Tc;
+  P->row_bytes = row_bytes;
+  P->sc_row = sc_row;
+  P->stage_bytes = P->R * (row_bytes + sc_row);
+  P->ngroups = (int)(((int64_t)N + P->R - 1) / P->R);
+  P->y_off = 128;
+  P->stage_off = tma_round16(P->y_off + K * 4);
+  P->tbuf_off = tma_round16(P->stage_off + NS * P->stage_bytes);
+  return true;
+}
+
+static size_t tma_smem(const TmaPlan& P, int K) {
+  return (size_t)P.tbuf_off + (size_t)tma_round16(2 * P.R * (K / 32 + 1) * 4);
+}
+
+template <int BITS, bool PERROW, bool FUSED, int U, int MAXT>
+static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err) {
+  static thread_local int cached_dev = -1;
+  static thread_local size_t smem_set = 0;
+  static thread_local int occ_cache = 0;
+  static thread_local size_t occ_smem = 0;
+  static thread_local int occ_threads = 0;
+  auto kern = gemv_tma_kernel<BITS, PERROW, FUSED, U, MAXT>;
+  const size_t smem = tma_smem(P, a.K);
+  const DevInfo& d = dev_info();
+  if (smem > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  if (dev != cached_dev) { cached_dev = dev; smem_set = 0; occ_smem = 0; occ_threads = 0; }
+  if (smem > smem_set) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+    smem_set = smem;
+  }
+  const int threads = 64 + P.Tc;
+  if (occ_smem != smem || occ_threads != threads) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_cache, kern, threads, smem);
+    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+    occ_smem = smem;
+    occ_threads = threads;
+  }
+  if (occ_cache < 1) return QMV_ERR_UNSUPPORTED;
+  int grid = d.sms * occ_cache;
+  if (grid > P.ngroups) grid = P.ngroups;
+  if (pdl_enabled()) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, P);
+    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  } else {
+    kern<<<grid, threads, smem, s>>>(a, P);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  return QMV_OK;
+}
+
+// CTAs of up to 256 compute threads (320 in all) get up to ~200 registers a
+// thread; larger ones (long K) are limited to 2 rows per thread.
+template <int BITS, bool PERROW, bool FUSED>
+static int tma_u(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err) {
+  const int U = P.R / P.RP;
+  if (P.Tc > 256) {
+    if (U >= 2) return run_tma<BITS, PERROW, FUSED, 2, 576>(a, P, s, err);
+    return run_tma<BITS, PERROW, FUSED, 1, 576>(a, P, s, err);
+  }
+  if (U >= 4) return run_tma<BITS, PERROW, FUSED, 4, 320>(a, P, s, err);
+  if (U == 2) return run_tma<BITS, PERROW, FUSED, 2, 320>(a, P, s, err);
+  return run_tma<BITS, PERROW, FUSED, 1, 320>(a, P, s, err);
+}
+
+template <int BITS>
+static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err, int tc_target) {
+  TmaPlan P;
+  const int umax = (BITS == 8) ? 2 : 4;
+  if (!tma_plan(a.N, a.K, BITS, a.perrow != 0, tc_target, umax, dev_info().sms, &P))
+    return QMV_ERR_UNSUPPORTED;
+  if (a.perrow) return a.fused ? tma_u<BITS, true, true>(a, P, s, err) : tma_u<BITS, true, false>(a, P, s, err);
+  return a.fused ? tma_u<BITS, false, true>(a, P, s, err) : tma_u<BITS, false, false>(a, P, s, err);
+}
+
+int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
+  static int tc_target = [] {
+    const char* e = getenv("QMV_TC");
+    const int v = e ? atoi(e) : 0;
+    return (v >= 128 && v <= 512) ? v : 256;
+  }();
+  switch (bits) {
+    case 2: return tma_bits<2>(a, s, err, tc_target);
+    case 4: return tma_bits<4>(a, s, err, tc_target);
+    default: return tma_bits<8>(a, s, err, tc_target);
+  }
+}
+
+int read_device_error(int clear, int* out) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_qmv_error, sizeof(int));
+  if (e != cudaSuccess) return (int)e;
+  if (clear && v) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_qmv_error, &z, sizeof(int));
+    if (e != cudaSuccess) return (int)e;
+  }
+  *out = v;
+  return 0;
+}
+
+}  // namespace qmv

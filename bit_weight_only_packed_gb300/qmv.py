@@ -39,6 +39,8 @@ SIGNATURES = {
     "qmv_destroy_pack": (_I, [_P]),
     "qmv_status_string": (ctypes.c_char_p, [_I]),
     "qmv_last_cuda_error": (_I, []),
+    "qmv_device_error": (_I, [ctypes.POINTER(_I), _I]),
+    "qmv_set_pdl": (_I, [_I]),
 }
 
 
@@ -192,3 +194,13 @@ def qmv_status_string(status: int) -> str:
 
 def qmv_last_cuda_error() -> int:
     return _lib.qmv_last_cuda_error()
+
+
+def qmv_set_pdl(enable: bool):
+    _check("qmv_set_pdl", _lib.qmv_set_pdl(1 if enable else 0))
+
+
+def qmv_device_error(clear: bool = True) -> int:
+    v = _I()
+    _check("qmv_device_error", _lib.qmv_device_error(ctypes.byref(v), 1 if clear else 0))
+    return v.value

@@ -164,12 +164,37 @@ QMV_API int qmv_pack_info(const qmv_pack *p, int *N, int *K, int *bits, int *gro
 /* qmv_destroy_pack -- free the host descriptor (never the device buffers). */
 QMV_API int qmv_destroy_pack(qmv_pack *p);
 
+/*
+ * qmv_set_pdl -- programmatic dependent launch of the M = 1 matvec kernels
+ * for the calling thread (default off).  When on, a matvec launched right
+ * after another kernel in the same stream may start while that kernel is
+ * still running: it begins streaming its packed weights at once and waits
+ * for the previous kernel to complete (griddepcontrol.wait) before it reads
+ * x / residual / gamma or writes any output.  This hides launch latency
+ * between the dependent matvecs of a decode layer ([A19] "What moved the
+ * needle", dispatch-count item: the per-dispatch tax between kernels).
+ * Requirement: the packed weights of a matvec must not be written by the
+ * kernel launched just before it in the stream (pack once, then run).
+ * Works under stream capture (CUDA graphs).  Always returns QMV_OK.
+ */
+QMV_API int qmv_set_pdl(int enable);
+
 /* qmv_status_string -- static text for a status code. */
 QMV_API const char *qmv_status_string(int status);
 
 /* qmv_last_cuda_error -- the raw cudaError_t behind the calling thread's
  * last QMV_ERR_CUDA (0 if none). */
 QMV_API int qmv_last_cuda_error(void);
+
+/*
+ * qmv_device_error -- the device error word of the current device: 0, or
+ * the code of the first bounded device-side wait that ran out (a kernel that
+ * hits one stops, lets its own copies land and returns; its outputs are then
+ * incomplete).  Synchronises with the device (reads a device symbol).
+ *   out    receives the word.  clear: non-zero resets it to 0.
+ * Errors: INVALID_ARG (out NULL), CUDA.
+ */
+QMV_API int qmv_device_error(int *out, int clear);
 
 #ifdef __cplusplus
 }

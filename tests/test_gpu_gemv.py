@@ -111,3 +111,55 @@ def test_shape_mismatch_rejected():
     assert lib.qmv_gemv(m.pack.handle, 0, 64, 128, 2, 32, x.data_ptr(), y.data_ptr(), 0, 0, s) == -1
     assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 2, 32, x.data_ptr() + 2, y.data_ptr(), 0, 0, s) == -3
     assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 2, 32, x.data_ptr(), y.data_ptr(), 7, 0, s) == -1
+
+
+def test_device_error_word_clear_after_runs():
+    q = qmv()
+    m = Mat("errword", 8192, 2048, 2, 32)
+    x, _, _ = acts("errword", 1, 2048)
+    for _ in range(3):
+        q.qmv_gemv(m.pack, to_dev(x))
+    torch.cuda.synchronize()
+    assert q.qmv_device_error(clear=True) == 0
+
+
+def _chain(q, packs, x, reps):
+    """x -> A -> B -> A -> ... with fp16 outputs feeding the next matvec."""
+    outs = []
+    cur = x
+    for i in range(reps):
+        p = packs[i % len(packs)]
+        cur = q.qmv_gemv(p, cur, y_dtype=q.QMV_F16)
+        outs.append(cur)
+    return outs
+
+
+def test_pdl_chain_matches_plain_launches():
+    q = qmv()
+    A = Mat("pdlA", 2048, 2048, 2, 32)
+    B = Mat("pdlB", 2048, 2048, 4, 32)
+    x, _, _ = acts("pdl", 1, 2048)
+    xd = to_dev(x)
+    ref = [t.clone() for t in _chain(q, [A.pack, B.pack], xd, 8)]
+    torch.cuda.synchronize()
+    q.qmv_set_pdl(True)
+    try:
+        got = _chain(q, [A.pack, B.pack], xd, 8)
+        torch.cuda.synchronize()
+        for r, g in zip(ref, got):
+            assert torch.equal(r.view(torch.int16), g.view(torch.int16))
+        # the same chain captured in a CUDA graph (programmatic edges)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            _chain(q, [A.pack, B.pack], xd, 2)           # warm-up on the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            gout = _chain(q, [A.pack, B.pack], xd, 8)
+        g.replay()
+        torch.cuda.synchronize()
+        for r, t in zip(ref, gout):
+            assert torch.equal(r.view(torch.int16), t.view(torch.int16))
+    finally:
+        q.qmv_set_pdl(False)
+    assert q.qmv_device_error(clear=True) == 0
