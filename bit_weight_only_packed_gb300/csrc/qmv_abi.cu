@@ -122,10 +122,26 @@ static qmv::GemvArgs base_args(const qmv_pack* p, int M, const void* x, void* y,
   return a;
 }
 
-// M columns through the CUDA-core kernels, 32 columns per launch above 32.
-static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s) {
+// Dispatch: M = 1 -> the bulk-copy pipeline kernel (or the generic one);
+// M <= 32, or any M in exact mode, or int4/int8 -> CUDA-core tiles, 32
+// columns per launch (bit-exact); M > 32 in fast mode with int2 weights ->
+// tcgen05 tensor-core tiles, 128 columns per launch.
+static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s, int mode) {
   cudaError_t err = cudaSuccess;
   int rc;
+  if (a.M > 32 && mode == QMV_FAST && bits == 2 && !a.fused) {
+    const int M = a.M;
+    const size_t ysz = a.y_f16 ? 2 : 4;
+    for (int m0 = 0; m0 < M; m0 += 128) {
+      qmv::GemvArgs b = a;
+      b.M = (M - m0 < 128) ? (M - m0) : 128;
+      b.x = a.x + (int64_t)m0 * a.K;
+      b.y = (char*)a.y + (size_t)m0 * (size_t)a.N * ysz;
+      rc = qmv::launch_tc_gemm(b, bits, s, &err);
+      if (rc != QMV_OK) return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
+    }
+    return QMV_OK;
+  }
   if (a.M == 1) {
     rc = qmv::launch_gemv_tma(a, bits, s, &err);
     if (rc == QMV_ERR_UNSUPPORTED) rc = qmv::launch_gemv_m1(a, bits, s, &err);
@@ -151,14 +167,14 @@ int qmv_gemv(const qmv_pack* p, int M, int N, int K, int bits, int group, const 
   int rc = check_common(p, M, x, y, y_dtype, mode);
   if (rc != QMV_OK) return rc;
   if (N != p->N || K != p->K || bits != p->bits || group != p->group) return QMV_ERR_SHAPE;
-  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream);
+  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream, mode);
 }
 
 int qmv_chunk_gemm(const qmv_pack* p, int M, const void* x, void* y, int y_dtype, int mode,
                    void* stream) {
   int rc = check_common(p, M, x, y, y_dtype, mode);
   if (rc != QMV_OK) return rc;
-  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream);
+  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream, mode);
 }
 
 int qmv_fused_rmsnorm_gemv(const qmv_pack* p, int M, const void* x, const void* residual,
@@ -177,7 +193,7 @@ int qmv_fused_rmsnorm_gemv(const qmv_pack* p, int M, const void* x, const void* 
   a.gamma = (const __half*)gamma;
   a.eps = eps;
   a.h_out = (__half*)h_out;
-  return run_cuda_core(a, p->bits, (cudaStream_t)stream);
+  return run_cuda_core(a, p->bits, (cudaStream_t)stream, mode);
 }
 
 int qmv_unpack_codes(const qmv_pack* p, int8_t* d_codes_out, void* stream) {

@@ -54,6 +54,9 @@ int launch_gemm_small(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* 
 // M = 1 through the bulk-copy pipeline; QMV_ERR_UNSUPPORTED if the shape does
 // not fit it (the caller then uses launch_gemv_m1).
 int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+// tcgen05 tensor-core tiles for 1..128 token columns, int2 weights (fast
+// mode); QMV_ERR_UNSUPPORTED for other widths or the fused prologue.
+int launch_tc_gemm(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
 // Programmatic dependent launch of the M = 1 kernels (off by default).
 bool pdl_enabled();
 void set_pdl(bool on);

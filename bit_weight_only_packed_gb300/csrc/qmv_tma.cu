@@ -581,7 +581,12 @@ int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* er
   }
 }
 
+int read_tc_error(int clear, int* out);
+
 int read_device_error(int clear, int* out) {
+  int t = 0;
+  const int et = read_tc_error(clear, &t);
+  if (et != 0) return et;
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_qmv_error, sizeof(int));
   if (e != cudaSuccess) return (int)e;
@@ -590,7 +595,7 @@ int read_device_error(int clear, int* out) {
     e = cudaMemcpyToSymbol(g_qmv_error, &z, sizeof(int));
     if (e != cudaSuccess) return (int)e;
   }
-  *out = v;
+  *out = v ? v : t;
   return 0;
 }
 
