@@ -52,6 +52,22 @@ def packed_bytes(N, K, bits, group):
 LAYER_BYTES = sum(packed_bytes(N, K, b, g) for _, N, K, b, g, _ in LAYER)
 
 
+def measured_traffic(key):
+    """DRAM bytes per launch from the committed ncu capture of this kernel,
+    or None if the kernel's sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))[key]
+        h = hashlib.sha256()
+        for src in d["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return d["traffic_bytes"] if h.hexdigest() == d["sources_sha256"] else None
+    except Exception:
+        return None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -298,13 +314,7 @@ def gpu_arm(args, rank, world, local):
     gbs = world * LAYER_BYTES * K / (ms_max * 1e-3) / 1e9
     dom_bytes = packed_bytes(2 * D_FF, D_MODEL, 2, 32)
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            traffic = json.load(open(tr_path)).get("gemv_m1_fused_int2_16384x2048")
-        except Exception:
-            traffic = None
+    traffic = measured_traffic("gemv_m1_fused_int2_16384x2048")
     out = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -414,8 +424,37 @@ def reference_arm(args, rank, world):
     }
 
 
+def probe(spec: str):
+    """Three launches of one matvec shape (for profiler captures):
+    spec = "N,K,bits,group,M[,fused]"."""
+    import torch
+
+    import synth
+    from bit_weight_only_packed_gb300 import qmv
+    parts = spec.split(",")
+    N, K, bits, group, M = (int(v) for v in parts[:5])
+    fused = len(parts) > 5 and parts[5] == "fused"
+    dev = torch.device("cuda")
+    codes = synth.codes(SEED, "probe", N, K, bits, device=dev)
+    scales = synth.scales(SEED, "probe", N, K // group, device=dev)
+    p = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
+    del codes, scales
+    x = torch.from_numpy(synth.normal_f16(SEED, "probe.x", (M, K))).to(dev)
+    r = torch.from_numpy(synth.normal_f16(SEED, "probe.r", (M, K))).to(dev)
+    g = torch.from_numpy(synth.normal_f16(SEED, "probe.g", (K,), mean=1.0, std=0.1)).to(dev)
+    for _ in range(3):
+        if fused:
+            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, 1e-6)
+        else:
+            qmv.qmv_chunk_gemm(p, x) if M > 1 else qmv.qmv_gemv(p, x)
+    torch.cuda.synchronize()
+    print(json.dumps({"probe": spec, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--probe", default=None,
+                    help="run 3 launches of one shape N,K,bits,group,M[,fused] and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
@@ -423,6 +462,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.probe:
+        probe(args.probe)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
