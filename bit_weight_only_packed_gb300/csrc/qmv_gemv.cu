@@ -36,7 +36,6 @@
 
 namespace qmv {
 
-constexpr int UMAX = 4;        // most passes of rows in flight per thread (gemv_m1)
 constexpr int M1_MAXT = 672;   // largest CTA of gemv_m1 (C*RP, a multiple of 32)
 
 // CTAs of up to 256 threads keep 4 passes in flight; larger CTAs (long or

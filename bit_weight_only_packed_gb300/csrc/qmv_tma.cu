@@ -30,6 +30,8 @@
 //   * Every mbarrier wait is bounded; on timeout the kernel records an error
 //     code in the device error word, stops issuing, lets its own copies land
 //     and returns.
+#include <cuda.h>
+
 #include "qmv_internal.cuh"
 
 namespace qmv {
@@ -38,10 +40,10 @@ __device__ int g_qmv_error = 0;
 
 namespace {
 
-constexpr int NS = 4;                      // ring stages
+constexpr int NS = 4;                      // ring stages (a power of two)
 constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (~0.5 s each)
 constexpr int ERR_TIMEOUT_FULL = 1, ERR_TIMEOUT_EMPTY = 2, ERR_TIMEOUT_TFULL = 3,
-              ERR_TIMEOUT_TEMPTY = 4;
+              ERR_TIMEOUT_TEMPTY = 4, ERR_SMEM_ALIGN = 5;
 
 typedef unsigned long long u64;
 
@@ -95,11 +97,13 @@ __device__ __noinline__ void mbar_drain(uint64_t* b, uint32_t parity) {
   atomicCAS(&g_qmv_error, 0, ERR_TIMEOUT_FULL);
 }
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+// 2-D tiled tensor copy global -> shared (box given by the tensor map),
+// completing on `bar`.  x is the innermost coordinate (in elements).
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           sa(dst)),
-      "l"(src), "r"(bytes), "r"(sa(bar))
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(sa(bar))
       : "memory");
 }
 
@@ -110,11 +114,6 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 __device__ __forceinline__ u64 pk(float a, float b) {
   u64 r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ u64 pku(uint32_t a, uint32_t b) {
-  u64 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
   return r;
 }
 __device__ __forceinline__ void upk(u64 v, float& a, float& b) {
@@ -208,14 +207,25 @@ __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32]
 }  // namespace
 
 // Launch plan (host computes it; the kernel reads it).
+//
+// Rows are processed in groups of R, and each group in NSEG segments of KS
+// codes (KS = K when K <= 2048, else the largest multiple of 256 up to 2048
+// that divides K).  A pipeline stage holds one (group, segment): R rows x KS
+// codes plus their group-32 scales.  The fold warp keeps one accumulator per
+// row across the segments of a group, so the fold stays serial over all K/32
+// blocks of the row while 32 rows are folded side by side.
 struct TmaPlan {
-  int C;             // 64-code items per row
-  int RP;            // rows in parallel (threads per row group = C*RP <= Tc)
-  int R;             // rows per group = RP*U
+  int C;             // 64-code items per row (table layout)
+  int Cs;            // 64-code items per segment
+  int KS, NSEG;      // codes per segment, segments per row
+  int RP;            // rows in parallel (Cs*RP <= Tc)
+  int R;             // rows per group = RP*U (<= 32: one fold lane per row)
   int Tc;            // compute threads (multiple of 32)
   int row_bytes;     // code bytes per row
-  int sc_row;        // scale bytes per row inside a stage (0 with one scale per row)
-  int stage_bytes;   // R*(row_bytes + sc_row)
+  int seg_bytes;     // code bytes per row per segment
+  int seg_sc;        // scale bytes per row per segment (0 with one scale per row)
+  int sc_off;        // offset of the scales inside a stage (128-byte aligned)
+  int stage_bytes;   // whole stage, a multiple of 128 bytes
   int ngroups;       // ceil(N / R)
   int y_off, stage_off, tbuf_off;   // shared-memory offsets (bytes)
 };
@@ -223,7 +233,9 @@ struct TmaPlan {
 __host__ __device__ inline int tma_round16(int x) { return (x + 15) & ~15; }
 
 template <int BITS, bool PERROW, bool FUSED, int U, int MAXT>
-__global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(GemvArgs a, TmaPlan P) {
+__global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
+    gemv_tma_kernel(GemvArgs a, TmaPlan P, const __grid_constant__ CUtensorMap tm_codes,
+                    const __grid_constant__ CUtensorMap tm_scales) {
   constexpr int IW = 64 * BITS / 32;   // words per item
   extern __shared__ __align__(128) unsigned char sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
@@ -237,23 +249,34 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(G
   float* tbuf = reinterpret_cast<float*>(sm + P.tbuf_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = a.K, NB = K / 32, GS = NB + 1, R = P.R;
+  const int K = a.K, NB = K / 32, R = P.R;
+  const int NBS = P.KS / 32;             // blocks per segment
+  const int GS = NBS + 1;                // fold-buffer row stride
   const int my_groups = (blockIdx.x < (unsigned)P.ngroups)
                             ? (P.ngroups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
                             : 0;
+  const int my_stages = my_groups * P.NSEG;
 
   // Programmatic dependent launch (a no-op when the launch did not ask for
   // it): let the next kernel in the stream be scheduled as soon as SMs free
   // up; its weight copies then overlap this kernel's tail.
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // tensor copies need 128-byte aligned destinations: the dynamic shared
+  // memory window starts aligned when there is no static shared memory
+  if ((sa(sm) & 127u) != 0u) {
+    if (threadIdx.x == 0) atomicCAS(&g_qmv_error, 0, ERR_SMEM_ALIGN);
+    return;
+  }
   if (threadIdx.x == 0) {
+    // consumers arrive once per warp (lane 0, after __syncwarp orders the
+    // lanes' shared-memory accesses before its release)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], P.Tc);
+      mbar_init(&empty[s], P.Tc / 32);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], P.Tc);
-      mbar_init(&tempty[b], 32);
+      mbar_init(&tfull[b], P.Tc / 32);
+      mbar_init(&tempty[b], 1);
     }
     *abort_f = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -262,29 +285,34 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(G
 
   // ------------------------------------------------------------ producer --
   if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < my_groups; ++i) {
-        const int s = i % NS;
-        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY)) break;
-        if (*abort_f) break;
-        const int64_t g = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
-        const int64_t r0 = g * R;
-        const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
-        const uint32_t cb = (uint32_t)rows * P.row_bytes;
-        const uint32_t sb = PERROW ? 0u : (uint32_t)rows * P.sc_row;
-        unsigned char* st = stages + (size_t)s * P.stage_bytes;
-        mbar_arrive_tx(&full[s], cb + sb);
-        bulk_g2s(st, reinterpret_cast<const unsigned char*>(a.codes) + r0 * P.row_bytes, cb, &full[s]);
-        if (!PERROW)
-          bulk_g2s(st + (size_t)R * P.row_bytes,
-                   reinterpret_cast<const unsigned char*>(a.scales) + r0 * P.sc_row, sb, &full[s]);
-        ++issued;
+    int issued = 0;
+    int seg = 0;
+    int64_t g = blockIdx.x;
+    for (int i = 0; i < my_stages; ++i) {
+      const int s = i & (NS - 1);
+      if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY)) break;
+      if (*abort_f) break;
+      const int64_t r0 = g * R;
+      const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
+      // one box of R rows x one segment: rows past N are zero-filled, the
+      // transaction count is always the whole box
+      unsigned char* st = stages + (size_t)s * P.stage_bytes;
+      if (lane == 0) {
+        const uint32_t tx = (uint32_t)R * P.seg_bytes + (PERROW ? 0u : (uint32_t)R * P.seg_sc);
+        mbar_arrive_tx(&full[s], tx);
+        tma_2d(st, &tm_codes, seg * (P.seg_bytes / 8), (int)r0, &full[s]);
+        if (!PERROW) tma_2d(st + P.sc_off, &tm_scales, seg * (P.KS / 32), (int)r0, &full[s]);
       }
-      // let every copy this thread issued land before the CTA can exit
+      ++issued;
+      if (++seg == P.NSEG) {
+        seg = 0;
+        g += gridDim.x;
+      }
+    }
+    // let every copy this warp issued land before the CTA can exit
+    if (lane == 0)
       for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
         mbar_drain(&full[j % NS], (j / NS) & 1);
-    }
     return;
   }
 
@@ -360,47 +388,63 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(G
 
   // ---------------------------------------------------------- fold warp --
   if (warp == 1) {
-    for (int i = 0; i < my_groups; ++i) {
+    float acc = 0.0f;   // this lane's row: group-32 accumulator, or the per-row block sum
+    int seg = 0;
+    int64_t g = blockIdx.x;
+    for (int i = 0; i < my_stages; ++i) {
       const int tb = i & 1;
       if (!mbar_wait(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL)) break;
-      const int64_t r0 = ((int64_t)blockIdx.x + (int64_t)i * gridDim.x) * R;
+      const int64_t r0 = g * R;
       const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
       if (lane < rows) {
         const float* tr = tbuf + (size_t)(tb * R + lane) * GS;
-        float acc;
         if (!PERROW) {
-          acc = 0.0f;
+          if (seg == 0) acc = 0.0f;
 #pragma unroll 8
-          for (int b = 0; b < NB; ++b) acc = __fadd_rn(acc, tr[b]);
+          for (int b = 0; b < NBS; ++b) acc = __fadd_rn(acc, tr[b]);
         } else {
-          float q = tr[0];
+          int b0 = 0;
+          if (seg == 0) {
+            acc = tr[0];
+            b0 = 1;
+          }
 #pragma unroll 8
-          for (int b = 1; b < NB; ++b) q = __fadd_rn(q, tr[b]);
-          acc = __fadd_rn(0.0f, __fmul_rn(q, __half2float(a.scales[r0 + lane])));
+          for (int b = b0; b < NBS; ++b) acc = __fadd_rn(acc, tr[b]);
         }
-        if (a.y_f16)
-          reinterpret_cast<__half*>(a.y)[r0 + lane] = __float2half_rn(acc);
-        else
-          reinterpret_cast<float*>(a.y)[r0 + lane] = acc;
+        if (seg == P.NSEG - 1) {
+          float out = acc;
+          if (PERROW) out = __fadd_rn(0.0f, __fmul_rn(acc, __half2float(a.scales[r0 + lane])));
+          if (a.y_f16)
+            reinterpret_cast<__half*>(a.y)[r0 + lane] = __float2half_rn(out);
+          else
+            reinterpret_cast<float*>(a.y)[r0 + lane] = out;
+        }
       }
-      mbar_arrive(&tempty[tb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[tb]);
+      if (++seg == P.NSEG) {
+        seg = 0;
+        g += gridDim.x;
+      }
     }
     return;
   }
 
   // ------------------------------------------------------- compute warps --
   const int tc = threadIdx.x - 64;
-  const bool active = tc < P.C * P.RP;
-  const int c = active ? tc % P.C : 0;
-  const int rp = active ? tc / P.C : 0;
+  const bool active = tc < P.Cs * P.RP;
+  const int c = active ? tc % P.Cs : 0;
+  const int rp = active ? tc / P.Cs : 0;
   const u64* y2s = reinterpret_cast<const u64*>(y2f);
 
-  for (int i = 0; i < my_groups; ++i) {
-    const int s = i % NS;
+  int seg = 0;
+  int64_t g = blockIdx.x;
+  for (int i = 0; i < my_stages; ++i) {
+    const int s = i & (NS - 1);
     const int tb = i & 1;
     if (!mbar_wait(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL)) break;
     if (i >= 2 && !mbar_wait(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY)) break;
-    const int64_t r0 = ((int64_t)blockIdx.x + (int64_t)i * gridDim.x) * R;
+    const int64_t r0 = g * R;
     const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
     if (active) {
       const unsigned char* st = stages + (size_t)s * P.stage_bytes;
@@ -409,7 +453,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(G
       for (int u = 0; u < U; ++u) {
         const int r = rp * U + u;
         if (r < rows) {
-          const uint4* src = reinterpret_cast<const uint4*>(st + (size_t)r * P.row_bytes + (size_t)c * (IW * 4));
+          const uint4* src = reinterpret_cast<const uint4*>(st + (size_t)r * P.seg_bytes + (size_t)c * (IW * 4));
 #pragma unroll
           for (int q = 0; q < IW / 4; ++q) {
             const uint4 v = src[q];
@@ -426,8 +470,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(G
       u64 acc[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = 0ull;
-      item_dots<BITS, U>(w, y2s, P.C, c, acc);
-      const __half* scs = reinterpret_cast<const __half*>(st + (size_t)R * P.row_bytes);
+      item_dots<BITS, U>(w, y2s, P.C, seg * P.Cs + c, acc);
+      const __half* scs = reinterpret_cast<const __half*>(st + P.sc_off);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int r = rp * U + u;
@@ -439,62 +483,154 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1) gemv_tma_kernel(G
             dst[0] = p0;
             dst[1] = p1;
           } else {
-            const __half2 s2 = *reinterpret_cast<const __half2*>(scs + (size_t)r * NB + 2 * c);
+            const __half2 s2 = *reinterpret_cast<const __half2*>(scs + (size_t)r * NBS + 2 * c);
             dst[0] = __fmul_rn(p0, __low2float(s2));
             dst[1] = __fmul_rn(p1, __high2float(s2));
           }
         }
       }
     }
-    mbar_arrive(&empty[s]);
-    mbar_arrive(&tfull[tb]);
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&empty[s]);
+      mbar_arrive(&tfull[tb]);
+    }
+    if (++seg == P.NSEG) {
+      seg = 0;
+      g += gridDim.x;
+    }
   }
 }
 
 // ------------------------------------------------------------- launcher --
 
-static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int umax, int sms,
-                     TmaPlan* P) {
+// Codes per segment: the whole row up to 2048, else the largest multiple of
+// 256 up to 2048 that divides K.
+static int tma_segment(int K) {
+  if (K <= 2048) return K;
+  for (int d = 8; d >= 1; --d)
+    if ((K / 256) % d == 0) return 256 * d;
+  return 256;
+}
+
+// Plan for about `tc_target` compute threads and U rows per thread
+// (RP*U <= 32 rows per group: one fold lane per row).
+static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int U, TmaPlan* P) {
   if (K % 256 != 0) return false;
-  const int C = K / 64;
-  if (C > 512) return false;
-  int RP = tc_target / C;
+  const int KS = tma_segment(K);
+  const int Cs = KS / 64;
+  int RP = tc_target / Cs;
   if (RP < 1) RP = 1;
   if (RP > 32) RP = 32;
-  int Tc = ((C * RP + 31) / 32) * 32;
+  const int Tc = ((Cs * RP + 31) / 32) * 32;
   if (Tc > 512) return false;
-  const int row_bytes = K * bits / 8;
-  const int sc_row = perrow ? 0 : (K / 32) * 2;
-  // U rows per thread: as many as fit a ~20 KB stage (so that 4 stages plus
-  // the activation table leave room for 2 CTAs per SM), but few enough that
-  // there are at least 3 row groups per CTA slot (load balance on small N).
-  // (Two rows per thread at least: one row leaves a single serial FMA chain
-  // per thread, which is latency-bound.)
-  int U = (Tc > 256 && umax > 2) ? 2 : umax;
-  while (U > 2 && (RP * U > 32 || RP * U * (row_bytes + sc_row) > 20 * 1024)) U /= 2;
-  while (U > 2 && ((int64_t)N + RP * U - 1) / (RP * U) < 3LL * 2 * sms) U /= 2;
-  while (U > 1 && (RP * U > 32 || RP * U * (row_bytes + sc_row) > 40 * 1024)) U /= 2;
   if (RP * U > 32) return false;
-  P->C = C;
+  P->C = K / 64;
+  P->Cs = Cs;
+  P->KS = KS;
+  P->NSEG = K / KS;
   P->RP = RP;
   P->R = RP * U;
   P->Tc = Tc;
-  P->row_bytes = row_bytes;
-  P->sc_row = sc_row;
-  P->stage_bytes = P->R * (row_bytes + sc_row);
+  P->row_bytes = K * bits / 8;
+  P->seg_bytes = KS * bits / 8;
+  P->seg_sc = perrow ? 0 : (KS / 32) * 2;
+  P->sc_off = (P->R * P->seg_bytes + 127) & ~127;
+  P->stage_bytes = (P->sc_off + P->R * P->seg_sc + 127) & ~127;
   P->ngroups = (int)(((int64_t)N + P->R - 1) / P->R);
   P->y_off = 128;
-  P->stage_off = tma_round16(P->y_off + K * 4);
+  P->stage_off = (P->y_off + K * 4 + 127) & ~127;
   P->tbuf_off = tma_round16(P->stage_off + NS * P->stage_bytes);
   return true;
 }
 
+// ------------------------------------------------------- tensor maps ----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return (EncodeTiledFn)f;
+  }();
+  return fn;
+}
+
+// Tensor maps of a pack for a plan: codes as UINT64 [N][row_bytes/8] with a
+// box of (segment bytes / 8) x R, scales as UINT16 [N][K/32] with a box of
+// (K_seg / 32) x R.  Cached per thread (a few entries).
+static bool tensor_maps(const GemvArgs& a, int bits, const TmaPlan& P, CUtensorMap* tc, CUtensorMap* ts) {
+  struct Entry { const void* codes; const void* scales; int N, K, bits, R, KS; CUtensorMap c, s; };
+  static thread_local Entry cache[8];
+  static thread_local int valid = 0, next = 0;
+  for (int i = 0; i < valid; ++i) {
+    const Entry& e = cache[i];
+    if (e.codes == a.codes && e.scales == a.scales && e.N == a.N && e.K == a.K && e.bits == bits &&
+        e.R == P.R && e.KS == P.KS) {
+      *tc = e.c;
+      *ts = e.s;
+      return true;
+    }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  Entry e;
+  e.codes = a.codes;
+  e.scales = a.scales;
+  e.N = a.N;
+  e.K = a.K;
+  e.bits = bits;
+  e.R = P.R;
+  e.KS = P.KS;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(P.row_bytes / 8), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)P.row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(P.seg_bytes / 8), (cuuint32_t)P.R};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&e.c, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, (void*)a.codes, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  if (a.perrow) {
+    e.s = e.c;   // unused
+  } else {
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 32) * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)(P.KS / 32), (cuuint32_t)P.R};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&e.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void*)a.scales, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  cache[next] = e;
+  next = (next + 1) % 8;
+  if (valid < 8) ++valid;
+  *tc = e.c;
+  *ts = e.s;
+  return true;
+}
+
+// The fold buffer (2 x R rows x (KS/32 + 1) floats) also holds the fused
+// prologue's K/32 block sums before the main loop starts.
 static size_t tma_smem(const TmaPlan& P, int K) {
-  return (size_t)P.tbuf_off + (size_t)tma_round16(2 * P.R * (K / 32 + 1) * 4);
+  const int fold = 2 * P.R * (P.KS / 32 + 1) * 4;
+  const int bsum = (K / 32) * 4;
+  return (size_t)P.tbuf_off + (size_t)tma_round16(fold > bsum ? fold : bsum);
 }
 
 template <int BITS, bool PERROW, bool FUSED, int U, int MAXT>
-static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err) {
+static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err,
+                   int* occ_only = nullptr) {
   static thread_local int cached_dev = -1;
   static thread_local size_t smem_set = 0;
   static thread_local int occ_cache = 0;
@@ -520,9 +656,15 @@ static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaErro
     occ_smem = smem;
     occ_threads = threads;
   }
+  if (occ_only) {
+    *occ_only = occ_cache;
+    return QMV_OK;
+  }
   if (occ_cache < 1) return QMV_ERR_UNSUPPORTED;
   int grid = d.sms * occ_cache;
   if (grid > P.ngroups) grid = P.ngroups;
+  CUtensorMap tmc, tms;
+  if (!tensor_maps(a, BITS, P, &tmc, &tms)) return QMV_ERR_UNSUPPORTED;
   if (pdl_enabled()) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -534,10 +676,10 @@ static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaErro
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, a, P);
+    e = cudaLaunchKernelEx(&cfg, kern, a, P, tmc, tms);
     if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   } else {
-    kern<<<grid, threads, smem, s>>>(a, P);
+    kern<<<grid, threads, smem, s>>>(a, P, tmc, tms);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
@@ -547,37 +689,86 @@ static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaErro
 // CTAs of up to 256 compute threads (320 in all) get up to ~200 registers a
 // thread; larger ones (long K) are limited to 2 rows per thread.
 template <int BITS, bool PERROW, bool FUSED>
-static int tma_u(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err) {
+static int tma_u(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err,
+                 int* occ_only) {
   const int U = P.R / P.RP;
   if (P.Tc > 256) {
-    if (U >= 2) return run_tma<BITS, PERROW, FUSED, 2, 576>(a, P, s, err);
-    return run_tma<BITS, PERROW, FUSED, 1, 576>(a, P, s, err);
+    if (U >= 2) return run_tma<BITS, PERROW, FUSED, 2, 576>(a, P, s, err, occ_only);
+    return run_tma<BITS, PERROW, FUSED, 1, 576>(a, P, s, err, occ_only);
   }
-  if (U >= 4) return run_tma<BITS, PERROW, FUSED, 4, 320>(a, P, s, err);
-  if (U == 2) return run_tma<BITS, PERROW, FUSED, 2, 320>(a, P, s, err);
-  return run_tma<BITS, PERROW, FUSED, 1, 320>(a, P, s, err);
+  if (U >= 4) return run_tma<BITS, PERROW, FUSED, 4, 320>(a, P, s, err, occ_only);
+  if (U == 2) return run_tma<BITS, PERROW, FUSED, 2, 320>(a, P, s, err, occ_only);
+  return run_tma<BITS, PERROW, FUSED, 1, 320>(a, P, s, err, occ_only);
 }
 
 template <int BITS>
-static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err, int tc_target) {
-  TmaPlan P;
-  const int umax = (BITS == 8) ? 2 : 4;
-  if (!tma_plan(a.N, a.K, BITS, a.perrow != 0, tc_target, umax, dev_info().sms, &P))
-    return QMV_ERR_UNSUPPORTED;
-  if (a.perrow) return a.fused ? tma_u<BITS, true, true>(a, P, s, err) : tma_u<BITS, true, false>(a, P, s, err);
-  return a.fused ? tma_u<BITS, false, true>(a, P, s, err) : tma_u<BITS, false, false>(a, P, s, err);
+static int tma_dispatch(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err,
+                        int* occ_only) {
+  if (a.perrow)
+    return a.fused ? tma_u<BITS, true, true>(a, P, s, err, occ_only)
+                   : tma_u<BITS, true, false>(a, P, s, err, occ_only);
+  return a.fused ? tma_u<BITS, false, true>(a, P, s, err, occ_only)
+                 : tma_u<BITS, false, false>(a, P, s, err, occ_only);
+}
+
+// Choose the plan with the most resident compute warps per SM (occupancy
+// from the runtime for the exact kernel, block size and shared memory); on a
+// tie, the larger row group.  Candidates: ~256 or ~512 compute threads, and
+// 4 or 2 rows per thread (2 for int8 and for the 512-thread CTAs), with at
+// least 3 row groups per CTA slot when N allows it (load balance).  The
+// choice is cached per shape.
+template <int BITS>
+static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
+  struct Key { int N, K, perrow, fused, dev; };
+  struct Entry { Key k; TmaPlan p; bool ok; };
+  static thread_local Entry cache[16];
+  static thread_local int next = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const Key key{a.N, a.K, a.perrow, a.fused, dev};
+  for (int i = 0; i < 16; ++i) {
+    const Key& k = cache[i].k;
+    if (cache[i].ok && k.N == key.N && k.K == key.K && k.perrow == key.perrow &&
+        k.fused == key.fused && k.dev == key.dev)
+      return tma_dispatch<BITS>(a, cache[i].p, s, err, nullptr);
+  }
+  static const int tc_force = [] {
+    const char* e = getenv("QMV_TC");
+    const int v = e ? atoi(e) : 0;
+    return (v >= 128 && v <= 512) ? v : 0;
+  }();
+  const int sms = dev_info().sms;
+  TmaPlan best;
+  int best_score = -1;
+  for (int tc : {256, 512}) {
+    if (tc_force && tc != tc_force) continue;
+    for (int U : {4, 2}) {
+      if (BITS == 8 && U > 2) continue;
+      if (tc > 256 && U > 2) continue;
+      TmaPlan P;
+      if (!tma_plan(a.N, a.K, BITS, a.perrow != 0, tc, U, &P)) continue;
+      if (tma_smem(P, a.K) > (size_t)dev_info().max_smem_optin) continue;
+      int occ = 0;
+      if (tma_dispatch<BITS>(a, P, s, err, &occ) != QMV_OK || occ < 1) continue;
+      int score = occ * (P.Tc / 32) * 64 + P.R;
+      if ((int64_t)P.ngroups < 3LL * occ * sms && U > 2) score -= 64 * 64;   // balance
+      if (score > best_score) {
+        best_score = score;
+        best = P;
+      }
+    }
+  }
+  if (best_score < 0) return QMV_ERR_UNSUPPORTED;
+  cache[next] = Entry{key, best, true};
+  next = (next + 1) % 16;
+  return tma_dispatch<BITS>(a, best, s, err, nullptr);
 }
 
 int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
-  static int tc_target = [] {
-    const char* e = getenv("QMV_TC");
-    const int v = e ? atoi(e) : 0;
-    return (v >= 128 && v <= 512) ? v : 256;
-  }();
   switch (bits) {
-    case 2: return tma_bits<2>(a, s, err, tc_target);
-    case 4: return tma_bits<4>(a, s, err, tc_target);
-    default: return tma_bits<8>(a, s, err, tc_target);
+    case 2: return tma_bits<2>(a, s, err);
+    case 4: return tma_bits<4>(a, s, err);
+    default: return tma_bits<8>(a, s, err);
   }
 }
 
