@@ -130,4 +130,52 @@ __device__ __forceinline__ float block_dot(const uint32_t* w, YF yk) {
   return p;
 }
 
+
+// ---- exact fp32 decode on paired lanes (used by the M = 1 pipeline and the
+// ---- M-column tiles) -------------------------------------------------------
+//
+// A b-bit field u at bit offset o < 16 - b of a 32-bit word becomes the fp32
+// value 2^23 + u*2^o with one LOP3 ((w & (mask << o)) | 0x4B000000, exact:
+// the field lies in the mantissa).  Subtracting 2^23 + 2^(b-1)*2^o gives
+// v*2^o exactly (v = u - 2^(b-1)).  Two such values, one from each of the two
+// 32-code blocks of a 64-code item, share one paired fp32 instruction; the
+// activation is pre-scaled by 2^-o so that (y*2^-o)*(v*2^o) = y*v exactly and
+// one paired FMA advances both blocks' serial sums by their exact products.
+
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 pk(float a, float b) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(u64 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+// d = a*b + c on two fp32 lanes, each lane rounded once
+__device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// v' = ((a & m) | 0x4B000000, (b & m) | 0x4B000000) - off on two fp32 lanes.
+// With m = (2^bits - 1) << o the magic float is 2^23 + u*2^o exactly, and
+// off = 2^23 + 2^(bits-1)*2^o, so v' = (u - 2^(bits-1)) * 2^o = v * 2^o
+// exactly.  Both LOP3s write the halves of one register pair that the paired
+// add reads.
+__device__ __forceinline__ u64 decode2(uint32_t a, uint32_t b, uint32_t m, u64 off) {
+  u64 v;
+  asm("{\n\t.reg .b32 t0, t1;\n\t.reg .b64 t;\n\t"
+      "lop3.b32 t0, %1, %3, 0x4B000000, 0xEA;\n\t"
+      "lop3.b32 t1, %2, %3, 0x4B000000, 0xEA;\n\t"
+      "mov.b64 t, {t0, t1};\n\t"
+      "sub.rn.f32x2 %0, t, %4;\n\t}"
+      : "=l"(v)
+      : "r"(a), "r"(b), "r"(m), "l"(off));
+  return v;
+}
+
 }  // namespace qmv

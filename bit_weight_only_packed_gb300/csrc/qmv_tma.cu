@@ -45,7 +45,6 @@ constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (~0.5 s each)
 constexpr int ERR_TIMEOUT_FULL = 1, ERR_TIMEOUT_EMPTY = 2, ERR_TIMEOUT_TFULL = 3,
               ERR_TIMEOUT_TEMPTY = 4, ERR_SMEM_ALIGN = 5;
 
-typedef unsigned long long u64;
 
 __device__ __forceinline__ uint32_t sa(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -111,23 +110,6 @@ __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ u64 pk(float a, float b) {
-  u64 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void upk(u64 v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-// d = a*b + c on two fp32 lanes, each lane rounded once
-__device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
-  u64 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
-__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
-
 // Store 8 consecutive fp16 activations starting at element e0 (a multiple of
 // 8) as fp32 into the pair layout: element 64*c + 32*h + k goes to
 // y2f[2*(k*C + c) + h].
@@ -143,23 +125,6 @@ __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32
     const float f = (e & 1) ? __high2float(v) : __low2float(v);
     y2f[2 * (k * C + c) + h] = __fmul_rn(f, pow2f(-o));
   }
-}
-
-// v' = ((a & m) | 0x4B000000, (b & m) | 0x4B000000) - off on two fp32 lanes.
-// With m = (2^bits - 1) << o the magic float is 2^23 + u*2^o exactly, and
-// off = 2^23 + 2^(bits-1)*2^o, so v' = (u - 2^(bits-1)) * 2^o = v * 2^o
-// exactly.  Both LOP3s write the halves of one register pair that the paired
-// add reads.
-__device__ __forceinline__ u64 decode2(uint32_t a, uint32_t b, uint32_t m, u64 off) {
-  u64 v;
-  asm("{\n\t.reg .b32 t0, t1;\n\t.reg .b64 t;\n\t"
-      "lop3.b32 t0, %1, %3, 0x4B000000, 0xEA;\n\t"
-      "lop3.b32 t1, %2, %3, 0x4B000000, 0xEA;\n\t"
-      "mov.b64 t, {t0, t1};\n\t"
-      "sub.rn.f32x2 %0, t, %4;\n\t}"
-      : "=l"(v)
-      : "r"(a), "r"(b), "r"(m), "l"(off));
-  return v;
 }
 
 // Both blocks of one 64-code item, for U rows at once.  w[u][0 .. 2*WPB-1]:
