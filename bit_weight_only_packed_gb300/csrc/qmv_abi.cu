@@ -132,15 +132,20 @@ static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s, int mode) {
   if (a.M > 32 && mode == QMV_FAST && bits == 2 && !a.fused) {
     const int M = a.M;
     const size_t ysz = a.y_f16 ? 2 : 4;
+    bool done = true;
     for (int m0 = 0; m0 < M; m0 += 128) {
       qmv::GemvArgs b = a;
       b.M = (M - m0 < 128) ? (M - m0) : 128;
       b.x = a.x + (int64_t)m0 * a.K;
       b.y = (char*)a.y + (size_t)m0 * (size_t)a.N * ysz;
       rc = qmv::launch_tc_gemm(b, bits, s, &err);
+      if (rc == QMV_ERR_UNSUPPORTED && m0 == 0) {   // shape outside the tensor tiles:
+        done = false;                                // the exact CUDA-core tiles below
+        break;
+      }
       if (rc != QMV_OK) return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
     }
-    return QMV_OK;
+    if (done) return QMV_OK;
   }
   if (a.M == 1) {
     rc = qmv::launch_gemv_tma(a, bits, s, &err);

@@ -11,19 +11,25 @@
 //
 // One CTA computes a 128-row x MT-token tile (MT = 64 or 128) over a K range
 // (split-K when there are fewer row tiles than SMs; partial tiles are added
-// into y with fp32 reductions).  Warps 0..3 stream the packed codes and the
-// activations, decode the weights into fp16 and write both operands into a
-// ring of shared-memory stages in the 128-byte-swizzled K-major layout; warp
-// 4 allocates the accumulator in tensor memory and issues tcgen05.mma (M=128,
-// N=MT, K=16; four per 64-wide K slab) from one thread, releasing each stage
-// with tcgen05.commit on the stage's mbarrier.  The epilogue reads the
-// accumulator back with tcgen05.ld (warp w owns TMEM lanes 32w..32w+31, i.e.
-// weight rows 32w..32w+31 of the tile).
-//
-// Inside every 16-code word the k order in shared memory is permuted the
-// same way for both operands (position 2i holds code i, position 2i+1 holds
-// code i+8): a dot product does not depend on the order of its terms, and
-// this order is the one in which the half2 decode yields the codes.
+// into y with fp32 reductions).  Roles:
+//   warp 8 (one thread): TMA of the packed codes and scales of the tile, 4
+//     K-slabs (256 codes) at a time, into a ring of 4 raw stages (16 slabs of
+//     prefetch).
+//   warp 10 (one thread): TMA of the activation tile of each 64-wide K slab
+//     straight into the MMA operand stage, with a 128-byte-swizzle tensor map
+//     (the K-major layout the MMA reads).
+//   warps 0..7: decode.  Threads r and 128 + r turn the two 32-code blocks of
+//     row r of a slab into fp16 weights w = v*s (half2 magic decode,
+//     re-paired into natural k order) and write them into the stage's
+//     128-byte-swizzled K-major A tile.  At the end they are the epilogue:
+//     tcgen05.ld of their TMEM lane quarter, half of the tile's columns each.
+//   warp 9 (one thread): allocates the accumulator in tensor memory and issues
+//     tcgen05.mma (M=128, N=MT, K=16; four per slab), releasing each stage with
+//     tcgen05.commit on its mbarrier.
+// Every wait is bounded; a wait that runs out records an error code in this
+// file's device error word and the CTA winds down.
+#include <cuda.h>
+
 #include "qmv_internal.cuh"
 
 namespace qmv {
@@ -35,6 +41,14 @@ namespace {
 
 constexpr uint32_t TC_SPIN = 1u << 22;
 constexpr int ERR_TC_TIMEOUT = 16;
+constexpr int RS = 4;          // K slabs per raw stage (256 codes)
+constexpr int NRAW = 2;        // raw stages
+constexpr int NDEC = 8;        // decode (and epilogue) warps
+constexpr int W_RAW = NDEC, W_MMA = NDEC + 1, W_B = NDEC + 2;   // role warps
+constexpr int TC_THREADS = 32 * (NDEC + 3);
+constexpr int RAW_CODES = 128 * RS * 16;   // bytes of codes per raw stage
+constexpr int RAW_SC = 128 * RS * 4;       // bytes of scales per raw stage
+constexpr int RAW_BYTES = RAW_CODES + RAW_SC;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -44,6 +58,10 @@ __device__ __forceinline__ void tc_mbar_init(uint64_t* b, uint32_t count) {
 }
 __device__ __forceinline__ void tc_mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void tc_mbar_arrive_tx(uint64_t* b, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(tx)
+               : "memory");
 }
 __device__ __forceinline__ bool tc_mbar_try(uint64_t* b, uint32_t parity) {
   uint32_t ok;
@@ -66,6 +84,22 @@ __device__ __noinline__ bool tc_wait(uint64_t* b, uint32_t parity, volatile int*
   atomicCAS(&g_tc_error, 0, ERR_TC_TIMEOUT);
   return false;
 }
+// bounded wait that ignores the abort flag (lets issued copies land)
+__device__ __noinline__ void tc_drain(uint64_t* b, uint32_t parity) {
+  for (uint32_t i = 0; i < TC_SPIN; ++i) {
+    if (tc_mbar_try(b, parity)) return;
+    __nanosleep(100);
+  }
+  atomicCAS(&g_tc_error, 0, ERR_TC_TIMEOUT);
+}
+
+__device__ __forceinline__ void tc_tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
 
 // 64-bit shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
 // rows of 128 bytes stacked in 1024-byte groups of 8 (SBO = 1024 B).
@@ -87,9 +121,7 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 }  // namespace
 
 struct TcArgs {
-  const uint32_t* codes;   // int2 words [N][K/16]
-  const __half* scales;    // [N][G]
-  const __half* x;         // [M][K]
+  const __half* scales;    // [N][G] (one scale per row when perrow)
   float* y;                // [M][N] fp32 (reduced into when split > 1)
   __half* y16;             // [M][N] fp16 output (only without split)
   int N, K, G, M, perrow;
@@ -98,7 +130,9 @@ struct TcArgs {
 };
 
 template <int MT, int NST>
-__global__ void __launch_bounds__(160, 1) tc_gemm_kernel(TcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_gemm_kernel(TcArgs a, const __grid_constant__ CUtensorMap tm_codes,
+                   const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_x) {
   constexpr int A_BYTES = 128 * 128;              // 128 rows x 64 fp16
   constexpr int B_BYTES = MT * 128;               // MT tokens x 64 fp16
   constexpr int STAGE = A_BYTES + B_BYTES;
@@ -110,29 +144,37 @@ __global__ void __launch_bounds__(160, 1) tc_gemm_kernel(TcArgs a) {
   const uint32_t raw = smem_u32(tc_smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
   unsigned char* tiles = tc_smem_raw + pad;
-  unsigned char* ctrl = tiles + NST * STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty = full + NST;
-  uint64_t* done = empty + NST;
+  unsigned char* rawbuf = tiles + NST * STAGE;             // NRAW x RAW_BYTES
+  unsigned char* ctrl = rawbuf + NRAW * RAW_BYTES;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* b_full = a_full + NST;
+  uint64_t* empty = b_full + NST;
+  uint64_t* raw_full = empty + NST;
+  uint64_t* raw_empty = raw_full + NRAW;
+  uint64_t* done = raw_empty + NRAW;
   volatile int* abort_f = reinterpret_cast<volatile int*>(done + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n0 = (int64_t)blockIdx.x * 128;
+  const int n0 = blockIdx.x * 128;
   const int slab0 = blockIdx.y * a.slabs_per_split;
-  const int nslab_total = a.K / 64;
-  const int nslab = min(a.slabs_per_split, nslab_total - slab0);
+  const int nslab = min(a.slabs_per_split, a.K / 64 - slab0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
-      tc_mbar_init(&full[s], 128);
+      tc_mbar_init(&a_full[s], NDEC);
+      tc_mbar_init(&b_full[s], 1);
       tc_mbar_init(&empty[s], 1);
+    }
+    for (int r = 0; r < NRAW; ++r) {
+      tc_mbar_init(&raw_full[r], 1);
+      tc_mbar_init(&raw_empty[r], NDEC);
     }
     tc_mbar_init(done, 1);
     *abort_f = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) {
+  if (warp == W_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"((uint32_t)MT)
@@ -144,12 +186,43 @@ __global__ void __launch_bounds__(160, 1) tc_gemm_kernel(TcArgs a) {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == W_RAW) {
+    // ------------------------------------------- TMA: packed codes/scales --
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nslab; i += RS) {
+        const int j = i / RS, rr = j % NRAW;
+        if (j >= NRAW && !tc_wait(&raw_empty[rr], ((j / NRAW) - 1) & 1, abort_f)) break;
+        unsigned char* rb = rawbuf + rr * RAW_BYTES;
+        tc_mbar_arrive_tx(&raw_full[rr], a.perrow ? RAW_CODES : RAW_BYTES);
+        tc_tma2d(rb, &tm_codes, (slab0 + i) * 4, n0, &raw_full[rr]);
+        if (!a.perrow) tc_tma2d(rb + RAW_CODES, &tm_scales, (slab0 + i) * 2, n0, &raw_full[rr]);
+        ++issued;
+      }
+      for (int j = (issued > NRAW ? issued - NRAW : 0); j < issued; ++j)
+        tc_drain(&raw_full[j % NRAW], (j / NRAW) & 1);
+    }
+  } else if (warp == W_B) {
+    // --------------------------------------------- TMA: activation tiles --
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < nslab; ++i) {
+        const int s = i % NST;
+        if (i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f)) break;
+        tc_mbar_arrive_tx(&b_full[s], B_BYTES);
+        tc_tma2d(tiles + s * STAGE + A_BYTES, &tm_x, (slab0 + i) * 64, 0, &b_full[s]);
+        ++issued;
+      }
+      for (int i = (issued > NST ? issued - NST : 0); i < issued; ++i)
+        tc_drain(&b_full[i % NST], (i / NST) & 1);
+    }
+  } else if (warp == W_MMA) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       for (int i = 0; i < nslab; ++i) {
         const int s = i % NST;
-        if (!tc_wait(&full[s], (i / NST) & 1, abort_f)) break;
+        if (!tc_wait(&a_full[s], (i / NST) & 1, abort_f)) break;
+        if (!tc_wait(&b_full[s], (i / NST) & 1, abort_f)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t abase = smem_u32(tiles + s * STAGE);
         const uint32_t bbase = abase + A_BYTES;
@@ -176,85 +249,65 @@ __global__ void __launch_bounds__(160, 1) tc_gemm_kernel(TcArgs a) {
           : "memory");
     }
   } else {
-    // -------------------------------------- producers (128 threads) ------
-    const int tid = threadIdx.x;     // weight row of the tile; token for B
-    const int64_t row = n0 + tid;
-    const bool row_ok = row < a.N;
-    const int wpr = a.K / 16;        // words per row
+    // ------------------------------- decode (NDEC warps, 2 per weight row) --
+    const int row = threadIdx.x & 127;      // weight row of the tile
+    const int blk = threadIdx.x >> 7;       // which 32-code block of the slab
+    const uint32_t prs = a.perrow && n0 + row < a.N
+                             ? (uint32_t)__half_as_ushort(__ldg(a.scales + n0 + row))
+                             : 0u;
     for (int i = 0; i < nslab; ++i) {
+      const int j = i / RS, rr = j % NRAW, sub = i % RS;
       const int s = i % NST;
-      const int slab = slab0 + i;
-      // operands for this slab (loaded before waiting for the stage)
-      uint4 cw = make_uint4(0u, 0u, 0u, 0u);
-      uint32_t sc2 = 0u;
-      if (row_ok) {
-        cw = __ldg(reinterpret_cast<const uint4*>(a.codes + row * wpr + slab * 4));
-        if (a.perrow) {
-          const uint32_t sh = (uint32_t)__half_as_ushort(__ldg(a.scales + row));
-          sc2 = sh | (sh << 16);
-        } else {
-          sc2 = __ldg(reinterpret_cast<const unsigned int*>(a.scales + row * a.G + slab * 2));
-        }
-      }
-      uint4 xv[8];
-      const bool tok_ok = tid < MT && tid < a.M;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        xv[c] = tok_ok ? __ldg(reinterpret_cast<const uint4*>(a.x + (int64_t)tid * a.K + slab * 64 + 8 * c))
-                       : make_uint4(0u, 0u, 0u, 0u);
+      if (sub == 0 && !tc_wait(&raw_full[rr], (j / NRAW) & 1, abort_f)) break;
       if (i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f)) break;
+      const unsigned char* rb = rawbuf + rr * RAW_BYTES;
+      const uint2 cw = *reinterpret_cast<const uint2*>(rb + row * (RS * 16) + sub * 16 + blk * 8);
+      uint32_t sb = prs;
+      if (!a.perrow)
+        sb = *reinterpret_cast<const uint16_t*>(rb + RAW_CODES + row * (RS * 4) + sub * 4 + blk * 2);
+      const __half2 s2 = u32_as_h2(sb | (sb << 16));
       unsigned char* A = tiles + s * STAGE;
-      unsigned char* B = A + A_BYTES;
-      // A: 4 words = 64 codes; word wi covers k = 16 wi .. 16 wi + 15 (two chunks)
-      const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+      const uint32_t words[2] = {cw.x, cw.y};
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        const __half2 s2 = u32_as_h2((blk == 0) ? ((sc2 & 0xFFFFu) | (sc2 << 16))
-                                                : ((sc2 >> 16) | (sc2 & 0xFFFF0000u)));
+      for (int wj = 0; wj < 2; ++wj) {
+        const int wi = 2 * blk + wj;
+        __half2 vp[8];
+        decode_word<2>(words[wj], vp);   // vp[i] = (v_i, v_{i+8})
+        uint32_t o[8];
 #pragma unroll
-        for (int wj = 0; wj < 2; ++wj) {
-          const int wi = 2 * blk + wj;
-          __half2 vp[8];
-          decode_word<2>(words[wi], vp);
-          uint32_t o[8];
-#pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const __half2 w2 = __hmul2(vp[p], s2);       // exact: v in {-2..1}
-            o[p] = *reinterpret_cast<const uint32_t*>(&w2);
-          }
-          *reinterpret_cast<uint4*>(A + sw128_off(tid, 2 * wi)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(A + sw128_off(tid, 2 * wi + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+        for (int q = 0; q < 4; ++q) {
+          // natural order: (v_2q, v_2q+1) and (v_8+2q, v_9+2q)
+          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&vp[2 * q]);
+          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&vp[2 * q + 1]);
+          const __half2 lo = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x5410)), s2);   // exact
+          const __half2 hi = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x7632)), s2);
+          o[q] = *reinterpret_cast<const uint32_t*>(&lo);
+          o[4 + q] = *reinterpret_cast<const uint32_t*>(&hi);
         }
-      }
-      // B: token tid, same permutation inside each 16-element word
-      if (tid < MT) {
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          const uint4 lo = xv[2 * wi], hi = xv[2 * wi + 1];   // x_0..7, x_8..15 of the word
-          const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w}, H[4] = {hi.x, hi.y, hi.z, hi.w};
-          uint32_t o[8];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            o[2 * j] = __byte_perm(L[j], H[j], 0x5410);      // (x_2j, x_8+2j)
-            o[2 * j + 1] = __byte_perm(L[j], H[j], 0x7632);  // (x_2j+1, x_9+2j)
-          }
-          *reinterpret_cast<uint4*>(B + sw128_off(tid, 2 * wi)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(B + sw128_off(tid, 2 * wi + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
+        *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_mbar_arrive(&full[s]);
+      __syncwarp();
+      if (lane == 0) {
+        tc_mbar_arrive(&a_full[s]);
+        if (sub == RS - 1 || i == nslab - 1) tc_mbar_arrive(&raw_empty[rr]);
+      }
     }
 
     // --------------------------------------------------------- epilogue --
-    if (tc_wait(done, 0, abort_f)) {
+    // warp w reads TMEM lanes 32*(w%4) .. +31 (its lane quarter), columns of
+    // its half of the tile's tokens
+    if (nslab > 0 && tc_wait(done, 0, abort_f)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int r = 32 * warp + lane;
-      const int64_t n = n0 + r;
+      const int q4 = warp & 3;
+      const int r = 32 * q4 + lane;
+      const int64_t n = (int64_t)n0 + r;
+      const int cbeg = (warp >> 2) * (MT / 2), cend = cbeg + MT / 2;
 #pragma unroll 1
-      for (int c0 = 0; c0 < MT; c0 += 16) {
+      for (int c0 = cbeg; c0 < cend; c0 += 16) {
         uint32_t v[16];
-        const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)c0;
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
             "%11, %12, %13, %14, %15}, [%16];"
@@ -266,10 +319,10 @@ __global__ void __launch_bounds__(160, 1) tc_gemm_kernel(TcArgs a) {
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (n < a.N) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int m = c0 + j;
+          for (int q = 0; q < 16; ++q) {
+            const int m = c0 + q;
             if (m < a.M) {
-              const float f = __uint_as_float(v[j]);
+              const float f = __uint_as_float(v[q]);
               const int64_t o = (int64_t)m * a.N + n;
               if (a.split > 1)
                 atomicAdd(a.y + o, f);
@@ -285,44 +338,11 @@ __global__ void __launch_bounds__(160, 1) tc_gemm_kernel(TcArgs a) {
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 4) {
+  if (warp == W_MMA) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)MT)
                  : "memory");
   }
-}
-
-template <int MT, int NST>
-static int run_tc(const TcArgs& a0, int tiles, cudaStream_t s, cudaError_t* err) {
-  constexpr int STAGE = 128 * 128 + MT * 128;
-  const size_t smem = 1024 + (size_t)NST * STAGE + 256;
-  static thread_local int set_dev = -1;
-  auto kern = tc_gemm_kernel<MT, NST>;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
-  if (set_dev != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
-    set_dev = dev;
-  }
-  TcArgs a = a0;
-  const int nslab = a.K / 64;
-  const int sms = dev_info().sms;
-  int split = 1;
-  if (a.y16 == nullptr) {
-    while (tiles * split * 2 <= sms && nslab / (split * 2) >= 8) split *= 2;
-  }
-  a.split = split;
-  a.slabs_per_split = (nslab + split - 1) / split;
-  if (split > 1) {
-    e = cudaMemsetAsync(a.y, 0, (size_t)a.M * a.N * sizeof(float), s);
-    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
-  }
-  kern<<<dim3(tiles, split), 160, smem, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
-  return QMV_OK;
 }
 
 int read_tc_error(int clear, int* out) {
@@ -338,13 +358,98 @@ int read_tc_error(int clear, int* out) {
   return 0;
 }
 
-// M in 33 .. 128 token columns, int2 weights; y fp32 or fp16.
+// ------------------------------------------------------------- launcher --
+
+typedef CUresult (*TcEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                               const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static TcEncodeFn tc_encode_fn() {
+  static TcEncodeFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (TcEncodeFn) nullptr;
+    return (TcEncodeFn)f;
+  }();
+  return fn;
+}
+
+static bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  TcEncodeFn enc = tc_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MT, int NST>
+static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s, cudaError_t* err) {
+  constexpr int STAGE = 128 * 128 + MT * 128;
+  const size_t smem = 1024 + (size_t)NST * STAGE + (size_t)NRAW * RAW_BYTES + 256;
+  static thread_local int set_dev = -1;
+  auto kern = tc_gemm_kernel<MT, NST>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  if (set_dev != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+    set_dev = dev;
+  }
+  // tensor maps: codes as UINT32 [N][K/16] (box 4*RS x 128), scales as UINT16
+  // [N][K/32] (box 2*RS x 128), activations as FP16 [M][K] (box 64 x MT,
+  // 128-byte swizzle = the MMA's K-major operand layout).  Rows past N or M
+  // and columns past K are zero-filled.
+  CUtensorMap tmc, tms, tmx;
+  if (!enc2d(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.codes, (uint64_t)g.K / 16, (uint64_t)g.N,
+             (uint64_t)g.K / 4, 4 * RS, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return QMV_ERR_UNSUPPORTED;
+  if (g.perrow) {
+    tms = tmc;   // unused
+  } else if (!enc2d(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.scales, (uint64_t)g.G, (uint64_t)g.N,
+                    (uint64_t)g.G * 2, 2 * RS, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    return QMV_ERR_UNSUPPORTED;
+  }
+  if (!enc2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.x, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K * 2,
+             64, MT, CU_TENSOR_MAP_SWIZZLE_128B))
+    return QMV_ERR_UNSUPPORTED;
+  TcArgs a = a0;
+  const int nslab = a.K / 64;
+  const int sms = dev_info().sms;
+  int split = 1;
+  if (a.y16 == nullptr) {
+    while (tiles * split * 2 <= sms && nslab / (split * 2) >= 8) split *= 2;
+  }
+  a.split = split;
+  // whole raw stages per split, so every box starts on a 16-byte boundary
+  a.slabs_per_split = (((nslab + split - 1) / split) + RS - 1) / RS * RS;
+  while (split > 1 && (split - 1) * a.slabs_per_split >= nslab) {
+    --split;
+    a.split = split;
+  }
+  if (split > 1) {
+    e = cudaMemsetAsync(a.y, 0, (size_t)a.M * a.N * sizeof(float), s);
+    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  }
+  kern<<<dim3(tiles, split), TC_THREADS, smem, s>>>(a, tmc, tms, tmx);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  return QMV_OK;
+}
+
+// M in 1 .. 128 token columns, int2 weights; y fp32 or fp16.
 int launch_tc_gemm(const GemvArgs& g, int bits, cudaStream_t s, cudaError_t* err) {
-  if (bits != 2 || g.fused || g.M < 1 || g.M > 128 || g.K % 64 != 0) return QMV_ERR_UNSUPPORTED;
+  if (bits != 2 || g.fused || g.M < 1 || g.M > 128 || g.K % 256 != 0) return QMV_ERR_UNSUPPORTED;
   TcArgs a;
-  a.codes = reinterpret_cast<const uint32_t*>(g.codes);
   a.scales = g.scales;
-  a.x = g.x;
   a.y = g.y_f16 ? nullptr : reinterpret_cast<float*>(g.y);
   a.y16 = g.y_f16 ? reinterpret_cast<__half*>(g.y) : nullptr;
   a.N = g.N;
@@ -355,8 +460,8 @@ int launch_tc_gemm(const GemvArgs& g, int bits, cudaStream_t s, cudaError_t* err
   a.split = 1;
   a.slabs_per_split = g.K / 64;
   const int tiles = (g.N + 127) / 128;
-  if (g.M <= 64) return run_tc<64, 4>(a, tiles, s, err);
-  return run_tc<128, 3>(a, tiles, s, err);
+  if (g.M <= 64) return run_tc<64, 8>(a, g, tiles, s, err);
+  return run_tc<128, 5>(a, g, tiles, s, err);
 }
 
 }  // namespace qmv
