@@ -124,11 +124,16 @@ static qmv::GemvArgs base_args(const qmv_pack* p, int M, const void* x, void* y,
 
 // Dispatch: M = 1 -> the bulk-copy pipeline kernel (or the generic one);
 // M <= 32, or any M in exact mode, or int4/int8 -> CUDA-core tiles, 32
-// columns per launch (bit-exact); M > 32 in fast mode with int2 weights ->
-// tcgen05 tensor-core tiles, 128 columns per launch.
+// columns per launch (each column equal to the M = 1 result); M > 32 in fast
+// mode with int2 weights -> tcgen05 tensor-core tiles, 128 columns per
+// launch.
 static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s, int mode) {
   cudaError_t err = cudaSuccess;
   int rc;
+  // fast mode: the folded-offset form, in the M = 1 pipeline and the
+  // M-column tiles alike, for the shapes the pipeline runs (elsewhere both
+  // keep the exact form, so a tile column always equals the M = 1 result)
+  a.folded = (mode == QMV_FAST && qmv::tma_fits(a.K, bits, a.perrow != 0)) ? 1 : 0;
   if (a.M > 32 && mode == QMV_FAST && bits == 2 && !a.fused) {
     const int M = a.M;
     const size_t ysz = a.y_f16 ? 2 : 4;

@@ -178,4 +178,40 @@ __device__ __forceinline__ u64 decode2(uint32_t a, uint32_t b, uint32_t m, u64 o
   return v;
 }
 
+// ---- fast mode: the folded-offset form ------------------------------------
+//
+// With v = u - 2^(b-1), a block's dot is sum_k y_k*u_k - 2^(b-1)*S where
+// S = sum_k y_k, so the offset can be taken out of the per-code work.  A field
+// at bit offset o (o + b <= 16) masked in place, (w & (mask << o)), read as
+// fp32 bits is the subnormal u * 2^o * 2^-149 exactly.  With the activation
+// pre-scaled to y' = y * 2^(FOLD_E - o) one paired FMA adds y*u*2^-40 (an
+// exact product, |y'| < 2^125 for every finite fp16 y, and every nonzero
+// product is a normal number) to the block's running sum P: one mask per code
+// and one paired FMA per two codes, no subtraction.  The block result is
+// fma(P, 2^40, -2^(b-1)*S) (P*2^40 is exact), then scaled as in the exact
+// form.  The sums differ from the exact form's serial order only by rounding,
+// so this is the fast mode's arithmetic.  S is the serial fp32 sum of the
+// block's activations in k order, the order of the dot itself: P is then
+// exactly 2^-40 times the serial sum of y*u, a block of zero weights (u =
+// 2^(b-1) throughout) gives exactly 0, and every kernel that uses the form
+// agrees bit for bit.
+constexpr int FOLD_E = 109;
+
+// (a & m, b & m) as two fp32 lanes (subnormal field values)
+__device__ __forceinline__ u64 fields2(uint32_t a, uint32_t b, uint32_t m) {
+  u64 v;
+  asm("{\n\t.reg .b32 t0, t1;\n\t"
+      "and.b32 t0, %1, %3;\n\t"
+      "and.b32 t1, %2, %3;\n\t"
+      "mov.b64 %0, {t0, t1};\n\t}"
+      : "=l"(v)
+      : "r"(a), "r"(b), "r"(m));
+  return v;
+}
+
+// block result from the running sum P (units of 2^-40) and bS = 2^(b-1)*S
+__device__ __forceinline__ float fold_block(float P, float bS) {
+  return __fmaf_rn(P, 1099511627776.0f /* 2^40 */, -bS);
+}
+
 }  // namespace qmv

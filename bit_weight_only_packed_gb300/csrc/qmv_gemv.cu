@@ -32,7 +32,7 @@
 //     activations from shared memory as broadcasts.  Fold threads own fixed
 //     (row, column) pairs and keep their accumulators in registers across
 //     slabs.
-#include "qmv_internal.cuh"
+#include "qmv_prologue.cuh"
 
 namespace qmv {
 
@@ -41,52 +41,6 @@ constexpr int M1_MAXT = 672;   // largest CTA of gemv_m1 (C*RP, a multiple of 32
 // CTAs of up to 256 threads keep 4 passes in flight; larger CTAs (long or
 // odd K) keep 2, so that two register sets still fit without spills.
 template <int MAXT> struct M1Lim { static constexpr int UM = (MAXT > 256) ? 2 : 4; };
-
-__device__ __forceinline__ uint4 ldg16(const uint4* p) { return __ldg(p); }
-
-__device__ __forceinline__ uint4 lds16(const __half* p) { return *reinterpret_cast<const uint4*>(p); }
-
-__device__ __forceinline__ __half h_of(const uint4& v, int e) {
-  const uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
-  return __ushort_as_half((e & 1) ? (uint16_t)(w >> 16) : (uint16_t)(w & 0xFFFFu));
-}
-
-// inv = 1 / sqrt(ss / K + eps), each step one IEEE fp32 operation
-__device__ __forceinline__ float rms_inv(float ss, int K, float eps) {
-  const float mean = __fdiv_rn(ss, (float)K);
-  const float t = __fadd_rn(mean, eps);
-  const float rt = __fsqrt_rn(t);
-  return __fdiv_rn(1.0f, rt);
-}
-
-__device__ __forceinline__ __half add_h(__half x, __half r) {
-  return __float2half_rn(__fadd_rn(__half2float(x), __half2float(r)));
-}
-
-__device__ __forceinline__ __half norm_h(__half h, float inv, __half g) {
-  return __float2half_rn(__fmul_rn(__fmul_rn(__half2float(h), inv), __half2float(g)));
-}
-
-// Block sum of squares of h = fp16(x + r) over the 32 codes at k0, serial in
-// k; optionally stores h.  Squares of fp16 values are exact in fp32, so the
-// fused multiply-add equals the rounded add of the square.
-__device__ __forceinline__ float block_sumsq(const __half* x, const __half* r, int k0,
-                                             __half* h_store) {
-  float blk = 0.0f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + k0 + 8 * q));
-    const uint4 rv = __ldg(reinterpret_cast<const uint4*>(r + k0 + 8 * q));
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const __half h = add_h(h_of(xv, e), h_of(rv, e));
-      if (h_store) h_store[k0 + 8 * q + e] = h;
-      const float hf = __half2float(h);
-      blk = __fmaf_rn(hf, hf, blk);
-    }
-  }
-  return blk;
-}
 
 // ============================================================== M = 1 ====
 
@@ -426,280 +380,8 @@ __global__ void __launch_bounds__(256) gemm_small_kernel(GemvArgs a) {
   }
 }
 
-// ============================================ M-column tiles, paired fp32 ====
-//
-// The same computation as gemm_small_kernel for K a multiple of 64, on the
-// arithmetic of the M = 1 pipeline: every 64-code item (two 32-code blocks)
-// is decoded per position into the exact fp32 pair (v_k, v_{32+k}) * 2^o with
-// two LOP3s and one paired subtract, and one fma.rn.f32x2 per column advances
-// that column's two block chains, with the activations pre-scaled by 2^-o in
-// shared memory ((y*2^-o)*(v*2^o) = y*v exactly, so each step is the oracle's
-// rounded fp32 add).  Lanes are rows; warp w takes item w of each 512-code
-// slab; a column's activation pairs are read as shared-memory broadcasts, two
-// columns per 16-byte load; columns are processed 16 at a time.
-
-constexpr int TL_WARPS = 8;
-constexpr int TL_SLAB = TL_WARPS * 64;   // codes per slab
-constexpr int TL_SB = TL_SLAB / 32;      // blocks per slab
-
-template <int MT, int U> struct TileCfg {
-  static constexpr int ROWS = 32 * U;                // rows per CTA (U per lane)
-  static constexpr int PAIRS = ROWS * MT;
-  static constexpr int PPT = (PAIRS + 255) / 256;
-  static constexpr int MS = MT + 2;                  // padded column stride of the pair table
-  static constexpr int YP = TL_WARPS * 32 * MS;      // activation pairs (u64) per slab
-  static constexpr int TB = TL_SB * MT * ROWS;       // fold buffer floats
-};
-
-template <int MT, int U>
-__host__ __device__ inline size_t tile_smem_bytes(int NB, bool fused) {
-  using S = TileCfg<MT, U>;
-  size_t b = (size_t)S::YP * 8 + (size_t)S::TB * 4 + (size_t)((MT + 3) & ~3) * 4;
-  if (fused) b += (size_t)MT * NB * 4;
-  return b;
-}
-
-template <int BITS, int MT, int U>
-__global__ void __launch_bounds__(256) gemm_tile_kernel(GemvArgs a) {
-  using S = TileCfg<MT, U>;
-  static_assert(MT % 2 == 0, "column chunks are whole pairs");
-  constexpr int IW = 64 * BITS / 32;      // words per item
-  constexpr int CPW = 32 / BITS, HALF = CPW / 2, WPB = 32 / CPW;
-  constexpr uint32_t MASK = (1u << BITS) - 1u;
-  constexpr int MTC = (MT < 16) ? MT : 16;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  // blockIdx.y selects a chunk of MT token columns (column split when there
-  // are few row tiles)
-  const int mc0 = blockIdx.y * MT;
-  a.x += (int64_t)mc0 * a.K;
-  if (a.fused) {
-    a.r += (int64_t)mc0 * a.K;
-    if (a.h_out) a.h_out += (int64_t)mc0 * a.K;
-  }
-  a.y = a.y_f16 ? (void*)(reinterpret_cast<__half*>(a.y) + (int64_t)mc0 * a.N)
-                : (void*)(reinterpret_cast<float*>(a.y) + (int64_t)mc0 * a.N);
-  a.M = min(MT, a.M - mc0);
-  const int K = a.K, NB = K / 32, M = a.M;
-  const int64_t row0 = (int64_t)blockIdx.x * S::ROWS;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  u64* yp = reinterpret_cast<u64*>(smem_raw);                 // [item][k][m], stride MT+2
-  float* tb = reinterpret_cast<float*>(yp + S::YP);           // [block][m][row]
-  float* inv = tb + S::TB;
-  float* bsum = inv + ((MT + 3) & ~3);
-
-  if (a.fused) {
-    for (int e = t; e < M * NB; e += 256) {
-      const int m = e / NB, b = e % NB;
-      bsum[m * NB + b] = block_sumsq(a.x + (int64_t)m * K, a.r + (int64_t)m * K, b * 32, nullptr);
-    }
-    __syncthreads();
-    if (t < M) {
-      float ss = 0.0f;
-      for (int b = 0; b < NB; ++b) ss = __fadd_rn(ss, bsum[t * NB + b]);
-      inv[t] = rms_inv(ss, K, a.eps);
-    }
-    __syncthreads();
-  }
-
-  float acc[S::PPT];
-#pragma unroll
-  for (int i = 0; i < S::PPT; ++i) acc[i] = 0.0f;
-
-  for (int s0 = 0; s0 < K; s0 += TL_SLAB) {
-    const int items = min(TL_WARPS, (K - s0) / 64);
-    // stage the slab's activations: (1) coalesced 16-byte loads (the fused
-    // path forms h and y here) into an fp16 buffer [m][512] that aliases the
-    // fold buffer (free between the fold and the block sums); (2) re-layout
-    // into fp32 pairs (y_k, y_{32+k}) * 2^-o(k), [item][k][m] with column
-    // stride MT+2, threads walking k fastest (conflict-free reads and stores)
-    __half* y16 = reinterpret_cast<__half*>(tb);
-    for (int e = t; e < MT * items * 8; e += 256) {
-      const int m = e / (items * 8), kk = 8 * (e % (items * 8));
-      uint4 out = make_uint4(0u, 0u, 0u, 0u);
-      if (m < M) {
-        const int64_t off = (int64_t)m * K + s0 + kk;
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + off));
-        if (a.fused) {
-          const uint4 rv = __ldg(reinterpret_cast<const uint4*>(a.r + off));
-          const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + s0 + kk));
-          const float iv = inv[m];
-          uint16_t hh[8], yy[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const __half h = add_h(h_of(xv, q), h_of(rv, q));
-            hh[q] = __half_as_ushort(h);
-            yy[q] = __half_as_ushort(norm_h(h, iv, h_of(gv, q)));
-          }
-          if (a.h_out && blockIdx.x == 0) {
-            uint4 hv;
-            memcpy(&hv, hh, 16);
-            *reinterpret_cast<uint4*>(a.h_out + off) = hv;
-          }
-          memcpy(&out, yy, 16);
-        } else {
-          out = xv;
-        }
-      }
-      *reinterpret_cast<uint4*>(y16 + m * TL_SLAB + kk) = out;
-    }
-    __syncthreads();
-    for (int e = t; e < items * 32 * MT; e += 256) {
-      const int k = e & 31, m = (e >> 5) % MT, it = (e >> 5) / MT;
-      const float sc = pow2f(-BITS * ((k % CPW) % HALF));
-      const float v0 = __fmul_rn(__half2float(y16[m * TL_SLAB + 64 * it + k]), sc);
-      const float v1 = __fmul_rn(__half2float(y16[m * TL_SLAB + 64 * it + 32 + k]), sc);
-      yp[(it * 32 + k) * S::MS + m] = pk(v0, v1);
-    }
-    __syncthreads();
-
-    if (warp < items) {
-      // item `warp` of this slab for rows lane + 32u of the tile
-      const int item = s0 / 64 + warp;
-      uint32_t w[U][IW];
-      float s_lo[U], s_hi[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t row = row0 + lane + 32 * u;
-        uint32_t sc = 0u;
-        if (row < a.N) {
-          const uint4* src = a.codes + row * a.row_u4 + (int64_t)item * (IW / 4);
-#pragma unroll
-          for (int q = 0; q < IW / 4; ++q) {
-            const uint4 v = ldg16(src + q);
-            w[u][4 * q] = v.x; w[u][4 * q + 1] = v.y; w[u][4 * q + 2] = v.z; w[u][4 * q + 3] = v.w;
-          }
-          if (!a.perrow) sc = __ldg(reinterpret_cast<const unsigned int*>(a.scales + row * a.G + (int64_t)item * 2));
-        } else {
-#pragma unroll
-          for (int q = 0; q < IW; ++q) w[u][q] = 0u;
-        }
-        s_lo[u] = __half2float(__ushort_as_half((uint16_t)(sc & 0xFFFFu)));
-        s_hi[u] = __half2float(__ushort_as_half((uint16_t)(sc >> 16)));
-      }
-      const u64* yit = yp + (size_t)warp * 32 * S::MS;
-#pragma unroll 1
-      for (int c0 = 0; c0 < MT; c0 += MTC) {
-        u64 acc2[U][MTC];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-          for (int mm = 0; mm < MTC; ++mm) acc2[u][mm] = 0ull;
-#pragma unroll
-        for (int wi = 0; wi < WPB; ++wi) {
-          uint32_t h0[U], h1[U];
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            h0[u] = w[u][wi] >> 16;
-            h1[u] = w[u][WPB + wi] >> 16;
-          }
-#pragma unroll
-          for (int j = 0; j < CPW; ++j) {
-            const int o = BITS * (j % HALF);
-            const float offf = pow2f(23) + (float)(1 << (BITS - 1 + o));
-            u64 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-              v[u] = decode2((j < HALF) ? w[u][wi] : h0[u], (j < HALF) ? w[u][WPB + wi] : h1[u],
-                             MASK << o, pk(offf, offf));
-            const u64* yk = yit + (wi * CPW + j) * S::MS + c0;
-#pragma unroll
-            for (int mm = 0; mm < MTC; mm += 2) {
-              const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
-#pragma unroll
-              for (int u = 0; u < U; ++u) {
-                acc2[u][mm] = ffma2(y2.x, v[u], acc2[u][mm]);
-                acc2[u][mm + 1] = ffma2(y2.y, v[u], acc2[u][mm + 1]);
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-#pragma unroll
-          for (int mm = 0; mm < MTC; ++mm) {
-            float p0, p1;
-            upk(acc2[u][mm], p0, p1);
-            const int r = lane + 32 * u;
-            tb[((2 * warp) * MT + c0 + mm) * S::ROWS + r] = a.perrow ? p0 : __fmul_rn(p0, s_lo[u]);
-            tb[((2 * warp + 1) * MT + c0 + mm) * S::ROWS + r] = a.perrow ? p1 : __fmul_rn(p1, s_hi[u]);
-          }
-      }
-    }
-    __syncthreads();
-
-    // fold this slab's blocks, in order, into the (row, column) accumulators
-    const int sbe = 2 * items;
-#pragma unroll
-    for (int i = 0; i < S::PPT; ++i) {
-      const int pq = t + 256 * i;
-      if (pq < S::PAIRS) {
-        const int prow = pq % S::ROWS, pm = pq / S::ROWS;
-        float v = acc[i];
-        for (int b = 0; b < sbe; ++b) v = __fadd_rn(v, tb[(b * MT + pm) * S::ROWS + prow]);
-        acc[i] = v;
-      }
-    }
-    // the next slab's staging reuses the fold buffer
-    __syncthreads();
-  }
-
-#pragma unroll
-  for (int i = 0; i < S::PPT; ++i) {
-    const int pq = t + 256 * i;
-    if (pq < S::PAIRS) {
-      const int prow = pq % S::ROWS, pm = pq / S::ROWS;
-      const int64_t r = row0 + prow;
-      if (r < a.N && pm < M) {
-        float v = acc[i];
-        if (a.perrow) v = __fadd_rn(0.0f, __fmul_rn(v, __half2float(a.scales[r])));
-        const int64_t o = (int64_t)pm * a.N + r;
-        if (a.y_f16)
-          reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(v);
-        else
-          reinterpret_cast<float*>(a.y)[o] = v;
-      }
-    }
-  }
-}
 
 // ============================================================ launchers ====
-
-// Per-kernel launch facts, cached per device: the dynamic shared-memory limit
-// set so far and the occupancy for one (threads, smem) shape.  This keeps the
-// host cost of a call to a few lookups after the first call.
-struct KernCache {
-  int dev = -1;
-  size_t smem_set = 48 * 1024;
-  int occ_threads = -1;
-  size_t occ_smem = 0;
-  int occ = 0;
-};
-
-template <typename Kern>
-static cudaError_t prep_kernel(Kern k, KernCache& c, int threads, size_t smem, int* occ) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (c.dev != dev) {
-    c = KernCache();
-    c.dev = dev;
-  }
-  if (smem > c.smem_set) {
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    c.smem_set = smem;
-  }
-  if (occ) {
-    if (c.occ_threads != threads || c.occ_smem != smem) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, threads, smem);
-      if (e != cudaSuccess) return e;
-      c.occ_threads = threads;
-      c.occ_smem = smem;
-    }
-    *occ = c.occ;
-  }
-  return cudaSuccess;
-}
 
 template <int BITS, bool PERROW, bool FUSED, int MAXT>
 static int run_m1_t(const GemvArgs& a, int C, int RP, cudaStream_t s, cudaError_t* err) {
@@ -772,40 +454,10 @@ static int run_small(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   return QMV_OK;
 }
 
-template <int BITS, int MT, int U>
-static int run_tile(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
-  const int NB = a.K / 32;
-  const size_t smem = tile_smem_bytes<MT, U>(NB, a.fused != 0);
-  const DevInfo& d = dev_info();
-  if (smem > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
-  auto kern = gemm_tile_kernel<BITS, MT, U>;
-  static thread_local KernCache cache;
-  cudaError_t e = prep_kernel(kern, cache, 256, smem, nullptr);
-  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
-  const int64_t grid = ((int64_t)a.N + 32 * U - 1) / (32 * U);
-  const int chunks = (a.M + MT - 1) / MT;
-  kern<<<dim3((unsigned)grid, (unsigned)chunks), 256, smem, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
-  return QMV_OK;
-}
-
 template <int BITS>
 static int small_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   if (a.K % 64 == 0) {
-    int rc;
-    // two rows per lane (half the activation loads per FMA) where the
-    // registers and the fold buffer allow it
-    constexpr int U2 = (BITS == 8) ? 1 : 2;
-    // column chunk: the whole M, halved (down to 4) while there are fewer
-    // than 2 CTAs per SM of row tiles x chunks
-    int mt = (a.M <= 4) ? 4 : (a.M <= 8) ? 8 : (a.M <= 16) ? 16 : 32;
-    const int64_t sms2 = 2LL * dev_info().sms;
-    while (mt > 4 && (((int64_t)a.N + 63) / 64) * ((a.M + mt - 1) / mt) < sms2) mt /= 2;
-    if (mt == 4) rc = run_tile<BITS, 4, U2>(a, s, err);
-    else if (mt == 8) rc = run_tile<BITS, 8, U2>(a, s, err);
-    else if (mt == 16) rc = run_tile<BITS, 16, U2>(a, s, err);
-    else rc = run_tile<BITS, 32, 1>(a, s, err);
+    const int rc = launch_tile(a, BITS, s, err);
     if (rc != QMV_ERR_UNSUPPORTED) return rc;
   }
   if (a.M <= 4) return run_small<BITS, 4>(a, s, err);
@@ -813,7 +465,6 @@ static int small_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   if (a.M <= 16) return run_small<BITS, 16>(a, s, err);
   return run_small<BITS, 32>(a, s, err);
 }
-
 int launch_gemm_small(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
   if (a.M < 1 || a.M > 32) return QMV_ERR_INVALID_ARG;
   switch (bits) {

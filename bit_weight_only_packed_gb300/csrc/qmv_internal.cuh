@@ -37,6 +37,7 @@ struct GemvArgs {
   int y_f16;
   int M;                      // columns (tokens)
   int fused;
+  int folded;                 // fast mode's folded-offset form (see qmv_decode.cuh)
 };
 
 struct DevInfo {
@@ -54,6 +55,9 @@ int launch_gemm_small(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* 
 // M = 1 through the bulk-copy pipeline; QMV_ERR_UNSUPPORTED if the shape does
 // not fit it (the caller then uses launch_gemv_m1).
 int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+// Whether the pipeline has a plan for this K (the fast mode's folded form is
+// used by the M = 1 pipeline and the M-column tiles exactly when it does).
+bool tma_fits(int K, int bits, bool perrow);
 // tcgen05 tensor-core tiles for 1..128 token columns, int2 weights (fast
 // mode); QMV_ERR_UNSUPPORTED for other widths or the fused prologue.
 int launch_tc_gemm(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
@@ -62,5 +66,46 @@ bool pdl_enabled();
 void set_pdl(bool on);
 // Read (and optionally clear) the device error word set by bounded waits.
 int read_device_error(int clear, int* out);
+// M-column tiles on paired fp32 arithmetic (K a multiple of 64, M <= 32);
+// QMV_ERR_UNSUPPORTED when the shape does not fit them.
+int launch_tile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+
+
+// Per-kernel launch facts, cached per device: the dynamic shared-memory limit
+// set so far and the occupancy for one (threads, smem) shape.  This keeps the
+// host cost of a call to a few lookups after the first call.
+struct KernCache {
+  int dev = -1;
+  size_t smem_set = 48 * 1024;
+  int occ_threads = -1;
+  size_t occ_smem = 0;
+  int occ = 0;
+};
+
+template <typename Kern>
+inline cudaError_t prep_kernel(Kern k, KernCache& c, int threads, size_t smem, int* occ) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (c.dev != dev) {
+    c = KernCache();
+    c.dev = dev;
+  }
+  if (smem > c.smem_set) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    c.smem_set = smem;
+  }
+  if (occ) {
+    if (c.occ_threads != threads || c.occ_smem != smem) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, threads, smem);
+      if (e != cudaSuccess) return e;
+      c.occ_threads = threads;
+      c.occ_smem = smem;
+    }
+    *occ = c.occ;
+  }
+  return cudaSuccess;
+}
 
 }  // namespace qmv

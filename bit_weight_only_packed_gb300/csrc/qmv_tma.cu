@@ -113,7 +113,8 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 // Store 8 consecutive fp16 activations starting at element e0 (a multiple of
 // 8) as fp32 into the pair layout: element 64*c + 32*h + k goes to
 // y2f[2*(k*C + c) + h].
-template <int BITS>
+// Exact form: y * 2^-o(k); folded form: y * 2^(FOLD_E - o(k)).
+template <int BITS, bool EXACT>
 __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32_t (&h8)[4]) {
   constexpr int CPW = 32 / BITS, HALF = CPW / 2;
   const int c = e0 >> 6, h = (e0 >> 5) & 1, k0 = e0 & 31;
@@ -123,7 +124,7 @@ __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32
     const int o = BITS * ((k % CPW) % HALF);
     const __half2 v = u32_as_h2(h8[e >> 1]);
     const float f = (e & 1) ? __high2float(v) : __low2float(v);
-    y2f[2 * (k * C + c) + h] = __fmul_rn(f, pow2f(-o));
+    y2f[2 * (k * C + c) + h] = __fmul_rn(f, pow2f(EXACT ? -o : FOLD_E - o));
   }
 }
 
@@ -135,8 +136,9 @@ __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32
 // y_k * v_k exactly (powers of two; no underflow for fp16 inputs).  acc[u] =
 // (p0, p1) are the two blocks' serial sums.  Fields in the high 16-bit half
 // of a word are first shifted down by 16, so every field is masked below
-// bit 16.
-template <int BITS, int U>
+// bit 16.  In the folded form (fast mode) the masked field itself is the
+// operand and the sums are of y*u*2^-40; the offset is removed per block.
+template <int BITS, int U, bool EXACT>
 __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32],
                                           const u64* __restrict__ y2s, int C, int c,
                                           u64 (&acc)[U]) {
@@ -162,7 +164,7 @@ __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32]
       for (int u = 0; u < U; ++u) {
         const uint32_t a = (j < HALF) ? w[u][wi] : h0[u];
         const uint32_t b = (j < HALF) ? w[u][WPB + wi] : h1[u];
-        const u64 v = decode2(a, b, MASK << o, off);
+        const u64 v = EXACT ? decode2(a, b, MASK << o, off) : fields2(a, b, MASK << o);
         acc[u] = ffma2(y, v, acc[u]);
       }
     }
@@ -192,12 +194,12 @@ struct TmaPlan {
   int sc_off;        // offset of the scales inside a stage (128-byte aligned)
   int stage_bytes;   // whole stage, a multiple of 128 bytes
   int ngroups;       // ceil(N / R)
-  int y_off, stage_off, tbuf_off;   // shared-memory offsets (bytes)
+  int y_off, ysum_off, stage_off, tbuf_off;   // shared-memory offsets (bytes)
 };
 
 __host__ __device__ inline int tma_round16(int x) { return (x + 15) & ~15; }
 
-template <int BITS, bool PERROW, bool FUSED, int U, int MAXT>
+template <int BITS, bool PERROW, bool FUSED, bool EXACT, int U, int MAXT>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     gemv_tma_kernel(GemvArgs a, TmaPlan P, const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_scales) {
@@ -210,6 +212,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   volatile int* abort_f = reinterpret_cast<volatile int*>(sm + 96);
   float* inv_sh = reinterpret_cast<float*>(sm + 100);
   float* y2f = reinterpret_cast<float*>(sm + P.y_off);   // pairs [k][item] as fp32
+  float* ysum = reinterpret_cast<float*>(sm + P.ysum_off); // folded form: 2^(b-1) * S per block
   unsigned char* stages = sm + P.stage_off;
   float* tbuf = reinterpret_cast<float*>(sm + P.tbuf_off);
 
@@ -340,13 +343,27 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
         const __half yh = __float2half_rn(__fmul_rn(__fmul_rn(hh, inv), __high2float(gg)));
         ys[e] = (uint32_t)__half_as_ushort(yl) | ((uint32_t)__half_as_ushort(yh) << 16);
       }
-      store_y8<BITS>(y2f, P.C, 8 * v8, ys);
+      store_y8<BITS, EXACT>(y2f, P.C, 8 * v8, ys);
     }
   } else {
     for (int v8 = tt; v8 < K / 8; v8 += nt) {
       const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 8 * v8));
       const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-      store_y8<BITS>(y2f, P.C, 8 * v8, xs);
+      store_y8<BITS, EXACT>(y2f, P.C, 8 * v8, xs);
+    }
+  }
+  if (!EXACT) {
+    // block sums of the activations, serial in k, read back from the scaled
+    // pairs (y' * 2^(o - FOLD_E) = y exactly), times the offset 2^(b-1)
+    named_bar(1, nt);
+    constexpr int CPW = 32 / BITS, HALF = CPW / 2;
+    for (int b = tt; b < NB; b += nt) {
+      const float* src = y2f + 2 * (b >> 1) + (b & 1);
+      float S = 0.0f;
+#pragma unroll 8
+      for (int k = 0; k < 32; ++k)
+        S = __fmaf_rn(src[2 * k * P.C], pow2f(BITS * ((k % CPW) % HALF) - FOLD_E), S);
+      ysum[b] = __fmul_rn(S, (float)(1 << (BITS - 1)));
     }
   }
   named_bar(1, nt);
@@ -435,14 +452,20 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
       u64 acc[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = 0ull;
-      item_dots<BITS, U>(w, y2s, P.C, seg * P.Cs + c, acc);
+      item_dots<BITS, U, EXACT>(w, y2s, P.C, seg * P.Cs + c, acc);
       const __half* scs = reinterpret_cast<const __half*>(st + P.sc_off);
+      float2 bS = make_float2(0.0f, 0.0f);
+      if (!EXACT) bS = *reinterpret_cast<const float2*>(ysum + 2 * (seg * P.Cs + c));
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int r = rp * U + u;
         if (r < rows) {
           float p0, p1;
           upk(acc[u], p0, p1);
+          if (!EXACT) {
+            p0 = fold_block(p0, bS.x);
+            p1 = fold_block(p1, bS.y);
+          }
           float* dst = tbuf + (size_t)(tb * R + r) * GS + 2 * c;
           if (PERROW) {
             dst[0] = p0;
@@ -486,7 +509,7 @@ static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int U, 
   const int Cs = KS / 64;
   int RP = tc_target / Cs;
   if (RP < 1) RP = 1;
-  if (RP > 32) RP = 32;
+  if (RP > 32 / U) RP = 32 / U;
   const int Tc = ((Cs * RP + 31) / 32) * 32;
   if (Tc > 512) return false;
   if (RP * U > 32) return false;
@@ -504,7 +527,8 @@ static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int U, 
   P->stage_bytes = (P->sc_off + P->R * P->seg_sc + 127) & ~127;
   P->ngroups = (int)(((int64_t)N + P->R - 1) / P->R);
   P->y_off = 128;
-  P->stage_off = (P->y_off + K * 4 + 127) & ~127;
+  P->ysum_off = P->y_off + K * 4;
+  P->stage_off = (P->ysum_off + (K / 32) * 4 + 127) & ~127;
   P->tbuf_off = tma_round16(P->stage_off + NS * P->stage_bytes);
   return true;
 }
@@ -593,7 +617,7 @@ static size_t tma_smem(const TmaPlan& P, int K) {
   return (size_t)P.tbuf_off + (size_t)tma_round16(fold > bsum ? fold : bsum);
 }
 
-template <int BITS, bool PERROW, bool FUSED, int U, int MAXT>
+template <int BITS, bool PERROW, bool FUSED, bool EXACT, int U, int MAXT>
 static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err,
                    int* occ_only = nullptr) {
   static thread_local int cached_dev = -1;
@@ -601,7 +625,7 @@ static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaErro
   static thread_local int occ_cache = 0;
   static thread_local size_t occ_smem = 0;
   static thread_local int occ_threads = 0;
-  auto kern = gemv_tma_kernel<BITS, PERROW, FUSED, U, MAXT>;
+  auto kern = gemv_tma_kernel<BITS, PERROW, FUSED, EXACT, U, MAXT>;
   const size_t smem = tma_smem(P, a.K);
   const DevInfo& d = dev_info();
   if (smem > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
@@ -651,29 +675,38 @@ static int run_tma(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaErro
   return QMV_OK;
 }
 
-// CTAs of up to 256 compute threads (320 in all) get up to ~200 registers a
-// thread; larger ones (long K) are limited to 2 rows per thread.
-template <int BITS, bool PERROW, bool FUSED>
+// CTAs of up to 256 compute threads (320 in all) take 4 or 2 rows per
+// thread (2 for int8); larger ones (long K) 2.  These are the plans
+// tma_bits generates.
+template <int BITS, bool PERROW, bool FUSED, bool EXACT>
 static int tma_u(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err,
                  int* occ_only) {
   const int U = P.R / P.RP;
   if (P.Tc > 256) {
-    if (U >= 2) return run_tma<BITS, PERROW, FUSED, 2, 576>(a, P, s, err, occ_only);
-    return run_tma<BITS, PERROW, FUSED, 1, 576>(a, P, s, err, occ_only);
+    if (U != 2) return QMV_ERR_UNSUPPORTED;
+    return run_tma<BITS, PERROW, FUSED, EXACT, 2, 576>(a, P, s, err, occ_only);
   }
-  if (U >= 4) return run_tma<BITS, PERROW, FUSED, 4, 320>(a, P, s, err, occ_only);
-  if (U == 2) return run_tma<BITS, PERROW, FUSED, 2, 320>(a, P, s, err, occ_only);
-  return run_tma<BITS, PERROW, FUSED, 1, 320>(a, P, s, err, occ_only);
+  if (U == 2) return run_tma<BITS, PERROW, FUSED, EXACT, 2, 320>(a, P, s, err, occ_only);
+  if constexpr (BITS != 8)
+    if (U == 4) return run_tma<BITS, PERROW, FUSED, EXACT, 4, 320>(a, P, s, err, occ_only);
+  return QMV_ERR_UNSUPPORTED;
+}
+
+template <int BITS, bool EXACT>
+static int tma_mode(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err,
+                    int* occ_only) {
+  if (a.perrow)
+    return a.fused ? tma_u<BITS, true, true, EXACT>(a, P, s, err, occ_only)
+                   : tma_u<BITS, true, false, EXACT>(a, P, s, err, occ_only);
+  return a.fused ? tma_u<BITS, false, true, EXACT>(a, P, s, err, occ_only)
+                 : tma_u<BITS, false, false, EXACT>(a, P, s, err, occ_only);
 }
 
 template <int BITS>
 static int tma_dispatch(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_t* err,
                         int* occ_only) {
-  if (a.perrow)
-    return a.fused ? tma_u<BITS, true, true>(a, P, s, err, occ_only)
-                   : tma_u<BITS, true, false>(a, P, s, err, occ_only);
-  return a.fused ? tma_u<BITS, false, true>(a, P, s, err, occ_only)
-                 : tma_u<BITS, false, false>(a, P, s, err, occ_only);
+  return a.folded ? tma_mode<BITS, false>(a, P, s, err, occ_only)
+                  : tma_mode<BITS, true>(a, P, s, err, occ_only);
 }
 
 // Choose the plan with the most resident compute warps per SM (occupancy
@@ -684,17 +717,17 @@ static int tma_dispatch(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cud
 // choice is cached per shape.
 template <int BITS>
 static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
-  struct Key { int N, K, perrow, fused, dev; };
+  struct Key { int N, K, perrow, fused, folded, dev; };
   struct Entry { Key k; TmaPlan p; bool ok; };
   static thread_local Entry cache[16];
   static thread_local int next = 0;
   int dev = 0;
   cudaGetDevice(&dev);
-  const Key key{a.N, a.K, a.perrow, a.fused, dev};
+  const Key key{a.N, a.K, a.perrow, a.fused, a.folded, dev};
   for (int i = 0; i < 16; ++i) {
     const Key& k = cache[i].k;
     if (cache[i].ok && k.N == key.N && k.K == key.K && k.perrow == key.perrow &&
-        k.fused == key.fused && k.dev == key.dev)
+        k.fused == key.fused && k.folded == key.folded && k.dev == key.dev)
       return tma_dispatch<BITS>(a, cache[i].p, s, err, nullptr);
   }
   static const int tc_force = [] {
@@ -727,6 +760,20 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   cache[next] = Entry{key, best, true};
   next = (next + 1) % 16;
   return tma_dispatch<BITS>(a, best, s, err, nullptr);
+}
+
+// Whether some plan of the pipeline fits this K (shared memory), i.e. whether
+// launch_gemv_tma can run the shape at all.
+bool tma_fits(int K, int bits, bool perrow) {
+  for (int tc : {256, 512})
+    for (int U : {4, 2}) {
+      if (bits == 8 && U > 2) continue;
+      if (tc > 256 && U > 2) continue;
+      TmaPlan P;
+      if (tma_plan(1, K, bits, perrow, tc, U, &P) && tma_smem(P, K) <= (size_t)dev_info().max_smem_optin)
+        return true;
+    }
+  return false;
 }
 
 int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {

@@ -8,7 +8,7 @@ import synth
 
 SEED = synth.DEFAULT_SEED
 EPS = 1e-6
-TOL = 1e-3   # max |y - ref| <= TOL * (1 + |ref|) for the tensor-core (fast, M > 32) path
+TOL = 1e-3   # fast mode: max |y - ref| <= TOL * (1 + |ref|)
 
 
 def qmv():
@@ -88,3 +88,10 @@ def within_tol(y, ref, tol=TOL):
     y = np.asarray(y, np.float64)
     ref = np.asarray(ref, np.float64)
     return np.all(np.abs(y - ref) <= tol * (1.0 + np.abs(ref)))
+
+
+def max_rel_err(y, ref):
+    """max |y - ref| / (1 + |ref|), for failure messages"""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(y - ref) / (1.0 + np.abs(ref))))

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import EPS, Mat, acts, bits_equal, first_diff, to_dev, qmv
+from gpu_util import EPS, Mat, acts, bits_equal, first_diff, to_dev, within_tol, qmv
 
 pytestmark = pytest.mark.gpu
 
@@ -44,11 +44,13 @@ def test_fused_without_h_out():
     q = qmv()
     m = Mat("fu_noh", 512, 2048, 2, 32)
     x, r, g = acts("fu_noh", 1, 2048)
-    y = q.qmv_fused_rmsnorm_gemv(m.pack, to_dev(x), to_dev(r), to_dev(g), EPS)
+    y = q.qmv_fused_rmsnorm_gemv(m.pack, to_dev(x), to_dev(r), to_dev(g), EPS, mode=q.QMV_EXACT)
+    yf = q.qmv_fused_rmsnorm_gemv(m.pack, to_dev(x), to_dev(r), to_dev(g), EPS, mode=q.QMV_FAST)
     torch.cuda.synchronize()
     codes, scales = m.host()
     _, _, ref = oracle.fused_rmsnorm_gemv(codes, scales, 32, x, r, g, EPS)
     assert bits_equal(y.cpu().numpy(), ref)
+    assert within_tol(yf.cpu().numpy(), ref)
 
 
 def test_fused_zero_input():
@@ -56,6 +58,7 @@ def test_fused_zero_input():
     m = Mat("fu_zero", 128, 1024, 2, 32)
     z = np.zeros((1, 1024), np.float16)
     _, _, g = acts("fu_zero", 1, 1024)
-    y = q.qmv_fused_rmsnorm_gemv(m.pack, to_dev(z), to_dev(z), to_dev(g), EPS)
-    torch.cuda.synchronize()
-    assert torch.all(y == 0)
+    for mode in (q.QMV_FAST, q.QMV_EXACT):
+        y = q.qmv_fused_rmsnorm_gemv(m.pack, to_dev(z), to_dev(z), to_dev(g), EPS, mode=mode)
+        torch.cuda.synchronize()
+        assert torch.all(y == 0)

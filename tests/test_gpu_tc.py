@@ -1,12 +1,13 @@
 """GPU parity of the tcgen05 tensor-core tiles (M > 32 token columns, fast
 mode, int2 weights) against the oracle, within max |y - ref| <= 1e-3*(1+|ref|);
-and the exact-mode / int4 paths at M > 32, which stay bit-exact."""
+the exact mode at M > 32, which stays bit-exact; and the fast int4/int8 tiles
+at M > 32."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import Mat, acts, bits_equal, first_diff, to_dev, within_tol, qmv
+from gpu_util import Mat, acts, bits_equal, first_diff, max_rel_err, to_dev, within_tol, qmv
 
 pytestmark = pytest.mark.gpu
 
@@ -50,13 +51,30 @@ def test_tensor_tiles_repeatable_without_split():
 
 
 @pytest.mark.parametrize("bits,M", [(4, 64), (8, 40), (2, 48)])
-def test_exact_or_wide_codes_above_32_columns_bit_exact(bits, M):
+def test_exact_above_32_columns_bit_exact(bits, M):
     q = qmv()
     m = Mat(f"ex{bits}", 200, 1024, bits, 32)
     x, _, _ = acts(f"ex{bits}m{M}", M, 1024)
-    mode = q.QMV_EXACT if bits == 2 else q.QMV_FAST
-    y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=mode)
+    y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_EXACT)
     torch.cuda.synchronize()
     codes, scales = m.host()
     ref = oracle.gemv(codes, scales, 32, x)
     assert bits_equal(y.cpu().numpy(), ref), first_diff(y.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("bits,M", [(4, 64), (8, 40)])
+def test_fast_wide_codes_above_32_columns(bits, M):
+    """int4/int8 above 32 columns run the CUDA-core tiles in 32-column chunks:
+    within tolerance, and every column equal to the fast M = 1 result."""
+    q = qmv()
+    m = Mat(f"ex{bits}", 200, 1024, bits, 32)
+    x, _, _ = acts(f"ex{bits}m{M}", M, 1024)
+    y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_FAST)
+    y1 = [q.qmv_gemv(m.pack, to_dev(x[i:i + 1]), mode=q.QMV_FAST) for i in (0, 31, 32, M - 1)]
+    torch.cuda.synchronize()
+    codes, scales = m.host()
+    ref = oracle.gemv(codes, scales, 32, x)
+    got = y.cpu().numpy()
+    assert within_tol(got, ref), max_rel_err(got, ref)
+    for yi, i in zip(y1, (0, 31, 32, M - 1)):
+        assert bits_equal(got[i], yi.cpu().numpy()[0])
