@@ -186,28 +186,19 @@ __device__ __forceinline__ u64 decode2(uint32_t a, uint32_t b, uint32_t m, u64 o
 // fp32 bits is the subnormal u * 2^o * 2^-149 exactly.  With the activation
 // pre-scaled to y' = y * 2^(FOLD_E - o) one paired FMA adds y*u*2^-40 (an
 // exact product, |y'| < 2^125 for every finite fp16 y, and every nonzero
-// product is a normal number) to the block's running sum P: one mask per code
-// and one paired FMA per two codes, no subtraction.  The block result is
-// fma(P, 2^40, -2^(b-1)*S) (P*2^40 is exact), then scaled as in the exact
-// form.  The sums differ from the exact form's serial order only by rounding,
-// so this is the fast mode's arithmetic.  S is the serial fp32 sum of the
-// block's activations in k order, the order of the dot itself: P is then
-// exactly 2^-40 times the serial sum of y*u, a block of zero weights (u =
-// 2^(b-1) throughout) gives exactly 0, and every kernel that uses the form
-// agrees bit for bit.
+// product is a normal number) to a running sum: one mask per code and one
+// paired FMA per two codes, no subtraction.  The two lanes of the paired FMA
+// take two adjacent words of a block (words 2p and 2p+1, which sit in one
+// 64-bit register pair, so one 64-bit AND masks both fields in place): lane 0
+// sums the block's even words and lane 1 its odd words, each serially in code
+// order, and P = P_even + P_odd.  The block result is fma(P, 2^40,
+// -2^(b-1)*S) (P*2^40 is exact), then scaled as in the exact form.  The sums
+// differ from the exact form's serial order only by rounding, so this is the
+// fast mode's arithmetic.  S is formed in the same order as P (S_even and
+// S_odd serially, then added): P*2^40 is then exactly 2^(b-1)*S when every
+// code of the block is zero (u = 2^(b-1)), which gives exactly 0, and every
+// kernel that uses the form agrees bit for bit.
 constexpr int FOLD_E = 109;
-
-// (a & m, b & m) as two fp32 lanes (subnormal field values)
-__device__ __forceinline__ u64 fields2(uint32_t a, uint32_t b, uint32_t m) {
-  u64 v;
-  asm("{\n\t.reg .b32 t0, t1;\n\t"
-      "and.b32 t0, %1, %3;\n\t"
-      "and.b32 t1, %2, %3;\n\t"
-      "mov.b64 %0, {t0, t1};\n\t}"
-      : "=l"(v)
-      : "r"(a), "r"(b), "r"(m));
-  return v;
-}
 
 // block result from the running sum P (units of 2^-40) and bS = 2^(b-1)*S
 __device__ __forceinline__ float fold_block(float P, float bS) {

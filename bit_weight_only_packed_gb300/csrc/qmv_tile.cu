@@ -138,31 +138,120 @@ __global__ void __launch_bounds__(256) gemm_tile_kernel(GemvArgs a) {
     }
     __syncthreads();
     if (FOLD) {
-      // block sums of the activations, serial in k, times 2^(b-1)
+      // block sums of the activations in the order of the dots (even and
+      // odd words serially, then added), times 2^(b-1)
       for (int e = t; e < MT * 2 * items; e += 256) {
         const int m = e / (2 * items), bl = e % (2 * items);
         const __half* yb = y16 + m * TL_SLAB + 32 * bl;
-        float S = 0.0f;
+        float S0 = 0.0f, S1 = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = lds16(yb + 8 * q);
-#pragma unroll
-          for (int e8 = 0; e8 < 8; ++e8) S = __fadd_rn(S, __half2float(h_of(v, e8)));
+        for (int tt = 0; tt < 16; ++tt) {
+          const int k0 = CPW * 2 * (tt / CPW) + tt % CPW;
+          S0 = __fadd_rn(S0, __half2float(yb[k0]));
+          S1 = __fadd_rn(S1, __half2float(yb[k0 + CPW]));
         }
-        ssl[m * TL_SB + bl] = __fmul_rn(S, (float)(1 << (BITS - 1)));
+        ssl[m * TL_SB + bl] = __fmul_rn(__fadd_rn(S0, S1), (float)(1 << (BITS - 1)));
       }
     }
     for (int e = t; e < items * 32 * MT; e += 256) {
       const int k = e & 31, m = (e >> 5) % MT, it = (e >> 5) / MT;
-      const int o = BITS * ((k % CPW) % HALF);
-      const float sc = pow2f(FOLD ? FOLD_E - o : -o);
-      const float v0 = __fmul_rn(__half2float(y16[m * TL_SLAB + 64 * it + k]), sc);
-      const float v1 = __fmul_rn(__half2float(y16[m * TL_SLAB + 64 * it + 32 + k]), sc);
+      const __half* yi = y16 + m * TL_SLAB + 64 * it;
+      float v0, v1;
+      if (!FOLD) {
+        // step k: (code k of block 0, code k of block 1)
+        const float sc = pow2f(-BITS * ((k % CPW) % HALF));
+        v0 = __fmul_rn(__half2float(yi[k]), sc);
+        v1 = __fmul_rn(__half2float(yi[32 + k]), sc);
+      } else {
+        // step k = 16*blk + CPW*p + j: (code j of word 2p, of word 2p + 1)
+        const int blk = k >> 4, p = (k & 15) / CPW, j = (k & 15) % CPW;
+        const float sc = pow2f(FOLD_E - BITS * (j % HALF));
+        const int k0 = 32 * blk + CPW * 2 * p + j;
+        v0 = __fmul_rn(__half2float(yi[k0]), sc);
+        v1 = __fmul_rn(__half2float(yi[k0 + CPW]), sc);
+      }
       yp[(it * 32 + k) * S::MS + m] = pk(v0, v1);
     }
     __syncthreads();
 
-    if (warp < items) {
+    if (FOLD && warp < items) {
+      // folded form: item `warp` of this slab, one block at a time, for rows
+      // lane + 32u of the tile; the words as 64-bit pairs (2q, 2q + 1)
+      constexpr int NP = 16 / CPW;   // word pairs per block
+      const int item = s0 / 64 + warp;
+      u64 wp[U][IW / 2];
+      uint32_t scw[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t row = row0 + lane + 32 * u;
+        scw[u] = 0u;
+        if (row < a.N) {
+          const ulonglong2* src =
+              reinterpret_cast<const ulonglong2*>(a.codes + row * a.row_u4 + (int64_t)item * (IW / 4));
+#pragma unroll
+          for (int q = 0; q < IW / 4; ++q) {
+            const ulonglong2 v = __ldg(src + q);
+            wp[u][2 * q] = v.x;
+            wp[u][2 * q + 1] = v.y;
+          }
+          if (!a.perrow) scw[u] = __ldg(reinterpret_cast<const unsigned int*>(a.scales + row * a.G + (int64_t)item * 2));
+        } else {
+#pragma unroll
+          for (int q = 0; q < IW / 2; ++q) wp[u][q] = 0ull;
+        }
+      }
+      const u64* yit = yp + (size_t)warp * 32 * S::MS;
+#pragma unroll 1
+      for (int c0 = 0; c0 < MT; c0 += MTC) {
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          u64 acc2[U][MTC];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int mm = 0; mm < MTC; ++mm) acc2[u][mm] = 0ull;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            u64 lo[U], hi[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              lo[u] = wp[u][blk * NP + p];
+              hi[u] = lo[u] >> 16;
+            }
+#pragma unroll
+            for (int j = 0; j < CPW; ++j) {
+              const uint32_t m32 = MASK << (BITS * (j % HALF));
+              const u64 mm64 = ((u64)m32 << 32) | m32;
+              u64 v[U];
+#pragma unroll
+              for (int u = 0; u < U; ++u) v[u] = ((j < HALF) ? lo[u] : hi[u]) & mm64;
+              const u64* yk = yit + (16 * blk + CPW * p + j) * S::MS + c0;
+#pragma unroll
+              for (int mm = 0; mm < MTC; mm += 2) {
+                const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                  acc2[u][mm] = ffma2(y2.x, v[u], acc2[u][mm]);
+                  acc2[u][mm + 1] = ffma2(y2.y, v[u], acc2[u][mm + 1]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const float sc = __half2float(__ushort_as_half((uint16_t)(blk ? (scw[u] >> 16) : (scw[u] & 0xFFFFu))));
+#pragma unroll
+            for (int mm = 0; mm < MTC; ++mm) {
+              float pe, po;
+              upk(acc2[u][mm], pe, po);
+              float pb = fold_block(__fadd_rn(pe, po), ssl[(c0 + mm) * TL_SB + 2 * warp + blk]);
+              if (!a.perrow) pb = __fmul_rn(pb, sc);
+              tb[((2 * warp + blk) * MT + c0 + mm) * S::ROWS + lane + 32 * u] = pb;
+            }
+          }
+        }
+      }
+    } else if (!FOLD && warp < items) {
       // item `warp` of this slab for rows lane + 32u of the tile
       const int item = s0 / 64 + warp;
       uint32_t w[U][IW];
@@ -211,7 +300,7 @@ __global__ void __launch_bounds__(256) gemm_tile_kernel(GemvArgs a) {
             for (int u = 0; u < U; ++u) {
               const uint32_t wa = (j < HALF) ? w[u][wi] : h0[u];
               const uint32_t wb = (j < HALF) ? w[u][WPB + wi] : h1[u];
-              v[u] = FOLD ? fields2(wa, wb, MASK << o) : decode2(wa, wb, MASK << o, pk(offf, offf));
+              v[u] = decode2(wa, wb, MASK << o, pk(offf, offf));
             }
             const u64* yk = yit + (wi * CPW + j) * S::MS + c0;
 #pragma unroll
@@ -231,10 +320,6 @@ __global__ void __launch_bounds__(256) gemm_tile_kernel(GemvArgs a) {
           for (int mm = 0; mm < MTC; ++mm) {
             float p0, p1;
             upk(acc2[u][mm], p0, p1);
-            if (FOLD) {
-              p0 = fold_block(p0, ssl[(c0 + mm) * TL_SB + 2 * warp]);
-              p1 = fold_block(p1, ssl[(c0 + mm) * TL_SB + 2 * warp + 1]);
-            }
             const int r = lane + 32 * u;
             tb[((2 * warp) * MT + c0 + mm) * S::ROWS + r] = a.perrow ? p0 : __fmul_rn(p0, s_lo[u]);
             tb[((2 * warp + 1) * MT + c0 + mm) * S::ROWS + r] = a.perrow ? p1 : __fmul_rn(p1, s_hi[u]);

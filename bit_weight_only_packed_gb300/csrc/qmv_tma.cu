@@ -87,6 +87,13 @@ __device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile in
   return false;
 }
 
+// The common case inline (one try_wait, which itself suspends the warp for a
+// while), the bounded loop out of line.
+__device__ __forceinline__ bool mbar_wait_fast(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                               int code) {
+  return mbar_try(b, parity) || mbar_wait(b, parity, abort_flag, code);
+}
+
 // Bounded wait that ignores the abort flag (used to let copies land).
 __device__ __noinline__ void mbar_drain(uint64_t* b, uint32_t parity) {
   for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
@@ -113,7 +120,9 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 // Store 8 consecutive fp16 activations starting at element e0 (a multiple of
 // 8) as fp32 into the pair layout: element 64*c + 32*h + k goes to
 // y2f[2*(k*C + c) + h].
-// Exact form: y * 2^-o(k); folded form: y * 2^(FOLD_E - o(k)).
+// Exact form: y * 2^-o(k), pairs (block 0, block 1) at step k.  Folded form:
+// y * 2^(FOLD_E - o(k)), pairs (even word, odd word) of one block: step
+// s = 16*blk + CPW*p + j holds code j of words 2p and 2p+1 of block blk.
 template <int BITS, bool EXACT>
 __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32_t (&h8)[4]) {
   constexpr int CPW = 32 / BITS, HALF = CPW / 2;
@@ -121,10 +130,15 @@ __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int k = k0 + e;
-    const int o = BITS * ((k % CPW) % HALF);
+    const int j = k % CPW, o = BITS * (j % HALF);
     const __half2 v = u32_as_h2(h8[e >> 1]);
     const float f = (e & 1) ? __high2float(v) : __low2float(v);
-    y2f[2 * (k * C + c) + h] = __fmul_rn(f, pow2f(EXACT ? -o : FOLD_E - o));
+    if (EXACT) {
+      y2f[2 * (k * C + c) + h] = __fmul_rn(f, pow2f(-o));
+    } else {
+      const int wi = k / CPW, step = 16 * h + CPW * (wi >> 1) + j;
+      y2f[2 * (step * C + c) + (wi & 1)] = __fmul_rn(f, pow2f(FOLD_E - o));
+    }
   }
 }
 
@@ -136,9 +150,8 @@ __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32
 // y_k * v_k exactly (powers of two; no underflow for fp16 inputs).  acc[u] =
 // (p0, p1) are the two blocks' serial sums.  Fields in the high 16-bit half
 // of a word are first shifted down by 16, so every field is masked below
-// bit 16.  In the folded form (fast mode) the masked field itself is the
-// operand and the sums are of y*u*2^-40; the offset is removed per block.
-template <int BITS, int U, bool EXACT>
+// bit 16.  (Exact form; the folded form is block_dots_fold.)
+template <int BITS, int U>
 __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32],
                                           const u64* __restrict__ y2s, int C, int c,
                                           u64 (&acc)[U]) {
@@ -164,8 +177,47 @@ __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32]
       for (int u = 0; u < U; ++u) {
         const uint32_t a = (j < HALF) ? w[u][wi] : h0[u];
         const uint32_t b = (j < HALF) ? w[u][WPB + wi] : h1[u];
-        const u64 v = EXACT ? decode2(a, b, MASK << o, off) : fields2(a, b, MASK << o);
+        const u64 v = decode2(a, b, MASK << o, off);
         acc[u] = ffma2(y, v, acc[u]);
+      }
+    }
+  }
+}
+
+// Folded form, both 32-code blocks of a 64-code item for U rows: wp[u][q]
+// are the item's words as 64-bit pairs (words 2q, 2q+1), so a pair's two
+// fields at one offset are masked by one 64-bit AND straight into the
+// register pair the paired FMA reads.  Lane 0 of acc[u][blk] sums block
+// blk's even words, lane 1 its odd words, each serially in code order; the
+// two blocks' chains are interleaved for independent work.  The high 16-bit
+// fields come from the pair shifted right by 16 as a whole: what crosses from
+// the odd word into the even word's upper half is masked off.
+template <int BITS, int U>
+__device__ __forceinline__ void item_dots_fold(const u64 (&wp)[U][BITS], const u64* __restrict__ y2s,
+                                               int C, int c, u64 (&acc)[U][2]) {
+  constexpr int CPW = 32 / BITS, HALF = CPW / 2;
+  constexpr int NP = 16 / CPW;                 // word pairs per block
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    u64 lo[U][2], hi[U][2];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        lo[u][blk] = wp[u][blk * NP + p];
+        hi[u][blk] = lo[u][blk] >> 16;
+      }
+#pragma unroll
+    for (int j = 0; j < CPW; ++j) {
+      const uint32_t m = MASK << (BITS * (j % HALF));
+      const u64 mm = ((u64)m << 32) | m;
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const u64 y = y2s[(16 * blk + CPW * p + j) * C + c];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          acc[u][blk] = ffma2(y, ((j < HALF) ? lo[u][blk] : hi[u][blk]) & mm, acc[u][blk]);
       }
     }
   }
@@ -258,7 +310,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     int64_t g = blockIdx.x;
     for (int i = 0; i < my_stages; ++i) {
       const int s = i & (NS - 1);
-      if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY)) break;
+      if (i >= NS && !mbar_wait_fast(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY)) break;
       if (*abort_f) break;
       const int64_t r0 = g * R;
       const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
@@ -353,17 +405,21 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     }
   }
   if (!EXACT) {
-    // block sums of the activations, serial in k, read back from the scaled
-    // pairs (y' * 2^(o - FOLD_E) = y exactly), times the offset 2^(b-1)
+    // block sums of the activations in the order of the dots (even and odd
+    // words serially, then added), read back from the scaled pairs
+    // (y' * 2^(o - FOLD_E) = y exactly), times the offset 2^(b-1)
     named_bar(1, nt);
     constexpr int CPW = 32 / BITS, HALF = CPW / 2;
     for (int b = tt; b < NB; b += nt) {
-      const float* src = y2f + 2 * (b >> 1) + (b & 1);
-      float S = 0.0f;
+      const float* src = y2f + 2 * (16 * (b & 1) * P.C + (b >> 1));
+      float S0 = 0.0f, S1 = 0.0f;
 #pragma unroll 8
-      for (int k = 0; k < 32; ++k)
-        S = __fmaf_rn(src[2 * k * P.C], pow2f(BITS * ((k % CPW) % HALF) - FOLD_E), S);
-      ysum[b] = __fmul_rn(S, (float)(1 << (BITS - 1)));
+      for (int t = 0; t < 16; ++t) {
+        const float sc = pow2f(BITS * ((t % CPW) % HALF) - FOLD_E);
+        S0 = __fmaf_rn(src[2 * t * P.C], sc, S0);
+        S1 = __fmaf_rn(src[2 * t * P.C + 1], sc, S1);
+      }
+      ysum[b] = __fmul_rn(__fadd_rn(S0, S1), (float)(1 << (BITS - 1)));
     }
   }
   named_bar(1, nt);
@@ -375,7 +431,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     int64_t g = blockIdx.x;
     for (int i = 0; i < my_stages; ++i) {
       const int tb = i & 1;
-      if (!mbar_wait(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL)) break;
+      if (!mbar_wait_fast(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL)) break;
       const int64_t r0 = g * R;
       const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
       if (lane < rows) {
@@ -424,11 +480,48 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   for (int i = 0; i < my_stages; ++i) {
     const int s = i & (NS - 1);
     const int tb = i & 1;
-    if (!mbar_wait(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL)) break;
-    if (i >= 2 && !mbar_wait(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY)) break;
+    if (!mbar_wait_fast(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL)) break;
+    if (i >= 2 && !mbar_wait_fast(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY)) break;
     const int64_t r0 = g * R;
     const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
-    if (active) {
+    if (active && !EXACT) {
+      // folded form: rows past N in the box are zero-filled, so every row of
+      // the group is computed (the fold warp stores only real rows)
+      const unsigned char* st = stages + (size_t)s * P.stage_bytes;
+      u64 wp[U][IW / 2];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = rp * U + u;
+        const ulonglong2* src =
+            reinterpret_cast<const ulonglong2*>(st + (size_t)r * P.seg_bytes + (size_t)c * (IW * 4));
+#pragma unroll
+        for (int q = 0; q < IW / 4; ++q) {
+          const ulonglong2 v = src[q];
+          wp[u][2 * q] = v.x;
+          wp[u][2 * q + 1] = v.y;
+        }
+      }
+      const __half* scs = reinterpret_cast<const __half*>(st + P.sc_off);
+      const float2 bS = *reinterpret_cast<const float2*>(ysum + 2 * (seg * P.Cs + c));
+      u64 acc[U][2];
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u][0] = acc[u][1] = 0ull;
+      item_dots_fold<BITS, U>(wp, y2s, P.C, seg * P.Cs + c, acc);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = rp * U + u;
+        float2 sc = make_float2(1.0f, 1.0f);
+        if (!PERROW) sc = __half22float2(*reinterpret_cast<const __half2*>(scs + (size_t)r * NBS + 2 * c));
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          float pe, po;
+          upk(acc[u][blk], pe, po);
+          float pb = fold_block(__fadd_rn(pe, po), blk ? bS.y : bS.x);
+          if (!PERROW) pb = __fmul_rn(pb, blk ? sc.y : sc.x);
+          tbuf[(size_t)(tb * R + r) * GS + 2 * c + blk] = pb;
+        }
+      }
+    } else if (active) {
       const unsigned char* st = stages + (size_t)s * P.stage_bytes;
       uint32_t w[U][IW];
 #pragma unroll
@@ -452,20 +545,14 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
       u64 acc[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = 0ull;
-      item_dots<BITS, U, EXACT>(w, y2s, P.C, seg * P.Cs + c, acc);
+      item_dots<BITS, U>(w, y2s, P.C, seg * P.Cs + c, acc);
       const __half* scs = reinterpret_cast<const __half*>(st + P.sc_off);
-      float2 bS = make_float2(0.0f, 0.0f);
-      if (!EXACT) bS = *reinterpret_cast<const float2*>(ysum + 2 * (seg * P.Cs + c));
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int r = rp * U + u;
         if (r < rows) {
           float p0, p1;
           upk(acc[u], p0, p1);
-          if (!EXACT) {
-            p0 = fold_block(p0, bS.x);
-            p1 = fold_block(p1, bS.y);
-          }
           float* dst = tbuf + (size_t)(tb * R + r) * GS + 2 * c;
           if (PERROW) {
             dst[0] = p0;
