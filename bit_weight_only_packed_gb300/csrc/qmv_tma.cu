@@ -41,7 +41,7 @@ __device__ int g_qmv_error = 0;
 namespace {
 
 constexpr int NS = 4;                      // ring stages (a power of two)
-constexpr uint32_t SPIN_LIMIT = 1u << 22;  // bounded waits (~0.5 s each)
+constexpr uint32_t SPIN_LIMIT = 1u << 22;  // tries per bounded wait (a backstop to the time limit)
 constexpr int ERR_TIMEOUT_FULL = 1, ERR_TIMEOUT_EMPTY = 2, ERR_TIMEOUT_TFULL = 3,
               ERR_TIMEOUT_TEMPTY = 4, ERR_SMEM_ALIGN = 5;
 
@@ -72,15 +72,39 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the warp sleeps in hardware until the
+// phase completes (it wakes at once then) or the hint elapses
+__device__ __forceinline__ bool mbar_try_hint(uint64_t* b, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+constexpr uint32_t WAIT_HINT_NS = 20000;            // one suspended try
+constexpr uint64_t WAIT_LIMIT_NS = 500000000ull;    // give up after 0.5 s
+
 // Bounded wait.  Returns false (after setting the CTA's abort flag and the
-// device error word) if the phase does not complete in SPIN_LIMIT tries, or
-// at once if another warp of the CTA has aborted.
+// device error word) if the phase does not complete within WAIT_LIMIT_NS (or
+// SPIN_LIMIT tries), or soon after another warp of the CTA has aborted.
 __device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
                                        int code) {
+  const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
-    if (mbar_try(b, parity)) return true;
+    if (mbar_try_hint(b, parity, WAIT_HINT_NS)) return true;
     if (*abort_flag) return false;
-    if (i > 16) __nanosleep(100);
+    if (global_ns() - t0 > WAIT_LIMIT_NS) break;
   }
   *abort_flag = 1;
   atomicCAS(&g_qmv_error, 0, code);
@@ -96,9 +120,10 @@ __device__ __forceinline__ bool mbar_wait_fast(uint64_t* b, uint32_t parity, vol
 
 // Bounded wait that ignores the abort flag (used to let copies land).
 __device__ __noinline__ void mbar_drain(uint64_t* b, uint32_t parity) {
+  const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
-    if (mbar_try(b, parity)) return;
-    __nanosleep(100);
+    if (mbar_try_hint(b, parity, WAIT_HINT_NS)) return;
+    if (global_ns() - t0 > WAIT_LIMIT_NS) break;
   }
   atomicCAS(&g_qmv_error, 0, ERR_TIMEOUT_FULL);
 }
@@ -117,14 +142,20 @@ __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// The activation table: per 64-code item c, 32 steps of fp32 pairs at
+// y2f[2*(YS*c + step) + lane].  The item stride YS = 34 pairs (272 bytes)
+// keeps 16-byte loads of two consecutive steps aligned and spreads the
+// threads of a warp (consecutive items) over all banks; within an item the
+// steps are immediate offsets.
+constexpr int YS = 34;
+
 // Store 8 consecutive fp16 activations starting at element e0 (a multiple of
-// 8) as fp32 into the pair layout: element 64*c + 32*h + k goes to
-// y2f[2*(k*C + c) + h].
-// Exact form: y * 2^-o(k), pairs (block 0, block 1) at step k.  Folded form:
-// y * 2^(FOLD_E - o(k)), pairs (even word, odd word) of one block: step
-// s = 16*blk + CPW*p + j holds code j of words 2p and 2p+1 of block blk.
+// 8; element 64*c + 32*h + k) into the table.  Exact form: y * 2^-o(k), step
+// k holds (block 0, block 1) code k.  Folded form: y * 2^(FOLD_E - o(k)),
+// step 16*blk + CPW*p + j holds (code j of word 2p, of word 2p+1) of block
+// blk.
 template <int BITS, bool EXACT>
-__device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32_t (&h8)[4]) {
+__device__ __forceinline__ void store_y8(float* y2f, int e0, const uint32_t (&h8)[4]) {
   constexpr int CPW = 32 / BITS, HALF = CPW / 2;
   const int c = e0 >> 6, h = (e0 >> 5) & 1, k0 = e0 & 31;
 #pragma unroll
@@ -134,18 +165,17 @@ __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32
     const __half2 v = u32_as_h2(h8[e >> 1]);
     const float f = (e & 1) ? __high2float(v) : __low2float(v);
     if (EXACT) {
-      y2f[2 * (k * C + c) + h] = __fmul_rn(f, pow2f(-o));
+      y2f[2 * (YS * c + k) + h] = __fmul_rn(f, pow2f(-o));
     } else {
       const int wi = k / CPW, step = 16 * h + CPW * (wi >> 1) + j;
-      y2f[2 * (step * C + c) + (wi & 1)] = __fmul_rn(f, pow2f(FOLD_E - o));
+      y2f[2 * (YS * c + step) + (wi & 1)] = __fmul_rn(f, pow2f(FOLD_E - o));
     }
   }
 }
 
 // Both blocks of one 64-code item, for U rows at once.  w[u][0 .. 2*WPB-1]:
-// words of block 0 then block 1.  y2s: activation pairs (y'_k, y'_{32+k}) of
-// all items, laid out [k][item] so that consecutive threads read consecutive
-// 8-byte pairs; one pair serves all U rows.  y'_k = y_k * 2^-o(k) where o(k)
+// words of block 0 then block 1.  yc: the item's activation pairs
+// (y'_k, y'_{32+k}), two steps per 16-byte load; one pair serves all U rows.  y'_k = y_k * 2^-o(k) where o(k)
 // is the bit offset the code k is decoded at, so y'_k * (v_k * 2^o(k)) =
 // y_k * v_k exactly (powers of two; no underflow for fp16 inputs).  acc[u] =
 // (p0, p1) are the two blocks' serial sums.  Fields in the high 16-bit half
@@ -153,8 +183,7 @@ __device__ __forceinline__ void store_y8(float* y2f, int C, int e0, const uint32
 // bit 16.  (Exact form; the folded form is block_dots_fold.)
 template <int BITS, int U>
 __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32],
-                                          const u64* __restrict__ y2s, int C, int c,
-                                          u64 (&acc)[U]) {
+                                          const u64* __restrict__ yc, u64 (&acc)[U]) {
   constexpr int CPW = 32 / BITS;   // codes per word
   constexpr int HALF = CPW / 2;    // codes per 16-bit half
   constexpr int WPB = 32 / CPW;    // words per block
@@ -172,7 +201,8 @@ __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32]
       const int o = BITS * (j % HALF);
       const float offf = pow2f(23) + (float)(1 << (BITS - 1 + o));
       const u64 off = pk(offf, offf);
-      const u64 y = y2s[(wi * CPW + j) * C + c];
+      const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yc + wi * CPW + (j & ~1));
+      const u64 y = (j & 1) ? y2.y : y2.x;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t a = (j < HALF) ? w[u][wi] : h0[u];
@@ -193,8 +223,8 @@ __device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32]
 // fields come from the pair shifted right by 16 as a whole: what crosses from
 // the odd word into the even word's upper half is masked off.
 template <int BITS, int U>
-__device__ __forceinline__ void item_dots_fold(const u64 (&wp)[U][BITS], const u64* __restrict__ y2s,
-                                               int C, int c, u64 (&acc)[U][2]) {
+__device__ __forceinline__ void item_dots_fold(const u64 (&wp)[U][BITS], const u64* __restrict__ yc,
+                                               u64 (&acc)[U][2]) {
   constexpr int CPW = 32 / BITS, HALF = CPW / 2;
   constexpr int NP = 16 / CPW;                 // word pairs per block
   constexpr uint32_t MASK = (1u << BITS) - 1u;
@@ -214,7 +244,9 @@ __device__ __forceinline__ void item_dots_fold(const u64 (&wp)[U][BITS], const u
       const u64 mm = ((u64)m << 32) | m;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
-        const u64 y = y2s[(16 * blk + CPW * p + j) * C + c];
+        const ulonglong2 y2 =
+            *reinterpret_cast<const ulonglong2*>(yc + 16 * blk + CPW * p + (j & ~1));
+        const u64 y = (j & 1) ? y2.y : y2.x;
 #pragma unroll
         for (int u = 0; u < U; ++u)
           acc[u][blk] = ffma2(y, ((j < HALF) ? lo[u][blk] : hi[u][blk]) & mm, acc[u][blk]);
@@ -395,13 +427,13 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
         const __half yh = __float2half_rn(__fmul_rn(__fmul_rn(hh, inv), __high2float(gg)));
         ys[e] = (uint32_t)__half_as_ushort(yl) | ((uint32_t)__half_as_ushort(yh) << 16);
       }
-      store_y8<BITS, EXACT>(y2f, P.C, 8 * v8, ys);
+      store_y8<BITS, EXACT>(y2f, 8 * v8, ys);
     }
   } else {
     for (int v8 = tt; v8 < K / 8; v8 += nt) {
       const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 8 * v8));
       const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-      store_y8<BITS, EXACT>(y2f, P.C, 8 * v8, xs);
+      store_y8<BITS, EXACT>(y2f, 8 * v8, xs);
     }
   }
   if (!EXACT) {
@@ -411,13 +443,13 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     named_bar(1, nt);
     constexpr int CPW = 32 / BITS, HALF = CPW / 2;
     for (int b = tt; b < NB; b += nt) {
-      const float* src = y2f + 2 * (16 * (b & 1) * P.C + (b >> 1));
+      const float* src = y2f + 2 * (YS * (b >> 1) + 16 * (b & 1));
       float S0 = 0.0f, S1 = 0.0f;
-#pragma unroll 8
+#pragma unroll
       for (int t = 0; t < 16; ++t) {
         const float sc = pow2f(BITS * ((t % CPW) % HALF) - FOLD_E);
-        S0 = __fmaf_rn(src[2 * t * P.C], sc, S0);
-        S1 = __fmaf_rn(src[2 * t * P.C + 1], sc, S1);
+        S0 = __fmaf_rn(src[2 * t], sc, S0);
+        S1 = __fmaf_rn(src[2 * t + 1], sc, S1);
       }
       ysum[b] = __fmul_rn(__fadd_rn(S0, S1), (float)(1 << (BITS - 1)));
     }
@@ -506,7 +538,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
       u64 acc[U][2];
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u][0] = acc[u][1] = 0ull;
-      item_dots_fold<BITS, U>(wp, y2s, P.C, seg * P.Cs + c, acc);
+      item_dots_fold<BITS, U>(wp, y2s + YS * (seg * P.Cs + c), acc);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int r = rp * U + u;
@@ -545,7 +577,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
       u64 acc[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) acc[u] = 0ull;
-      item_dots<BITS, U>(w, y2s, P.C, seg * P.Cs + c, acc);
+      item_dots<BITS, U>(w, y2s + YS * (seg * P.Cs + c), acc);
       const __half* scs = reinterpret_cast<const __half*>(st + P.sc_off);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -614,7 +646,7 @@ static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int U, 
   P->stage_bytes = (P->sc_off + P->R * P->seg_sc + 127) & ~127;
   P->ngroups = (int)(((int64_t)N + P->R - 1) / P->R);
   P->y_off = 128;
-  P->ysum_off = P->y_off + K * 4;
+  P->ysum_off = P->y_off + (K / 64) * YS * 8;
   P->stage_off = (P->ysum_off + (K / 32) * 4 + 127) & ~127;
   P->tbuf_off = tma_round16(P->stage_off + NS * P->stage_bytes);
   return true;
