@@ -27,6 +27,8 @@ bool shape_ok(int K, int bits) {
 
 namespace qmv {
 
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 static thread_local bool g_pdl = false;
 bool pdl_enabled() { return g_pdl; }
 void set_pdl(bool on) { g_pdl = on; }

@@ -66,6 +66,8 @@ bool pdl_enabled();
 void set_pdl(bool on);
 // Read (and optionally clear) the device error word set by bounded waits.
 int read_device_error(int clear, int* out);
+// Record a CUDA error as the calling thread's last one; returns QMV_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
 // M-column tiles on paired fp32 arithmetic (K a multiple of 64, M <= 32);
 // QMV_ERR_UNSUPPORTED when the shape does not fit them.
 int launch_tile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);

@@ -5,289 +5,41 @@
 // with exact products, scaled (group 32), and folded serially over blocks
 // ("Gemma4 raw-Metal loop on A19", section "What moved the needle": int2 at
 // 16 codes per word, exact products, fp32 in code order; the residual-add +
-// RMSNorm fold into the matvec prologue).
+// RMSNorm fold into the matvec prologue).  Fast mode runs the folded-offset
+// form of the same sums (qmv_decode.cuh).
 //
-// How:
-//   * Rows are processed in groups of R rows.  A group's codes (and its
-//     group-32 scales) are contiguous in memory, so one producer thread moves
-//     each group into a ring of NS shared-memory stages with two
-//     cp.async.bulk copies completing on the stage's "full" mbarrier.  The
-//     producer runs ahead of the math by up to NS groups (tens of KB in
-//     flight per SM) and starts before the prologue, since weights do not
-//     depend on the activations.
+// How (building blocks in qmv_pipe.cuh):
+//   * Rows are processed in groups of R rows, each in NSEG segments of K.  A
+//     producer warp moves each (group, segment) -- R rows of codes and their
+//     group-32 scales -- into a ring of NS shared-memory stages with two 2-D
+//     tensor copies completing on the stage's "full" mbarrier.  It runs ahead
+//     of the math by up to NS stages and starts before the prologue, since
+//     weights do not depend on the activations.
 //   * Compute warps: thread t owns one 64-code item (two 32-code blocks) of
-//     RP rows in parallel, U rows after another, and keeps that item's 64
-//     activations in registers as fp32 pairs (y_k, y_{32+k}).  A code field
-//     is turned into fp32 exactly by one LOP3: (w & (mask << o)) | 0x4B000000
-//     = 2^23 + u*2^o (every field is first brought below bit 16: the low and
-//     high halves of a word use the same o).  One packed sub.rn.f32x2 maps
-//     the pair (block 0, block 1) to v*2^o exactly, and one fma.rn.f32x2 with
-//     the activations pre-scaled by 2^-o advances both blocks' serial sums
-//     (y*2^-o times v*2^o is y*v exactly).  About 2 instructions per code.
+//     RP rows in parallel, U rows after another, reading the item's
+//     activations from a shared-memory table pre-scaled per bit offset.  Exact
+//     form: a field becomes fp32 exactly by one LOP3 ((w & (mask << o)) |
+//     0x4B000000 = 2^23 + u*2^o), one paired subtract gives v*2^o, and one
+//     paired FMA advances both blocks' serial sums.  Folded form: one 64-bit
+//     AND per field pair and one paired FMA.
 //   * Block sums (scaled) go to a double-buffered fold buffer; a dedicated
 //     fold warp adds them serially per row (one lane per row) and writes y,
 //     so the compute warps never wait at a CTA-wide barrier.
 //   * Every mbarrier wait is bounded; on timeout the kernel records an error
 //     code in the device error word, stops issuing, lets its own copies land
 //     and returns.
-#include <cuda.h>
-
-#include "qmv_internal.cuh"
+#include "qmv_pipe.cuh"
 
 namespace qmv {
 
 __device__ int g_qmv_error = 0;
 
-namespace {
-
-constexpr int NS = 4;                      // ring stages (a power of two)
-constexpr uint32_t SPIN_LIMIT = 1u << 22;  // tries per bounded wait (a backstop to the time limit)
-constexpr int ERR_TIMEOUT_FULL = 1, ERR_TIMEOUT_EMPTY = 2, ERR_TIMEOUT_TFULL = 3,
-              ERR_TIMEOUT_TEMPTY = 4, ERR_SMEM_ALIGN = 5;
-
-
-__device__ __forceinline__ uint32_t sa(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t tx) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(tx)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(sa(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// try_wait with a suspend-time hint: the warp sleeps in hardware until the
-// phase completes (it wakes at once then) or the hint elapses
-__device__ __forceinline__ bool mbar_try_hint(uint64_t* b, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(sa(b)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-constexpr uint32_t WAIT_HINT_NS = 20000;            // one suspended try
-constexpr uint64_t WAIT_LIMIT_NS = 500000000ull;    // give up after 0.5 s
-
-// Bounded wait.  Returns false (after setting the CTA's abort flag and the
-// device error word) if the phase does not complete within WAIT_LIMIT_NS (or
-// SPIN_LIMIT tries), or soon after another warp of the CTA has aborted.
-__device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
-                                       int code) {
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
-    if (mbar_try_hint(b, parity, WAIT_HINT_NS)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > WAIT_LIMIT_NS) break;
-  }
-  *abort_flag = 1;
-  atomicCAS(&g_qmv_error, 0, code);
-  return false;
-}
-
-// The common case inline (one try_wait, which itself suspends the warp for a
-// while), the bounded loop out of line.
-__device__ __forceinline__ bool mbar_wait_fast(uint64_t* b, uint32_t parity, volatile int* abort_flag,
-                                               int code) {
-  return mbar_try(b, parity) || mbar_wait(b, parity, abort_flag, code);
-}
-
-// Bounded wait that ignores the abort flag (used to let copies land).
-__device__ __noinline__ void mbar_drain(uint64_t* b, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 0; i < SPIN_LIMIT; ++i) {
-    if (mbar_try_hint(b, parity, WAIT_HINT_NS)) return;
-    if (global_ns() - t0 > WAIT_LIMIT_NS) break;
-  }
-  atomicCAS(&g_qmv_error, 0, ERR_TIMEOUT_FULL);
-}
-
-// 2-D tiled tensor copy global -> shared (box given by the tensor map),
-// completing on `bar`.  x is the innermost coordinate (in elements).
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          sa(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(sa(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void named_bar(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// The activation table: per 64-code item c, 32 steps of fp32 pairs at
-// y2f[2*(YS*c + step) + lane].  The item stride YS = 34 pairs (272 bytes)
-// keeps 16-byte loads of two consecutive steps aligned and spreads the
-// threads of a warp (consecutive items) over all banks; within an item the
-// steps are immediate offsets.
-constexpr int YS = 34;
-
-// Store 8 consecutive fp16 activations starting at element e0 (a multiple of
-// 8; element 64*c + 32*h + k) into the table.  Exact form: y * 2^-o(k), step
-// k holds (block 0, block 1) code k.  Folded form: y * 2^(FOLD_E - o(k)),
-// step 16*blk + CPW*p + j holds (code j of word 2p, of word 2p+1) of block
-// blk.
-template <int BITS, bool EXACT>
-__device__ __forceinline__ void store_y8(float* y2f, int e0, const uint32_t (&h8)[4]) {
-  constexpr int CPW = 32 / BITS, HALF = CPW / 2;
-  const int c = e0 >> 6, h = (e0 >> 5) & 1, k0 = e0 & 31;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int k = k0 + e;
-    const int j = k % CPW, o = BITS * (j % HALF);
-    const __half2 v = u32_as_h2(h8[e >> 1]);
-    const float f = (e & 1) ? __high2float(v) : __low2float(v);
-    if (EXACT) {
-      y2f[2 * (YS * c + k) + h] = __fmul_rn(f, pow2f(-o));
-    } else {
-      const int wi = k / CPW, step = 16 * h + CPW * (wi >> 1) + j;
-      y2f[2 * (YS * c + step) + (wi & 1)] = __fmul_rn(f, pow2f(FOLD_E - o));
-    }
-  }
-}
-
-// Both blocks of one 64-code item, for U rows at once.  w[u][0 .. 2*WPB-1]:
-// words of block 0 then block 1.  yc: the item's activation pairs
-// (y'_k, y'_{32+k}), two steps per 16-byte load; one pair serves all U rows.  y'_k = y_k * 2^-o(k) where o(k)
-// is the bit offset the code k is decoded at, so y'_k * (v_k * 2^o(k)) =
-// y_k * v_k exactly (powers of two; no underflow for fp16 inputs).  acc[u] =
-// (p0, p1) are the two blocks' serial sums.  Fields in the high 16-bit half
-// of a word are first shifted down by 16, so every field is masked below
-// bit 16.  (Exact form; the folded form is block_dots_fold.)
-template <int BITS, int U>
-__device__ __forceinline__ void item_dots(const uint32_t (&w)[U][64 * BITS / 32],
-                                          const u64* __restrict__ yc, u64 (&acc)[U]) {
-  constexpr int CPW = 32 / BITS;   // codes per word
-  constexpr int HALF = CPW / 2;    // codes per 16-bit half
-  constexpr int WPB = 32 / CPW;    // words per block
-  constexpr uint32_t MASK = (1u << BITS) - 1u;
-#pragma unroll
-  for (int wi = 0; wi < WPB; ++wi) {
-    uint32_t h0[U], h1[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      h0[u] = w[u][wi] >> 16;
-      h1[u] = w[u][WPB + wi] >> 16;
-    }
-#pragma unroll
-    for (int j = 0; j < CPW; ++j) {
-      const int o = BITS * (j % HALF);
-      const float offf = pow2f(23) + (float)(1 << (BITS - 1 + o));
-      const u64 off = pk(offf, offf);
-      const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yc + wi * CPW + (j & ~1));
-      const u64 y = (j & 1) ? y2.y : y2.x;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint32_t a = (j < HALF) ? w[u][wi] : h0[u];
-        const uint32_t b = (j < HALF) ? w[u][WPB + wi] : h1[u];
-        const u64 v = decode2(a, b, MASK << o, off);
-        acc[u] = ffma2(y, v, acc[u]);
-      }
-    }
-  }
-}
-
-// Folded form, both 32-code blocks of a 64-code item for U rows: wp[u][q]
-// are the item's words as 64-bit pairs (words 2q, 2q+1), so a pair's two
-// fields at one offset are masked by one 64-bit AND straight into the
-// register pair the paired FMA reads.  Lane 0 of acc[u][blk] sums block
-// blk's even words, lane 1 its odd words, each serially in code order; the
-// two blocks' chains are interleaved for independent work.  The high 16-bit
-// fields come from the pair shifted right by 16 as a whole: what crosses from
-// the odd word into the even word's upper half is masked off.
-template <int BITS, int U>
-__device__ __forceinline__ void item_dots_fold(const u64 (&wp)[U][BITS], const u64* __restrict__ yc,
-                                               u64 (&acc)[U][2]) {
-  constexpr int CPW = 32 / BITS, HALF = CPW / 2;
-  constexpr int NP = 16 / CPW;                 // word pairs per block
-  constexpr uint32_t MASK = (1u << BITS) - 1u;
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    u64 lo[U][2], hi[U][2];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-#pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        lo[u][blk] = wp[u][blk * NP + p];
-        hi[u][blk] = lo[u][blk] >> 16;
-      }
-#pragma unroll
-    for (int j = 0; j < CPW; ++j) {
-      const uint32_t m = MASK << (BITS * (j % HALF));
-      const u64 mm = ((u64)m << 32) | m;
-#pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        const ulonglong2 y2 =
-            *reinterpret_cast<const ulonglong2*>(yc + 16 * blk + CPW * p + (j & ~1));
-        const u64 y = (j & 1) ? y2.y : y2.x;
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          acc[u][blk] = ffma2(y, ((j < HALF) ? lo[u][blk] : hi[u][blk]) & mm, acc[u][blk]);
-      }
-    }
-  }
-}
-
-}  // namespace
-
-// Launch plan (host computes it; the kernel reads it).
-//
-// Rows are processed in groups of R, and each group in NSEG segments of KS
-// codes (KS = K when K <= 2048, else the largest multiple of 256 up to 2048
-// that divides K).  A pipeline stage holds one (group, segment): R rows x KS
-// codes plus their group-32 scales.  The fold warp keeps one accumulator per
-// row across the segments of a group, so the fold stays serial over all K/32
-// blocks of the row while 32 rows are folded side by side.
-struct TmaPlan {
-  int C;             // 64-code items per row (table layout)
-  int Cs;            // 64-code items per segment
-  int KS, NSEG;      // codes per segment, segments per row
-  int RP;            // rows in parallel (Cs*RP <= Tc)
-  int R;             // rows per group = RP*U (<= 32: one fold lane per row)
-  int Tc;            // compute threads (multiple of 32)
-  int row_bytes;     // code bytes per row
-  int seg_bytes;     // code bytes per row per segment
-  int seg_sc;        // scale bytes per row per segment (0 with one scale per row)
-  int sc_off;        // offset of the scales inside a stage (128-byte aligned)
-  int stage_bytes;   // whole stage, a multiple of 128 bytes
-  int ngroups;       // ceil(N / R)
-  int y_off, ysum_off, stage_off, tbuf_off;   // shared-memory offsets (bytes)
-};
-
-__host__ __device__ inline int tma_round16(int x) { return (x + 15) & ~15; }
+using namespace pipe;
 
 template <int BITS, bool PERROW, bool FUSED, bool EXACT, int U, int MAXT>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     gemv_tma_kernel(GemvArgs a, TmaPlan P, const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_scales) {
-  constexpr int IW = 64 * BITS / 32;   // words per item
   extern __shared__ __align__(128) unsigned char sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
   uint64_t* empty = full + NS;
@@ -295,15 +47,15 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   uint64_t* tempty = tfull + 2;
   volatile int* abort_f = reinterpret_cast<volatile int*>(sm + 96);
   float* inv_sh = reinterpret_cast<float*>(sm + 100);
-  float* y2f = reinterpret_cast<float*>(sm + P.y_off);   // pairs [k][item] as fp32
+  float* y2f = reinterpret_cast<float*>(sm + P.y_off);     // activation table
   float* ysum = reinterpret_cast<float*>(sm + P.ysum_off); // folded form: 2^(b-1) * S per block
   unsigned char* stages = sm + P.stage_off;
   float* tbuf = reinterpret_cast<float*>(sm + P.tbuf_off);
+  int* err = &g_qmv_error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = a.K, NB = K / 32, R = P.R;
-  const int NBS = P.KS / 32;             // blocks per segment
-  const int GS = NBS + 1;                // fold-buffer row stride
+  const int R = P.R;
+  const int GS = P.KS / 32 + 1;          // fold-buffer row stride
   const int my_groups = (blockIdx.x < (unsigned)P.ngroups)
                             ? (P.ngroups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
                             : 0;
@@ -316,7 +68,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   // tensor copies need 128-byte aligned destinations: the dynamic shared
   // memory window starts aligned when there is no static shared memory
   if ((sa(sm) & 127u) != 0u) {
-    if (threadIdx.x == 0) atomicCAS(&g_qmv_error, 0, ERR_SMEM_ALIGN);
+    if (threadIdx.x == 0) atomicCAS(err, 0, ERR_SMEM_ALIGN);
     return;
   }
   if (threadIdx.x == 0) {
@@ -342,10 +94,9 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     int64_t g = blockIdx.x;
     for (int i = 0; i < my_stages; ++i) {
       const int s = i & (NS - 1);
-      if (i >= NS && !mbar_wait_fast(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY)) break;
+      if (i >= NS && !mbar_wait_fast(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY, err)) break;
       if (*abort_f) break;
       const int64_t r0 = g * R;
-      const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
       // one box of R rows x one segment: rows past N are zero-filled, the
       // transaction count is always the whole box
       unsigned char* st = stages + (size_t)s * P.stage_bytes;
@@ -364,7 +115,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     // let every copy this warp issued land before the CTA can exit
     if (lane == 0)
       for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-        mbar_drain(&full[j % NS], (j / NS) & 1);
+        mbar_drain(&full[j % NS], (j / NS) & 1, err);
     return;
   }
 
@@ -374,87 +125,10 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   // without a programmatic launch).  The producer above never waits: packed
   // weights are not written by the kernels a matvec overlaps.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int tt = threadIdx.x - 32;        // 0 .. 32 + Tc - 1
-  const int nt = 32 + P.Tc;
-  if (FUSED) {
-    float* bsum = tbuf;                   // the fold buffer is free until the main loop
-    __half* h_out = (blockIdx.x == 0) ? a.h_out : nullptr;
-    for (int b = tt; b < NB; b += nt) {
-      float blk = 0.0f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 32 * b + 8 * q));
-        const uint4 rv = __ldg(reinterpret_cast<const uint4*>(a.r + 32 * b + 8 * q));
-        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w};
-        uint32_t hs[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half2 xx = u32_as_h2(xs[e]), rr = u32_as_h2(rs[e]);
-          const __half lo = __float2half_rn(__fadd_rn(__low2float(xx), __low2float(rr)));
-          const __half hi = __float2half_rn(__fadd_rn(__high2float(xx), __high2float(rr)));
-          const float fl = __half2float(lo), fh = __half2float(hi);
-          blk = __fmaf_rn(fl, fl, blk);
-          blk = __fmaf_rn(fh, fh, blk);
-          hs[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-        }
-        if (h_out)
-          *reinterpret_cast<uint4*>(h_out + 32 * b + 8 * q) = make_uint4(hs[0], hs[1], hs[2], hs[3]);
-      }
-      bsum[b] = blk;
-    }
-    named_bar(1, nt);
-    if (tt == 0) {
-      float ss = 0.0f;
-      for (int b = 0; b < NB; ++b) ss = __fadd_rn(ss, bsum[b]);
-      const float mean = __fdiv_rn(ss, (float)K);
-      *inv_sh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
-    }
-    named_bar(1, nt);
-    const float inv = *inv_sh;
-    for (int v8 = tt; v8 < K / 8; v8 += nt) {
-      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 8 * v8));
-      const uint4 rv = __ldg(reinterpret_cast<const uint4*>(a.r + 8 * v8));
-      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + 8 * v8));
-      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, rs[4] = {rv.x, rv.y, rv.z, rv.w},
-                     gs[4] = {gv.x, gv.y, gv.z, gv.w};
-      uint32_t ys[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __half2 xx = u32_as_h2(xs[e]), rr = u32_as_h2(rs[e]), gg = u32_as_h2(gs[e]);
-        const float hl = __half2float(__float2half_rn(__fadd_rn(__low2float(xx), __low2float(rr))));
-        const float hh = __half2float(__float2half_rn(__fadd_rn(__high2float(xx), __high2float(rr))));
-        const __half yl = __float2half_rn(__fmul_rn(__fmul_rn(hl, inv), __low2float(gg)));
-        const __half yh = __float2half_rn(__fmul_rn(__fmul_rn(hh, inv), __high2float(gg)));
-        ys[e] = (uint32_t)__half_as_ushort(yl) | ((uint32_t)__half_as_ushort(yh) << 16);
-      }
-      store_y8<BITS, EXACT>(y2f, 8 * v8, ys);
-    }
-  } else {
-    for (int v8 = tt; v8 < K / 8; v8 += nt) {
-      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + 8 * v8));
-      const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-      store_y8<BITS, EXACT>(y2f, 8 * v8, xs);
-    }
-  }
-  if (!EXACT) {
-    // block sums of the activations in the order of the dots (even and odd
-    // words serially, then added), read back from the scaled pairs
-    // (y' * 2^(o - FOLD_E) = y exactly), times the offset 2^(b-1)
-    named_bar(1, nt);
-    constexpr int CPW = 32 / BITS, HALF = CPW / 2;
-    for (int b = tt; b < NB; b += nt) {
-      const float* src = y2f + 2 * (YS * (b >> 1) + 16 * (b & 1));
-      float S0 = 0.0f, S1 = 0.0f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float sc = pow2f(BITS * ((t % CPW) % HALF) - FOLD_E);
-        S0 = __fmaf_rn(src[2 * t], sc, S0);
-        S1 = __fmaf_rn(src[2 * t + 1], sc, S1);
-      }
-      ysum[b] = __fmul_rn(__fadd_rn(S0, S1), (float)(1 << (BITS - 1)));
-    }
-  }
-  named_bar(1, nt);
+  // the fold buffer is free until the main loop: it holds the block sums
+  build_table<BITS, FUSED, EXACT>(a, y2f, ysum, tbuf, inv_sh, (blockIdx.x == 0) ? a.h_out : nullptr,
+                                  threadIdx.x - 32, 32 + P.Tc, 1);
+  named_bar(1, 32 + P.Tc);
 
   // ---------------------------------------------------------- fold warp --
   if (warp == 1) {
@@ -463,33 +137,10 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     int64_t g = blockIdx.x;
     for (int i = 0; i < my_stages; ++i) {
       const int tb = i & 1;
-      if (!mbar_wait_fast(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL)) break;
+      if (!mbar_wait_fast(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL, err)) break;
       const int64_t r0 = g * R;
       const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
-      if (lane < rows) {
-        const float* tr = tbuf + (size_t)(tb * R + lane) * GS;
-        if (!PERROW) {
-          if (seg == 0) acc = 0.0f;
-#pragma unroll 8
-          for (int b = 0; b < NBS; ++b) acc = __fadd_rn(acc, tr[b]);
-        } else {
-          int b0 = 0;
-          if (seg == 0) {
-            acc = tr[0];
-            b0 = 1;
-          }
-#pragma unroll 8
-          for (int b = b0; b < NBS; ++b) acc = __fadd_rn(acc, tr[b]);
-        }
-        if (seg == P.NSEG - 1) {
-          float out = acc;
-          if (PERROW) out = __fadd_rn(0.0f, __fmul_rn(acc, __half2float(a.scales[r0 + lane])));
-          if (a.y_f16)
-            reinterpret_cast<__half*>(a.y)[r0 + lane] = __float2half_rn(out);
-          else
-            reinterpret_cast<float*>(a.y)[r0 + lane] = out;
-        }
-      }
+      fold_stage(a, P, tbuf + (size_t)tb * R * GS, GS, lane, r0, rows, seg, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[tb]);
       if (++seg == P.NSEG) {
@@ -512,91 +163,13 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   for (int i = 0; i < my_stages; ++i) {
     const int s = i & (NS - 1);
     const int tb = i & 1;
-    if (!mbar_wait_fast(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL)) break;
-    if (i >= 2 && !mbar_wait_fast(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY)) break;
+    if (!mbar_wait_fast(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL, err)) break;
+    if (i >= 2 && !mbar_wait_fast(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY, err)) break;
     const int64_t r0 = g * R;
     const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
-    if (active && !EXACT) {
-      // folded form: rows past N in the box are zero-filled, so every row of
-      // the group is computed (the fold warp stores only real rows)
-      const unsigned char* st = stages + (size_t)s * P.stage_bytes;
-      u64 wp[U][IW / 2];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int r = rp * U + u;
-        const ulonglong2* src =
-            reinterpret_cast<const ulonglong2*>(st + (size_t)r * P.seg_bytes + (size_t)c * (IW * 4));
-#pragma unroll
-        for (int q = 0; q < IW / 4; ++q) {
-          const ulonglong2 v = src[q];
-          wp[u][2 * q] = v.x;
-          wp[u][2 * q + 1] = v.y;
-        }
-      }
-      const __half* scs = reinterpret_cast<const __half*>(st + P.sc_off);
-      const float2 bS = *reinterpret_cast<const float2*>(ysum + 2 * (seg * P.Cs + c));
-      u64 acc[U][2];
-#pragma unroll
-      for (int u = 0; u < U; ++u) acc[u][0] = acc[u][1] = 0ull;
-      item_dots_fold<BITS, U>(wp, y2s + YS * (seg * P.Cs + c), acc);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int r = rp * U + u;
-        float2 sc = make_float2(1.0f, 1.0f);
-        if (!PERROW) sc = __half22float2(*reinterpret_cast<const __half2*>(scs + (size_t)r * NBS + 2 * c));
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          float pe, po;
-          upk(acc[u][blk], pe, po);
-          float pb = fold_block(__fadd_rn(pe, po), blk ? bS.y : bS.x);
-          if (!PERROW) pb = __fmul_rn(pb, blk ? sc.y : sc.x);
-          tbuf[(size_t)(tb * R + r) * GS + 2 * c + blk] = pb;
-        }
-      }
-    } else if (active) {
-      const unsigned char* st = stages + (size_t)s * P.stage_bytes;
-      uint32_t w[U][IW];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int r = rp * U + u;
-        if (r < rows) {
-          const uint4* src = reinterpret_cast<const uint4*>(st + (size_t)r * P.seg_bytes + (size_t)c * (IW * 4));
-#pragma unroll
-          for (int q = 0; q < IW / 4; ++q) {
-            const uint4 v = src[q];
-            w[u][4 * q + 0] = v.x;
-            w[u][4 * q + 1] = v.y;
-            w[u][4 * q + 2] = v.z;
-            w[u][4 * q + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < IW; ++q) w[u][q] = 0x00000000u;
-        }
-      }
-      u64 acc[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) acc[u] = 0ull;
-      item_dots<BITS, U>(w, y2s + YS * (seg * P.Cs + c), acc);
-      const __half* scs = reinterpret_cast<const __half*>(st + P.sc_off);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int r = rp * U + u;
-        if (r < rows) {
-          float p0, p1;
-          upk(acc[u], p0, p1);
-          float* dst = tbuf + (size_t)(tb * R + r) * GS + 2 * c;
-          if (PERROW) {
-            dst[0] = p0;
-            dst[1] = p1;
-          } else {
-            const __half2 s2 = *reinterpret_cast<const __half2*>(scs + (size_t)r * NBS + 2 * c);
-            dst[0] = __fmul_rn(p0, __low2float(s2));
-            dst[1] = __fmul_rn(p1, __high2float(s2));
-          }
-        }
-      }
-    }
+    if (active)
+      compute_stage<BITS, PERROW, EXACT, U>(stages + (size_t)s * P.stage_bytes, P, c, rp, seg, rows, y2s,
+                                            ysum, tbuf + (size_t)tb * R * GS, GS);
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&empty[s]);
@@ -610,15 +183,6 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
 }
 
 // ------------------------------------------------------------- launcher --
-
-// Codes per segment: the whole row up to 2048, else the largest multiple of
-// 256 up to 2048 that divides K.
-static int tma_segment(int K) {
-  if (K <= 2048) return K;
-  for (int d = 8; d >= 1; --d)
-    if ((K / 256) % d == 0) return 256 * d;
-  return 256;
-}
 
 // Plan for about `tc_target` compute threads and U rows per thread
 // (RP*U <= 32 rows per group: one fold lane per row).
@@ -674,7 +238,35 @@ static EncodeTiledFn encode_fn() {
 
 // Tensor maps of a pack for a plan: codes as UINT64 [N][row_bytes/8] with a
 // box of (segment bytes / 8) x R, scales as UINT16 [N][K/32] with a box of
-// (K_seg / 32) x R.  Cached per thread (a few entries).
+// (K_seg / 32) x R.  tensor_maps caches them per thread (a few entries).
+bool encode_pack_maps(const GemvArgs& a, const TmaPlan& P, CUtensorMap* tc, CUtensorMap* ts) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)(P.row_bytes / 8), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)P.row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(P.seg_bytes / 8), (cuuint32_t)P.R};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(tc, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, (void*)a.codes, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  if (a.perrow) {
+    *ts = *tc;   // unused
+  } else {
+    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 32) * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)(P.KS / 32), (cuuint32_t)P.R};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void*)a.scales, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 static bool tensor_maps(const GemvArgs& a, int bits, const TmaPlan& P, CUtensorMap* tc, CUtensorMap* ts) {
   struct Entry { const void* codes; const void* scales; int N, K, bits, R, KS; CUtensorMap c, s; };
   static thread_local Entry cache[8];
@@ -688,8 +280,6 @@ static bool tensor_maps(const GemvArgs& a, int bits, const TmaPlan& P, CUtensorM
       return true;
     }
   }
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
   Entry e;
   e.codes = a.codes;
   e.scales = a.scales;
@@ -698,28 +288,7 @@ static bool tensor_maps(const GemvArgs& a, int bits, const TmaPlan& P, CUtensorM
   e.bits = bits;
   e.R = P.R;
   e.KS = P.KS;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)(P.row_bytes / 8), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)P.row_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)(P.seg_bytes / 8), (cuuint32_t)P.R};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&e.c, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, (void*)a.codes, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
-  if (a.perrow) {
-    e.s = e.c;   // unused
-  } else {
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 32), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 32) * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)(P.KS / 32), (cuuint32_t)P.R};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&e.s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void*)a.scales, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return false;
-  }
+  if (!encode_pack_maps(a, P, &e.c, &e.s)) return false;
   cache[next] = e;
   next = (next + 1) % 8;
   if (valid < 8) ++valid;
@@ -904,11 +473,15 @@ int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* er
 }
 
 int read_tc_error(int clear, int* out);
+int read_chain_error(int clear, int* out);
 
 int read_device_error(int clear, int* out) {
-  int t = 0;
+  int t = 0, ch = 0;
   const int et = read_tc_error(clear, &t);
   if (et != 0) return et;
+  const int ec = read_chain_error(clear, &ch);
+  if (ec != 0) return ec;
+  if (ch) t = ch;
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_qmv_error, sizeof(int));
   if (e != cudaSuccess) return (int)e;

@@ -41,6 +41,13 @@ SIGNATURES = {
     "qmv_last_cuda_error": (_I, []),
     "qmv_device_error": (_I, [ctypes.POINTER(_I), _I]),
     "qmv_set_pdl": (_I, [_I]),
+    "qmv_chain_workspace_bytes": (ctypes.c_size_t, [_I]),
+    "qmv_chain_create": (_I, [ctypes.POINTER(_P), _I, _P, ctypes.c_size_t]),
+    "qmv_chain_add_gemv": (_I, [_P, _P, _P, _P, _I, _I]),
+    "qmv_chain_add_fused_rmsnorm_gemv": (_I, [_P, _P, _P, _P, _P, _F, _P, _P, _I, _I]),
+    "qmv_chain_run": (_I, [_P, _P]),
+    "qmv_chain_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "qmv_chain_destroy": (_I, [_P]),
 }
 
 
@@ -204,3 +211,51 @@ def qmv_device_error(clear: bool = True) -> int:
     v = _I()
     _check("qmv_device_error", _lib.qmv_device_error(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+class Chain:
+    """A chain of M = 1 matvecs run by one persistent launch (qmv_chain_*).
+    The workspace is a torch uint8 device tensor; the tensors of every added
+    op are kept referenced for the chain's lifetime."""
+
+    def __init__(self, max_ops: int, device=None):
+        n = _lib.qmv_chain_workspace_bytes(max_ops)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+        h = _P()
+        _check("qmv_chain_create", _lib.qmv_chain_create(ctypes.byref(h), max_ops, _dptr(self.ws), n))
+        self.handle = h
+        self._keep = []
+
+    def add_gemv(self, p: Pack, x, y, y_dtype=QMV_F32, mode=QMV_FAST):
+        _check("qmv_chain_add_gemv", _lib.qmv_chain_add_gemv(self.handle, p.handle, _dptr(x), _dptr(y),
+                                                             y_dtype, mode))
+        self._keep += [p, x, y]
+        return self
+
+    def add_fused_rmsnorm_gemv(self, p: Pack, x, residual, gamma, eps, h_out, y, y_dtype=QMV_F32,
+                               mode=QMV_FAST):
+        _check("qmv_chain_add_fused_rmsnorm_gemv", _lib.qmv_chain_add_fused_rmsnorm_gemv(
+            self.handle, p.handle, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out),
+            _dptr(y), y_dtype, mode))
+        self._keep += [p, x, residual, gamma, h_out, y]
+        return self
+
+    def run(self, stream=None):
+        _check("qmv_chain_run", _lib.qmv_chain_run(self.handle, _stream(stream)))
+
+    def info(self):
+        n, b, sm = _I(), _I(), _I()
+        _check("qmv_chain_info", _lib.qmv_chain_info(self.handle, ctypes.byref(n), ctypes.byref(b),
+                                                     ctypes.byref(sm)))
+        return {"ops": n.value, "barriers": b.value, "smem": sm.value}
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            _lib.qmv_chain_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -36,14 +36,24 @@
  * field holds u = v + 2^(bits-1) for the signed code v, so int2 fields
  * 0,1,2,3 decode to -2,-1,0,1.  Scales are fp16 [N][K/group].
  *
- * Accumulation order (both modes of the CUDA-core paths, M <= 32): for each
- * output scalar, each block of 32 consecutive codes is summed serially in k
- * in fp32 (products are exact); with group 32 the block sum is multiplied by
- * its scale (rounded) and added to the accumulator (rounded), blocks in
- * order; with one scale per row (group == K) the block sums are added
- * serially and the total is multiplied by the scale once.  This is the
+ * Accumulation order (QMV_EXACT, CUDA-core paths, M <= 32 per launch): for
+ * each output scalar, each block of 32 consecutive codes is summed serially
+ * in k in fp32 (products are exact); with group 32 the block sum is
+ * multiplied by its scale (rounded) and added to the accumulator (rounded),
+ * blocks in order; with one scale per row (group == K) the block sums are
+ * added serially and the total is multiplied by the scale once.  This is the
  * oracle's order, so QMV_EXACT results are bit-identical to it, and every
  * column of an M-tile is bit-identical to the M = 1 result.
+ *
+ * QMV_FAST (M <= 32): the same blocks, scales and fold, with the code offset
+ * taken out of the per-code work: each block is summed as sum(y*u) over the
+ * unsigned fields u (even and odd words in two serial chains, then added)
+ * minus 2^(bits-1) times the block's activation sum formed in the same
+ * order.  Results are within max |y - ref| <= 1e-3*(1+|ref|) of the oracle
+ * (in practice a few fp32 ulps of the block sums), a block of zero codes
+ * gives exactly 0, and every column of an M-tile is still bit-identical to
+ * the QMV_FAST M = 1 result.  Shapes outside the M = 1 pipeline (K not a
+ * multiple of 256) keep the exact order in both modes.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -62,6 +72,7 @@ extern "C" {
 #endif
 
 typedef struct qmv_pack qmv_pack;   /* opaque host descriptor; owns no device memory */
+typedef struct qmv_chain qmv_chain; /* opaque host descriptor of a matvec chain */
 
 typedef enum {
     QMV_OK = 0,
@@ -112,10 +123,12 @@ QMV_API int qmv_pack_weights(qmv_pack *p, const int8_t *d_codes_in, const uint16
  * x[m][k] * v[n][k]) * s[n][g] in the order stated at the top of this file.
  * [A19] int2 item (exact products, fp32 in code order); [PLAY] K-order-fixed
  * row for M <= 16 and matrix-unit row for M >= 64.
- *   M            1 .. 4096.  M <= 32 runs the CUDA-core kernels (bit-exact
- *                in both modes); M > 32 with QMV_FAST runs tcgen05 tensor-core
- *                tiles (fp32 accumulate, hardware order); M > 32 with
- *                QMV_EXACT runs the CUDA-core kernels 32 columns at a time.
+ *   M            1 .. 4096.  M <= 32 runs the CUDA-core kernels (QMV_EXACT
+ *                bit-exact, QMV_FAST within tolerance); M > 32 with QMV_FAST
+ *                runs tcgen05 tensor-core tiles for int2 (fp32 accumulate,
+ *                hardware order) and the CUDA-core tiles for int4/int8; M > 32
+ *                with QMV_EXACT runs the CUDA-core kernels 32 columns at a
+ *                time.
  *   N, K, bits, group  must equal the pack's (QMV_ERR_SHAPE otherwise).
  *   x            device fp16 [M][K], 16-byte aligned.
  *   y            device [M][N] of y_dtype (fp32, or fp16 = RNE of the fp32
@@ -195,6 +208,65 @@ QMV_API int qmv_last_cuda_error(void);
  * Errors: INVALID_ARG (out NULL), CUDA.
  */
 QMV_API int qmv_device_error(int *out, int clear);
+
+/*
+ * Chains: a sequence of M = 1 matvecs (plain or with the fused residual-add +
+ * RMSNorm prologue) run by one persistent launch -- the whole-layer / multi-
+ * stage single dispatch of [A19] "The parked levers" (mega-kernel item),
+ * against the per-dispatch tax of "What moved the needle".  Each op computes
+ * exactly what the matching qmv_gemv / qmv_fused_rmsnorm_gemv call computes
+ * (bit for bit, same mode), in order.  The weight stream runs across op
+ * boundaries; a grid-wide barrier is inserted only before an op whose
+ * activation reads (x, residual, gamma) overlap the outputs (y, h_out) of an
+ * earlier op since the last barrier, or whose outputs overlap the reads or
+ * outputs of such an op.  Packed weights must not change while a chain runs.
+ * Every op needs K % 256 == 0.
+ *
+ * qmv_chain_workspace_bytes -- device bytes a chain of up to max_ops ops
+ * needs (barrier words + op table); 0 if max_ops < 1.
+ */
+QMV_API size_t qmv_chain_workspace_bytes(int max_ops);
+
+/*
+ * qmv_chain_create -- an empty chain using the caller's device workspace
+ * (256-byte aligned, at least qmv_chain_workspace_bytes(max_ops) bytes; it
+ * must outlive the chain and must not be shared by two chains that run at
+ * the same time).  Host only.
+ * Errors: INVALID_ARG (NULL, max_ops < 1, workspace too small), ALIGNMENT.
+ */
+QMV_API int qmv_chain_create(qmv_chain **out, int max_ops, void *d_workspace,
+                             size_t workspace_bytes);
+
+/*
+ * qmv_chain_add_gemv / qmv_chain_add_fused_rmsnorm_gemv -- append one M = 1
+ * matvec with the arguments of qmv_gemv / qmv_fused_rmsnorm_gemv (pointers
+ * are recorded, not read, until qmv_chain_run).  Host only.
+ * Errors: INVALID_ARG (NULL, chain full, bad enum), ALIGNMENT, UNSUPPORTED
+ * (K % 256 != 0, or K too large for the chain's shared memory).
+ */
+QMV_API int qmv_chain_add_gemv(qmv_chain *c, const qmv_pack *p, const void *x, void *y,
+                               int y_dtype, int mode);
+QMV_API int qmv_chain_add_fused_rmsnorm_gemv(qmv_chain *c, const qmv_pack *p, const void *x,
+                                             const void *residual, const void *gamma, float eps,
+                                             void *h_out, void *y, int y_dtype, int mode);
+
+/*
+ * qmv_chain_run -- run every op of the chain, in order, as one cooperative
+ * launch of one CTA per SM on `stream`.  The first run after ops were added
+ * copies the op table to the workspace synchronously; later runs only clear
+ * the barrier words (an async memset) and launch, and can be captured in a
+ * CUDA graph.  Two runs of chains that share a workspace must not overlap.
+ * A bounded device wait that runs out shows in qmv_device_error.
+ * Errors: INVALID_ARG, UNSUPPORTED (kernel does not fit an SM), CUDA.
+ */
+QMV_API int qmv_chain_run(qmv_chain *c, void *stream);
+
+/* qmv_chain_info -- ops, inserted grid barriers, and the kernel's dynamic
+ * shared memory (any out pointer may be NULL). */
+QMV_API int qmv_chain_info(const qmv_chain *c, int *n_ops, int *n_barriers, int *smem_bytes);
+
+/* qmv_chain_destroy -- free the host descriptor (never the workspace). */
+QMV_API int qmv_chain_destroy(qmv_chain *c);
 
 #ifdef __cplusplus
 }
