@@ -6,6 +6,11 @@ Workload (one "step"): one synthetic decode layer at M = 1, d_model 2048 --
   residual-add + RMSNorm fused into gate/up          (int2, 16384 x 2048, group 32)
   down                                               (int2, 2048 x 8192, group 32)
 = 21,037,056 packed bytes (codes + fp16 scales) per layer, 4 kernel launches.
+Each matvec reads the previous one's fp16 output, as in a decode loop (the
+attention and the gated activation between them are not part of this path:
+o_proj reads the first 2048 q/k/v outputs, down the first 8192 gate/up
+outputs), and a layer's outputs (down's y, the residual h2) are the next
+layer's inputs.
 `--layers L` distinct layers are resident (default 32, 673 MB, > 5x L2) and
 the steps walk through them in turn, so every step reads its weights from
 HBM (inputs larger than L2; no flush needed).
@@ -195,14 +200,36 @@ def host_inputs():
     return dict(x=x, r=r, g1=g1, g2=g2, attn=attn, act=act)
 
 
+def layer_ops(lay, b):
+    """One decode layer as 4 dependent matvecs: (kind, pack, x, residual,
+    gamma, h_out, y).  x, r -> q/k/v (h) -> o -> gate/up (h2 -> r) -> down
+    (y -> x)."""
+    return [("fused", lay["qkv"], b["x"], b["r"], b["g1"], b["h"], b["y_qkv"]),
+            ("gemv", lay["o"], b["y_qkv"][:, :D_MODEL], None, None, None, b["y_o"]),
+            ("fused", lay["gateup"], b["y_o"], b["h"], b["g2"], b["r"], b["y_gu"]),
+            ("gemv", lay["down"], b["y_gu"][:, :D_FF], None, None, None, b["x"])]
+
+
 def run_layer(qmv, lay, b, stream):
-    """One decode layer: 4 launches on `stream`."""
-    qmv.qmv_fused_rmsnorm_gemv(lay["qkv"], b["x"], b["r"], b["g1"], 1e-6, h_out=b["h"],
-                               y=b["y_qkv"], mode=qmv.QMV_FAST, stream=stream)
-    qmv.qmv_gemv(lay["o"], b["attn"], y=b["y_o"], mode=qmv.QMV_FAST, stream=stream)
-    qmv.qmv_fused_rmsnorm_gemv(lay["gateup"], b["attn"], b["h"], b["g2"], 1e-6, h_out=b["h2"],
-                               y=b["y_gu"], mode=qmv.QMV_FAST, stream=stream)
-    qmv.qmv_gemv(lay["down"], b["act"], y=b["y_down"], mode=qmv.QMV_FAST, stream=stream)
+    """One decode layer: 4 launches on `stream`, fp16 outputs."""
+    for kind, p, x, r, g, h, y in layer_ops(lay, b):
+        if kind == "fused":
+            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, 1e-6, h_out=h, y=y, y_dtype=qmv.QMV_F16,
+                                       mode=qmv.QMV_FAST, stream=stream)
+        else:
+            qmv.qmv_gemv(p, x, y=y, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
+
+
+def chain_layers(qmv, layers, b, n):
+    """The same n layers (rotating over the resident ones) as one persistent chain."""
+    ch = qmv.Chain(4 * n)
+    for i in range(n):
+        for kind, p, x, r, g, h, y in layer_ops(layers[i % len(layers)], b):
+            if kind == "fused":
+                ch.add_fused_rmsnorm_gemv(p, x, r, g, 1e-6, h, y, y_dtype=qmv.QMV_F16)
+            else:
+                ch.add_gemv(p, x, y, y_dtype=qmv.QMV_F16)
+    return ch
 
 
 def gpu_arm(args, rank, world, local):
@@ -215,13 +242,9 @@ def gpu_arm(args, rank, world, local):
     L = args.layers
     layers = build_layers(L, dev)
     hin = host_inputs()
-    b = {k: torch.from_numpy(v).to(dev) for k, v in hin.items()}
-    b["h"] = torch.empty(1, D_MODEL, dtype=torch.float16, device=dev)
-    b["h2"] = torch.empty(1, D_MODEL, dtype=torch.float16, device=dev)
-    b["y_qkv"] = torch.empty(1, 2560, device=dev)
-    b["y_o"] = torch.empty(1, D_MODEL, device=dev)
-    b["y_gu"] = torch.empty(1, 2 * D_FF, device=dev)
-    b["y_down"] = torch.empty(1, D_MODEL, device=dev)
+    b = {k: torch.from_numpy(hin[k]).to(dev) for k in ("x", "r", "g1", "g2")}
+    f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
+    b.update(h=f16(D_MODEL), y_qkv=f16(2560), y_o=f16(D_MODEL), y_gu=f16(2 * D_FF))
     K, W = args.steps, args.warmup
 
     # dependent matvecs overlap through programmatic dependent launch
@@ -248,9 +271,9 @@ def gpu_arm(args, rank, world, local):
     g_dom = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_dom, stream=stream):
         for li in range(L):
-            qmv.qmv_fused_rmsnorm_gemv(layers[li]["gateup"], b["attn"], b["h"], b["g2"], 1e-6,
-                                       h_out=b["h2"], y=b["y_gu"], mode=qmv.QMV_FAST,
-                                       stream=stream)
+            kind, p, x, r, g, h, y = layer_ops(layers[li], b)[2]
+            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, 1e-6, h_out=h, y=y, y_dtype=qmv.QMV_F16,
+                                       mode=qmv.QMV_FAST, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(2):
             g_all.replay()
@@ -287,12 +310,26 @@ def gpu_arm(args, rank, world, local):
     ms_max = reduce_max(ms)
 
     # ---- end to end through the public API: pinned host -> device -> host ----
-    pin = {k: torch.from_numpy(v).pin_memory() for k, v in hin.items()}
-    outs = {k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory()
-            for k in ("y_qkv", "y_o", "y_gu", "y_down", "h2")}
+    pin = {k: torch.from_numpy(hin[k]).pin_memory() for k in ("x", "r", "g1", "g2")}
+    outs = {k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory() for k in ("x", "r")}
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = sum(v.numel() * v.element_size() for v in outs.values())
     KE = max(3, K // 2)
+
+    def e2e_step(li):
+        for k, v in pin.items():
+            b[k].copy_(v, non_blocking=True)
+        run_layer(qmv, layers[li], b, stream)
+        for k, v in outs.items():
+            v.copy_(b[k], non_blocking=True)
+
+    # one graph per layer: the copies are memcpy nodes, run again on every replay
+    g_e2e = []
+    for li in range(L):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_step(li)
+        g_e2e.append(g)
     torch.cuda.synchronize()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -300,15 +337,30 @@ def gpu_arm(args, rank, world, local):
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(KE):
-            for k, v in pin.items():
-                b[k].copy_(v, non_blocking=True)
-            run_layer(qmv, layers[i % L], b, stream)
-            for k, v in outs.items():
-                v.copy_(b[k], non_blocking=True)
+            g_e2e[i % L].replay()
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(e0.elapsed_time(e1))
     barrier()
+
+    # ---- the same layers as one persistent chain launch (L layers) ----
+    ch = chain_layers(qmv, layers, b, L)
+    reps = max(1, K // L)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            ch.run(stream)
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        c0.record(stream)
+        for _ in range(reps):
+            ch.run(stream)
+        c1.record(stream)
+    torch.cuda.synchronize()
+    chain_ms = reduce_max(c0.elapsed_time(c1)) / (reps * L)
+    chain_info = ch.info()
+    ch.close()
 
     peak, peak_kind = peaks()
     gbs = world * LAYER_BYTES * K / (ms_max * 1e-3) / 1e9
@@ -345,6 +397,11 @@ def gpu_arm(args, rank, world, local):
         "e2e": {"value": round(world * LAYER_BYTES * KE / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": ck,
+        "chain": {"value": round(world * LAYER_BYTES / (chain_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                  "ms_per_step": round(chain_ms, 5), "layers_per_launch": L,
+                  "grid_barriers": chain_info["barriers"],
+                  "note": "same dependent layers as one persistent cooperative launch (qmv_chain_run); "
+                          "the headline value uses CUDA graphs with programmatic dependent launch"},
     }
     return out
 
@@ -365,6 +422,9 @@ def oracle_sample(frac_rows: int):
 
 
 def oracle_layer(oracle, hin, mats):
+    """The layer's four matvecs on the CPU oracle, for timing: a row sample
+    cannot carry the layer's dependencies, so o_proj and down read static
+    stand-in inputs of their widths."""
     x, r, g1, g2, attn, act = (hin[k] for k in ("x", "r", "g1", "g2", "attn", "act"))
     c, s, g, _, _ = mats["qkv"]
     h, _, _ = oracle.fused_rmsnorm_gemv(c, s, g, x, r, g1)
