@@ -72,6 +72,13 @@ struct ChainOp {
 };
 static_assert(alignof(ChainOp) >= 64 && sizeof(ChainOp) % 64 == 0, "tensor maps stay 64-byte aligned");
 
+// The library's own chain scratch (barrier words + op table), for chains made
+// by qmv_chain_create_no_alloc: a file-scope device array, so nothing is
+// allocated at run time by anyone.  One per device (a module global); chains
+// that use it must not run at the same time.
+constexpr int CH_STATIC_OPS = 1024;
+static __device__ __align__(256) unsigned char g_chain_scratch[256 + CH_STATIC_OPS * sizeof(ChainOp)];
+
 namespace {
 
 struct ChainParams {
@@ -417,6 +424,7 @@ struct qmv_chain {
   int max_K;
   int groups_so_far;
   bool dirty;
+  int static_dev;     // >= 0: the workspace is the library's scratch array on this device
 };
 
 static bool chain_ok(const qmv_chain* c) { return c && c->magic == QMV_CHAIN_MAGIC; }
@@ -442,8 +450,30 @@ int qmv_chain_create(qmv_chain** out, int max_ops, void* d_workspace, size_t wor
   c->max_K = 0;
   c->groups_so_far = 0;
   c->dirty = true;
+  c->static_dev = -1;
   *out = c;
   return QMV_OK;
+}
+
+// the chain whose op table the scratch array of each device holds
+static const qmv_chain* g_static_owner[64];
+
+int qmv_chain_create_no_alloc(qmv_chain** out, int max_ops) {
+  if (!out || max_ops < 1) return QMV_ERR_INVALID_ARG;
+  if (max_ops > qmv::CH_STATIC_OPS) return QMV_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return qmv::record_cuda_error(e);
+  if (dev < 0 || dev >= 64) return QMV_ERR_UNSUPPORTED;
+  // the scratch array's address on this device (set-up, per device)
+  static void* addr[64];
+  if (!addr[dev]) {
+    e = cudaGetSymbolAddress(&addr[dev], qmv::g_chain_scratch);
+    if (e != cudaSuccess) return qmv::record_cuda_error(e);
+  }
+  const int rc = qmv_chain_create(out, max_ops, addr[dev], sizeof(qmv::g_chain_scratch));
+  if (rc == QMV_OK) (*out)->static_dev = dev;
+  return rc;
 }
 
 static int chain_add(qmv_chain* c, const qmv_pack* p, const void* x, const void* r, const void* g,
@@ -533,11 +563,19 @@ int qmv_chain_run(qmv_chain* c, void* stream) {
   if (c->ops.empty()) return QMV_OK;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
+  if (c->static_dev >= 0) {
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    if (dev != c->static_dev) return QMV_ERR_INVALID_ARG;
+    if (g_static_owner[dev] != c) c->dirty = true;   // another chain's table is there
+  }
   if (c->dirty) {
     e = cudaMemcpy(c->d_ws + CH_WS_HEAD, c->ops.data(), c->ops.size() * sizeof(ChainOp),
                    cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return record_cuda_error(e);
     c->dirty = false;
+    if (c->static_dev >= 0) g_static_owner[c->static_dev] = c;
   }
   const ChainLayout L = chain_layout(c->max_K);
   static thread_local int set_dev = -1;
@@ -588,6 +626,7 @@ int qmv_chain_info(const qmv_chain* c, int* n_ops, int* n_barriers, int* smem_by
 
 int qmv_chain_destroy(qmv_chain* c) {
   if (!chain_ok(c)) return QMV_ERR_INVALID_ARG;
+  if (c->static_dev >= 0 && g_static_owner[c->static_dev] == c) g_static_owner[c->static_dev] = nullptr;
   c->magic = 0;
   delete c;
   return QMV_OK;

@@ -43,6 +43,7 @@ SIGNATURES = {
     "qmv_set_pdl": (_I, [_I]),
     "qmv_chain_workspace_bytes": (ctypes.c_size_t, [_I]),
     "qmv_chain_create": (_I, [ctypes.POINTER(_P), _I, _P, ctypes.c_size_t]),
+    "qmv_chain_create_no_alloc": (_I, [ctypes.POINTER(_P), _I]),
     "qmv_chain_add_gemv": (_I, [_P, _P, _P, _P, _I, _I]),
     "qmv_chain_add_fused_rmsnorm_gemv": (_I, [_P, _P, _P, _P, _P, _F, _P, _P, _I, _I]),
     "qmv_chain_run": (_I, [_P, _P]),
@@ -218,11 +219,17 @@ class Chain:
     The workspace is a torch uint8 device tensor; the tensors of every added
     op are kept referenced for the chain's lifetime."""
 
-    def __init__(self, max_ops: int, device=None):
-        n = _lib.qmv_chain_workspace_bytes(max_ops)
-        self.ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    def __init__(self, max_ops: int, device=None, no_alloc: bool = False):
+        """no_alloc: use the library's own scratch array (qmv_chain_create_no_alloc)
+        instead of a workspace tensor."""
         h = _P()
-        _check("qmv_chain_create", _lib.qmv_chain_create(ctypes.byref(h), max_ops, _dptr(self.ws), n))
+        if no_alloc:
+            self.ws = None
+            _check("qmv_chain_create_no_alloc", _lib.qmv_chain_create_no_alloc(ctypes.byref(h), max_ops))
+        else:
+            n = _lib.qmv_chain_workspace_bytes(max_ops)
+            self.ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+            _check("qmv_chain_create", _lib.qmv_chain_create(ctypes.byref(h), max_ops, _dptr(self.ws), n))
         self.handle = h
         self._keep = []
 

@@ -238,6 +238,21 @@ QMV_API int qmv_chain_create(qmv_chain **out, int max_ops, void *d_workspace,
                              size_t workspace_bytes);
 
 /*
+ * qmv_chain_create_no_alloc -- an empty chain whose barrier words and op table
+ * live in the library's own scratch array (a file-scope device array, one per
+ * device, room for 1024 ops), so neither the caller nor the library allocates
+ * device memory for it.  The paper has no counterpart: it is an interface
+ * variant of qmv_chain_create.  The array's address is looked up once per
+ * device; the chain must run on the device that was current here.  Every run
+ * clears the barrier words; a run after another chain used the array re-copies
+ * this chain's op table.  Chains made this way share the array: runs of two of
+ * them that overlap in time race (and so would a run overlapping its own
+ * earlier run on another stream).
+ * Errors: INVALID_ARG (NULL, max_ops < 1), UNSUPPORTED (max_ops > 1024), CUDA.
+ */
+QMV_API int qmv_chain_create_no_alloc(qmv_chain **out, int max_ops);
+
+/*
  * qmv_chain_add_gemv / qmv_chain_add_fused_rmsnorm_gemv -- append one M = 1
  * matvec with the arguments of qmv_gemv / qmv_fused_rmsnorm_gemv (pointers
  * are recorded, not read, until qmv_chain_run).  Host only.
@@ -252,7 +267,8 @@ QMV_API int qmv_chain_add_fused_rmsnorm_gemv(qmv_chain *c, const qmv_pack *p, co
 
 /*
  * qmv_chain_run -- run every op of the chain, in order, as one cooperative
- * launch of one CTA per SM on `stream`.  The first run after ops were added
+ * launch of one CTA per SM on `stream` (INVALID_ARG for a chain from
+ * qmv_chain_create_no_alloc run on another device).  The first run after ops were added
  * copies the op table to the workspace synchronously; later runs only clear
  * the barrier words (an async memset) and launch, and can be captured in a
  * CUDA graph.  Two runs of chains that share a workspace must not overlap.
