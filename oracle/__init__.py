@@ -76,6 +76,8 @@ def _load():
                                                        ctypes.c_float, P, P]
             lib.orc_gemv.argtypes = [P, P, i64, i64, i64, P, i64, P]
             lib.orc_gemv.restype = ctypes.c_int
+            lib.orc_argmax.argtypes = [P, i64, P]
+            lib.orc_argmax.restype = i64
             _lib = lib
     return _lib
 
@@ -192,6 +194,16 @@ def gemv(codes, scales, group: int, y) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"orc_gemv failed ({rc})")
     return out
+
+
+def argmax(y):
+    """(index, value) of the largest of the fp32 vector y, first max on ties;
+    (-1, nan) if there is none."""
+    y = _c(np.asarray(y, np.float32).ravel(), np.float32)
+    v = ctypes.c_float(float("nan"))
+    lib = _load()
+    idx = lib.orc_argmax(_ptr(y), y.size, ctypes.byref(v))
+    return int(idx), float(v.value)
 
 
 def fused_rmsnorm_gemv(codes, scales, group: int, x, r, gamma, eps: float = 1e-6):

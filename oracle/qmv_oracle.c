@@ -307,3 +307,21 @@ int orc_gemv(const int8_t *codes, const uint16_t *scales, int64_t N, int64_t K,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------- argmax --- */
+/* The greedy token after the lm_head matvec ("Gemma4 raw-Metal loop on A19",
+ * "The parked levers" table, argmax stage1+2 merge row: one dispatch that
+ * keeps the first-max tie-break): the index of the largest y[n], the lowest
+ * index among equal maxima.  Values compare as numbers (-0 equals +0); a NaN
+ * is never the maximum.  *max_out (nullable) receives y at that index.
+ * Returns the index, or -1 when N < 1 or every value is NaN. */
+int64_t orc_argmax(const float *y, int64_t N, float *max_out)
+{
+    int64_t best = -1;
+    for (int64_t n = 0; n < N; ++n) {
+        if (y[n] != y[n]) continue;                 /* NaN */
+        if (best < 0 || y[n] > y[best]) best = n;   /* strictly greater: first max wins */
+    }
+    if (max_out && best >= 0) *max_out = y[best];
+    return best;
+}
