@@ -208,6 +208,36 @@ int qmv_fused_rmsnorm_gemv(const qmv_pack* p, int M, const void* x, const void* 
   return run_cuda_core(a, p->bits, (cudaStream_t)stream, mode);
 }
 
+size_t qmv_argmax_workspace_bytes(void) { return 16; }
+
+int qmv_gemv_argmax(const qmv_pack* p, const void* x, const void* residual, const void* gamma,
+                    float eps, void* h_out, void* y, int y_dtype, int mode, int* d_index,
+                    float* d_value, void* d_workspace, void* stream) {
+  if (!pack_ok(p) || !p->bound || !x || !d_index || !d_workspace) return QMV_ERR_INVALID_ARG;
+  if (y && y_dtype != QMV_F32 && y_dtype != QMV_F16) return QMV_ERR_INVALID_ARG;
+  if (mode != QMV_FAST && mode != QMV_EXACT) return QMV_ERR_INVALID_ARG;
+  if (residual && (!gamma || !(eps >= 0.0f))) return QMV_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (y && !aligned(y, 4)) || !aligned(d_index, 4) || (d_value && !aligned(d_value, 4)) ||
+      !aligned(d_workspace, 8) || (residual && (!aligned(residual, 16) || !aligned(gamma, 16))) ||
+      (h_out && !aligned(h_out, 16)))
+    return QMV_ERR_ALIGNMENT;
+  qmv::GemvArgs a = base_args(p, 1, x, y, y ? y_dtype : QMV_F32);
+  if (residual) {
+    a.fused = 1;
+    a.r = (const __half*)residual;
+    a.gamma = (const __half*)gamma;
+    a.eps = eps;
+    a.h_out = (__half*)h_out;
+  }
+  a.folded = (mode == QMV_FAST && qmv::tma_fits(a.K, p->bits, a.perrow != 0)) ? 1 : 0;
+  a.amax_ws = (unsigned long long*)d_workspace;
+  a.amax_index = d_index;
+  a.amax_value = d_value;
+  cudaError_t err = cudaSuccess;
+  const int rc = qmv::launch_gemv_tma(a, p->bits, (cudaStream_t)stream, &err);
+  return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
+}
+
 int qmv_unpack_codes(const qmv_pack* p, int8_t* d_codes_out, void* stream) {
   if (!pack_ok(p) || !p->bound || !d_codes_out) return QMV_ERR_INVALID_ARG;
   if (!aligned(d_codes_out, 16)) return QMV_ERR_ALIGNMENT;

@@ -38,6 +38,12 @@ struct GemvArgs {
   int M;                      // columns (tokens)
   int fused;
   int folded;                 // fast mode's folded-offset form (see qmv_decode.cuh)
+  // fused argmax epilogue (M = 1 pipeline only; null when off): workspace
+  // {u64 key, u32 CTA count} (zero before a launch, left zero after it) and
+  // the outputs
+  unsigned long long* amax_ws;
+  int* amax_index;
+  float* amax_value;
 };
 
 struct DevInfo {

@@ -484,10 +484,54 @@ __device__ __forceinline__ void compute_stage(const unsigned char* st, const Tma
   }
 }
 
+// Argmax key of output row n with value v: the value's bits made
+// order-preserving as an unsigned number (after -0 -> +0) in the high word,
+// ~n in the low word, so the largest key is the largest value and, among
+// equal values, the lowest row (first-max tie-break).  NaN gets 0 (never
+// wins; every other value's key is nonzero).
+__device__ __forceinline__ unsigned long long amax_key(float v, int64_t n) {
+  if (v != v) return 0ull;
+  const uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)n);
+}
+
+// The fold warp's argmax epilogue, after its last stage: the warp's best key
+// goes into the workspace key with one atomic max; the CTA that arrives last
+// on the workspace counter writes the index and value and clears both words.
+__device__ __forceinline__ void amax_finish(const GemvArgs& a, unsigned long long best, int lane) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+    best = o > best ? o : best;
+  }
+  if (lane != 0) return;
+  unsigned long long* key = a.amax_ws;
+  unsigned int* count = reinterpret_cast<unsigned int*>(a.amax_ws + 1);
+  if (best) atomicMax(key, best);
+  __threadfence();
+  if (atomicAdd(count, 1u) == gridDim.x - 1) {
+    __threadfence();
+    const unsigned long long k = atomicExch(key, 0ull);
+    atomicExch(count, 0u);
+    int idx = -1;
+    float val = __uint_as_float(0x7FC00000u);
+    if (k) {
+      idx = (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+      const uint32_t ord = (uint32_t)(k >> 32);
+      val = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+    }
+    *a.amax_index = idx;
+    if (a.amax_value) *a.amax_value = val;
+  }
+}
+
 // The fold warp's share of one stage: lane = row of the group; acc carries
-// the row's accumulator across the segments; the last segment stores y.
+// the row's accumulator across the segments; the last segment stores y (when
+// a.y is set) and, with the argmax epilogue, updates the lane's best key.
 __device__ __forceinline__ void fold_stage(const GemvArgs& a, const TmaPlan& P, const float* tbr, int GS,
-                                           int lane, int64_t r0, int rows, int seg, float& acc) {
+                                           int lane, int64_t r0, int rows, int seg, float& acc,
+                                           unsigned long long* best = nullptr) {
   const int NBS = P.KS / 32;
   if (lane < rows) {
     const float* tr = tbr + (size_t)lane * GS;
@@ -507,10 +551,16 @@ __device__ __forceinline__ void fold_stage(const GemvArgs& a, const TmaPlan& P, 
     if (seg == P.NSEG - 1) {
       float out = acc;
       if (a.perrow) out = __fadd_rn(0.0f, __fmul_rn(acc, __half2float(a.scales[r0 + lane])));
-      if (a.y_f16)
-        reinterpret_cast<__half*>(a.y)[r0 + lane] = __float2half_rn(out);
-      else
-        reinterpret_cast<float*>(a.y)[r0 + lane] = out;
+      if (a.y) {
+        if (a.y_f16)
+          reinterpret_cast<__half*>(a.y)[r0 + lane] = __float2half_rn(out);
+        else
+          reinterpret_cast<float*>(a.y)[r0 + lane] = out;
+      }
+      if (best) {
+        const unsigned long long k = amax_key(out, r0 + lane);
+        if (k > *best) *best = k;
+      }
     }
   }
 }

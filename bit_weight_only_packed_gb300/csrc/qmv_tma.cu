@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   // ---------------------------------------------------------- fold warp --
   if (warp == 1) {
     float acc = 0.0f;   // this lane's row: group-32 accumulator, or the per-row block sum
+    unsigned long long best = 0ull;   // argmax epilogue: this lane's best key
     int seg = 0;
     int64_t g = blockIdx.x;
     for (int i = 0; i < my_stages; ++i) {
@@ -140,7 +141,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
       if (!mbar_wait_fast(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL, err)) break;
       const int64_t r0 = g * R;
       const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
-      fold_stage(a, P, tbuf + (size_t)tb * R * GS, GS, lane, r0, rows, seg, acc);
+      fold_stage(a, P, tbuf + (size_t)tb * R * GS, GS, lane, r0, rows, seg, acc,
+                 a.amax_ws ? &best : nullptr);
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[tb]);
       if (++seg == P.NSEG) {
@@ -148,6 +150,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
         g += gridDim.x;
       }
     }
+    if (a.amax_ws) amax_finish(a, best, lane);
     return;
   }
 

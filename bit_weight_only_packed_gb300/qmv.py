@@ -41,6 +41,8 @@ SIGNATURES = {
     "qmv_last_cuda_error": (_I, []),
     "qmv_device_error": (_I, [ctypes.POINTER(_I), _I]),
     "qmv_set_pdl": (_I, [_I]),
+    "qmv_argmax_workspace_bytes": (ctypes.c_size_t, []),
+    "qmv_gemv_argmax": (_I, [_P, _P, _P, _P, _F, _P, _P, _I, _I, _P, _P, _P, _P]),
     "qmv_chain_workspace_bytes": (ctypes.c_size_t, [_I]),
     "qmv_chain_create": (_I, [ctypes.POINTER(_P), _I, _P, ctypes.c_size_t]),
     "qmv_chain_create_no_alloc": (_I, [ctypes.POINTER(_P), _I]),
@@ -180,6 +182,25 @@ def qmv_fused_rmsnorm_gemv(p: Pack, x, residual, gamma, eps=1e-6, h_out=None, y=
         p.handle, M, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out), _dptr(y),
         y_dtype, mode, _stream(stream)))
     return y
+
+
+def qmv_argmax_workspace(device=None):
+    """A zeroed workspace for qmv_gemv_argmax (left zero by every completed call)."""
+    return torch.zeros(_lib.qmv_argmax_workspace_bytes(), dtype=torch.uint8, device=device or "cuda")
+
+
+def qmv_gemv_argmax(p: Pack, x, workspace, residual=None, gamma=None, eps=1e-6, h_out=None, y=None,
+                    y_dtype=QMV_F32, mode=QMV_FAST, stream=None, index=None, value=None):
+    """(index, value) device tensors of the greedy token; y (logits) is stored
+    only if given."""
+    if index is None:
+        index = torch.empty(1, dtype=torch.int32, device=x.device)
+    if value is None:
+        value = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check("qmv_gemv_argmax", _lib.qmv_gemv_argmax(
+        p.handle, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out), _dptr(y), y_dtype,
+        mode, _dptr(index), _dptr(value), _dptr(workspace), _stream(stream)))
+    return index, value
 
 
 def qmv_unpack_codes(p: Pack, out=None, stream=None):

@@ -165,6 +165,31 @@ QMV_API int qmv_chunk_gemm(const qmv_pack *p, int M, const void *x, void *y, int
                    int mode, void *stream);
 
 /*
+ * qmv_gemv_argmax -- the lm_head matvec with the greedy-token step fused into
+ * its epilogue ([A19] "The parked levers" table, argmax stage1+2 merge row:
+ * one dispatch, first-max tie-break): y = matvec(x) for M = 1 as qmv_gemv
+ * (or, with residual != NULL, as qmv_fused_rmsnorm_gemv with gamma, eps and
+ * h_out), then the index of the largest fp32 result -- the lowest index among
+ * equal maxima; values compare as numbers (-0 equals +0); NaN never wins.
+ *   y            nullable: device [N] of y_dtype receives the logits; NULL
+ *                skips the store.
+ *   d_index      device int32: receives the index (-1 if every value is NaN).
+ *   d_value      nullable device fp32: receives the maximum (its value;
+ *                a maximum of -0 reads +0).
+ *   d_workspace  device, qmv_argmax_workspace_bytes() bytes, 8-byte aligned,
+ *                all zero before the first call; every completed call leaves
+ *                it zero.  Calls sharing a workspace must not overlap.
+ * The index is exact against the oracle in QMV_EXACT mode.  Needs
+ * K % 256 == 0 (the M = 1 pipeline); QMV_ERR_UNSUPPORTED otherwise.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA.
+ */
+QMV_API size_t qmv_argmax_workspace_bytes(void);
+QMV_API int qmv_gemv_argmax(const qmv_pack *p, const void *x, const void *residual,
+                            const void *gamma, float eps, void *h_out, void *y, int y_dtype,
+                            int mode, int *d_index, float *d_value, void *d_workspace,
+                            void *stream);
+
+/*
  * qmv_unpack_codes -- decode the packed words back to signed int8 codes
  * [N][K] with the same decode routine the matvec kernels use (a check of
  * that routine; not on the hot path).  d_codes_out: device int8, N*K bytes.
