@@ -3,7 +3,7 @@
 // computes on the host: every step of the matvec runs in the kernels.
 #include <new>
 
-#include "qmv_internal.cuh"
+#include "qmv_pipe.cuh"
 
 namespace {
 
@@ -233,6 +233,25 @@ int qmv_gemv_argmax(const qmv_pack* p, const void* x, const void* residual, cons
   a.amax_ws = (unsigned long long*)d_workspace;
   a.amax_index = d_index;
   a.amax_value = d_value;
+  cudaError_t err = cudaSuccess;
+  const int rc = qmv::launch_gemv_tma(a, p->bits, (cudaStream_t)stream, &err);
+  return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
+}
+
+int qmv_gemv_gather(const qmv_pack* p, int rows_per_expert, const int* d_expert_ids, int n_selected,
+                    const void* x, void* y, int y_dtype, int mode, void* stream) {
+  if (!pack_ok(p) || !p->bound || !x || !y || !d_expert_ids) return QMV_ERR_INVALID_ARG;
+  if (y_dtype != QMV_F32 && y_dtype != QMV_F16) return QMV_ERR_INVALID_ARG;
+  if (mode != QMV_FAST && mode != QMV_EXACT) return QMV_ERR_INVALID_ARG;
+  if (rows_per_expert < 1 || p->N % rows_per_expert != 0) return QMV_ERR_SHAPE;
+  if (n_selected < 1 || n_selected > qmv::pipe::GATHER_MAX) return QMV_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 4) || !aligned(d_expert_ids, 4)) return QMV_ERR_ALIGNMENT;
+  qmv::GemvArgs a = base_args(p, 1, x, y, y_dtype);
+  a.folded = (mode == QMV_FAST && qmv::tma_fits(a.K, p->bits, a.perrow != 0)) ? 1 : 0;
+  a.gather_ids = d_expert_ids;
+  a.gather_rows = rows_per_expert;
+  a.gather_n = n_selected;
+  a.gather_E = p->N / rows_per_expert;
   cudaError_t err = cudaSuccess;
   const int rc = qmv::launch_gemv_tma(a, p->bits, (cudaStream_t)stream, &err);
   return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;

@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1) gemv_chain_kernel(ChainParams c
         for (int seg = 0; seg < P.NSEG; ++seg, ++i) {
           const int tb = i & 1;
           if (!dead && !mbar_wait_fast(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL, err)) dead = true;
-          if (!dead) fold_stage(a, P, tbuf + (size_t)tb * CH_TBUF, CH_GS, lane, r0, rows, seg, acc);
+          if (!dead) fold_stage(a, P, tbuf + (size_t)tb * CH_TBUF, CH_GS, lane, GroupRows{r0, r0, rows, true},
+                                seg, acc);
           __syncwarp();
           if (lane == 0 && !dead) mbar_arrive(&tempty[tb]);
         }

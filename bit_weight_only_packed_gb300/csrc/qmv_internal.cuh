@@ -44,6 +44,11 @@ struct GemvArgs {
   unsigned long long* amax_ws;
   int* amax_index;
   float* amax_value;
+  // expert gather (M = 1 pipeline only; gather_rows == 0 when off): the pack
+  // holds gather_E experts of gather_rows rows each; output block j (rows
+  // j*gather_rows ..) is expert gather_ids[j], j < gather_n
+  const int* gather_ids;
+  int gather_rows, gather_n, gather_E;
 };
 
 struct DevInfo {

@@ -19,7 +19,7 @@ namespace pipe {
 constexpr int NS = 4;                      // ring stages (a power of two)
 constexpr uint32_t SPIN_LIMIT = 1u << 22;  // tries per bounded wait (a backstop to the time limit)
 constexpr int ERR_TIMEOUT_FULL = 1, ERR_TIMEOUT_EMPTY = 2, ERR_TIMEOUT_TFULL = 3,
-              ERR_TIMEOUT_TEMPTY = 4, ERR_SMEM_ALIGN = 5;
+              ERR_TIMEOUT_TEMPTY = 4, ERR_SMEM_ALIGN = 5, ERR_BAD_EXPERT = 8;
 
 
 __device__ __forceinline__ uint32_t sa(const void* p) {
@@ -254,7 +254,41 @@ struct TmaPlan {
   int stage_bytes;   // whole stage, a multiple of 128 bytes
   int ngroups;       // ceil(N / R)
   int y_off, ysum_off, stage_off, tbuf_off;   // shared-memory offsets (bytes)
+  int ids_off;       // expert gather: the selected experts' ids (shared memory)
 };
+
+constexpr int GATHER_MAX = 256;   // selected experts per expert-gather call at most
+
+// Where row group g of a matvec sits: the first output row (log0), the first
+// row of the pack it reads (phys0), the rows it really has, and whether its
+// expert id is valid.  Without expert gather the two are the same.  With it,
+// each selected expert's rows form ceil(rows/R) groups; an invalid id reads
+// past the end of the pack (the copies zero-fill) and its outputs are zeroed.
+struct GroupRows {
+  int64_t log0, phys0;
+  int rows;
+  bool ok;
+};
+
+__host__ __device__ __forceinline__ GroupRows group_rows(const GemvArgs& a, int R, int64_t g,
+                                                         const int* ids) {
+  GroupRows gr;
+  if (!a.gather_rows) {
+    gr.log0 = gr.phys0 = g * R;
+    gr.rows = (int)((int64_t)a.N - g * R < R ? (int64_t)a.N - g * R : R);
+    gr.ok = true;
+    return gr;
+  }
+  const int gpe = (a.gather_rows + R - 1) / R;
+  const int64_t j = g / gpe;
+  const int lr0 = (int)(g % gpe) * R;
+  const int e = ids[j];
+  gr.ok = e >= 0 && e < a.gather_E;
+  gr.log0 = j * a.gather_rows + lr0;
+  gr.rows = (a.gather_rows - lr0 < R) ? a.gather_rows - lr0 : R;
+  gr.phys0 = gr.ok ? (int64_t)e * a.gather_rows + lr0 : (int64_t)a.N;
+  return gr;
+}
 
 __host__ __device__ inline int tma_round16(int x) { return (x + 15) & ~15; }
 
@@ -530,10 +564,11 @@ __device__ __forceinline__ void amax_finish(const GemvArgs& a, unsigned long lon
 // the row's accumulator across the segments; the last segment stores y (when
 // a.y is set) and, with the argmax epilogue, updates the lane's best key.
 __device__ __forceinline__ void fold_stage(const GemvArgs& a, const TmaPlan& P, const float* tbr, int GS,
-                                           int lane, int64_t r0, int rows, int seg, float& acc,
+                                           int lane, const GroupRows& gr, int seg, float& acc,
                                            unsigned long long* best = nullptr) {
   const int NBS = P.KS / 32;
-  if (lane < rows) {
+  const int64_t r0 = gr.log0;
+  if (lane < gr.rows) {
     const float* tr = tbr + (size_t)lane * GS;
     if (!a.perrow) {
       if (seg == 0) acc = 0.0f;
@@ -550,7 +585,8 @@ __device__ __forceinline__ void fold_stage(const GemvArgs& a, const TmaPlan& P, 
     }
     if (seg == P.NSEG - 1) {
       float out = acc;
-      if (a.perrow) out = __fadd_rn(0.0f, __fmul_rn(acc, __half2float(a.scales[r0 + lane])));
+      if (a.perrow && gr.ok) out = __fadd_rn(0.0f, __fmul_rn(acc, __half2float(a.scales[gr.phys0 + lane])));
+      if (!gr.ok) out = 0.0f;
       if (a.y) {
         if (a.y_f16)
           reinterpret_cast<__half*>(a.y)[r0 + lane] = __float2half_rn(out);

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   float* ysum = reinterpret_cast<float*>(sm + P.ysum_off); // folded form: 2^(b-1) * S per block
   unsigned char* stages = sm + P.stage_off;
   float* tbuf = reinterpret_cast<float*>(sm + P.tbuf_off);
+  int* ids_sh = reinterpret_cast<int*>(sm + P.ids_off);   // expert gather: selected ids
   int* err = &g_qmv_error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,6 +90,14 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
 
   // ------------------------------------------------------------ producer --
   if (warp == 0) {
+    if (a.gather_rows) {
+      // the expert ids may come from the previous kernel: wait for it, then
+      // keep them in shared memory (the fold warp reads them there, after
+      // the stage barriers that follow these stores)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      for (int t = lane; t < a.gather_n; t += 32) ids_sh[t] = a.gather_ids[t];
+      __syncwarp();
+    }
     int issued = 0;
     int seg = 0;
     int64_t g = blockIdx.x;
@@ -96,7 +105,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
       const int s = i & (NS - 1);
       if (i >= NS && !mbar_wait_fast(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY, err)) break;
       if (*abort_f) break;
-      const int64_t r0 = g * R;
+      const int64_t r0 = group_rows(a, R, g, ids_sh).phys0;
       // one box of R rows x one segment: rows past N are zero-filled, the
       // transaction count is always the whole box
       unsigned char* st = stages + (size_t)s * P.stage_bytes;
@@ -139,10 +148,9 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     for (int i = 0; i < my_stages; ++i) {
       const int tb = i & 1;
       if (!mbar_wait_fast(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL, err)) break;
-      const int64_t r0 = g * R;
-      const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
-      fold_stage(a, P, tbuf + (size_t)tb * R * GS, GS, lane, r0, rows, seg, acc,
-                 a.amax_ws ? &best : nullptr);
+      const GroupRows gr = group_rows(a, R, g, ids_sh);
+      if (!gr.ok && lane == 0 && seg == 0) atomicCAS(err, 0, ERR_BAD_EXPERT);
+      fold_stage(a, P, tbuf + (size_t)tb * R * GS, GS, lane, gr, seg, acc, a.amax_ws ? &best : nullptr);
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[tb]);
       if (++seg == P.NSEG) {
@@ -168,8 +176,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     const int tb = i & 1;
     if (!mbar_wait_fast(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL, err)) break;
     if (i >= 2 && !mbar_wait_fast(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY, err)) break;
-    const int64_t r0 = g * R;
-    const int rows = (int)min((int64_t)R, (int64_t)a.N - r0);
+    const int rows = a.gather_rows ? group_rows(a, R, g, ids_sh).rows
+                                   : (int)min((int64_t)R, (int64_t)a.N - g * R);
     if (active)
       compute_stage<BITS, PERROW, EXACT, U>(stages + (size_t)s * P.stage_bytes, P, c, rp, seg, rows, y2s,
                                             ysum, tbuf + (size_t)tb * R * GS, GS);
@@ -216,6 +224,11 @@ static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int U, 
   P->ysum_off = P->y_off + (K / 64) * YS * 8;
   P->stage_off = (P->ysum_off + (K / 32) * 4 + 127) & ~127;
   P->tbuf_off = tma_round16(P->stage_off + NS * P->stage_bytes);
+  {
+    const int fold = 2 * P->R * (P->KS / 32 + 1) * 4;
+    const int bsum = (K / 32) * 4;
+    P->ids_off = P->tbuf_off + tma_round16(fold > bsum ? fold : bsum);
+  }
   return true;
 }
 
@@ -300,12 +313,11 @@ static bool tensor_maps(const GemvArgs& a, int bits, const TmaPlan& P, CUtensorM
   return true;
 }
 
-// The fold buffer (2 x R rows x (KS/32 + 1) floats) also holds the fused
-// prologue's K/32 block sums before the main loop starts.
-static size_t tma_smem(const TmaPlan& P, int K) {
-  const int fold = 2 * P.R * (P.KS / 32 + 1) * 4;
-  const int bsum = (K / 32) * 4;
-  return (size_t)P.tbuf_off + (size_t)tma_round16(fold > bsum ? fold : bsum);
+// Shared memory of a plan: up to the fold buffer (2 x R rows x (KS/32 + 1)
+// floats, which also holds the fused prologue's K/32 block sums before the
+// main loop), then room for GATHER_MAX expert ids.
+static size_t tma_smem(const TmaPlan& P, int /*K*/) {
+  return (size_t)P.ids_off + (size_t)GATHER_MAX * 4;
 }
 
 template <int BITS, bool PERROW, bool FUSED, bool EXACT, int U, int MAXT>
@@ -408,18 +420,24 @@ static int tma_dispatch(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cud
 // choice is cached per shape.
 template <int BITS>
 static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
-  struct Key { int N, K, perrow, fused, folded, dev; };
+  struct Key { int N, K, perrow, fused, folded, gather, dev; };
   struct Entry { Key k; TmaPlan p; bool ok; };
   static thread_local Entry cache[16];
   static thread_local int next = 0;
   int dev = 0;
   cudaGetDevice(&dev);
-  const Key key{a.N, a.K, a.perrow, a.fused, a.folded, dev};
+  // rows the launch covers: the pack's, or the selected experts' (gather)
+  const int Nl = a.gather_rows ? a.gather_n * a.gather_rows : a.N;
+  auto gather_groups = [&](TmaPlan P) {
+    if (a.gather_rows) P.ngroups = a.gather_n * ((a.gather_rows + P.R - 1) / P.R);
+    return P;
+  };
+  const Key key{Nl, a.K, a.perrow, a.fused, a.folded, a.gather_rows, dev};
   for (int i = 0; i < 16; ++i) {
     const Key& k = cache[i].k;
     if (cache[i].ok && k.N == key.N && k.K == key.K && k.perrow == key.perrow &&
-        k.fused == key.fused && k.folded == key.folded && k.dev == key.dev)
-      return tma_dispatch<BITS>(a, cache[i].p, s, err, nullptr);
+        k.fused == key.fused && k.folded == key.folded && k.gather == key.gather && k.dev == key.dev)
+      return tma_dispatch<BITS>(a, gather_groups(cache[i].p), s, err, nullptr);
   }
   static const int tc_force = [] {
     const char* e = getenv("QMV_TC");
@@ -435,7 +453,7 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
       if (BITS == 8 && U > 2) continue;
       if (tc > 256 && U > 2) continue;
       TmaPlan P;
-      if (!tma_plan(a.N, a.K, BITS, a.perrow != 0, tc, U, &P)) continue;
+      if (!tma_plan(Nl, a.K, BITS, a.perrow != 0, tc, U, &P)) continue;
       if (tma_smem(P, a.K) > (size_t)dev_info().max_smem_optin) continue;
       int occ = 0;
       if (tma_dispatch<BITS>(a, P, s, err, &occ) != QMV_OK || occ < 1) continue;
@@ -450,7 +468,7 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   if (best_score < 0) return QMV_ERR_UNSUPPORTED;
   cache[next] = Entry{key, best, true};
   next = (next + 1) % 16;
-  return tma_dispatch<BITS>(a, best, s, err, nullptr);
+  return tma_dispatch<BITS>(a, gather_groups(best), s, err, nullptr);
 }
 
 // Whether some plan of the pipeline fits this K (shared memory), i.e. whether

@@ -41,6 +41,7 @@ SIGNATURES = {
     "qmv_last_cuda_error": (_I, []),
     "qmv_device_error": (_I, [ctypes.POINTER(_I), _I]),
     "qmv_set_pdl": (_I, [_I]),
+    "qmv_gemv_gather": (_I, [_P, _I, _P, _I, _P, _P, _I, _I, _P]),
     "qmv_argmax_workspace_bytes": (ctypes.c_size_t, []),
     "qmv_gemv_argmax": (_I, [_P, _P, _P, _P, _F, _P, _P, _I, _I, _P, _P, _P, _P]),
     "qmv_chain_workspace_bytes": (ctypes.c_size_t, [_I]),
@@ -181,6 +182,16 @@ def qmv_fused_rmsnorm_gemv(p: Pack, x, residual, gamma, eps=1e-6, h_out=None, y=
     _check("qmv_fused_rmsnorm_gemv", _lib.qmv_fused_rmsnorm_gemv(
         p.handle, M, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out), _dptr(y),
         y_dtype, mode, _stream(stream)))
+    return y
+
+
+def qmv_gemv_gather(p: Pack, rows_per_expert: int, expert_ids, x, y=None, y_dtype=QMV_F32,
+                    mode=QMV_FAST, stream=None):
+    """y [1, n_selected * rows_per_expert]: the selected experts' rows times x."""
+    n = expert_ids.numel()
+    y = _out(y, 1, n * rows_per_expert, y_dtype, x)
+    _check("qmv_gemv_gather", _lib.qmv_gemv_gather(p.handle, rows_per_expert, _dptr(expert_ids), n,
+                                                   _dptr(x), _dptr(y), y_dtype, mode, _stream(stream)))
     return y
 
 

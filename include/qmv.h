@@ -190,6 +190,28 @@ QMV_API int qmv_gemv_argmax(const qmv_pack *p, const void *x, const void *residu
                             void *stream);
 
 /*
+ * qmv_gemv_gather -- the expert-gather matvec of a mixture-of-experts decode
+ * step, with no gathered copy of the weights ([PLAY] ranked-targets table,
+ * MoE row: a zero-materialization expert-gather matvec): the pack holds E = N / rows_per_expert experts
+ * of rows_per_expert rows each, stacked; for the n_selected expert ids in
+ * d_expert_ids, y[j*rows_per_expert + r] = (row r of expert ids[j]) . x, for
+ * M = 1, computed exactly as qmv_gemv computes those rows (the row groups of
+ * the selected experts are fetched by index inside the kernel).
+ *   rows_per_expert  divides N.
+ *   d_expert_ids     device int32 [n_selected], 1 <= n_selected <= 256; may be
+ *                    written by the kernel launched just before (it is read
+ *                    after that kernel completes).  An id outside [0, E)
+ *                    yields zero outputs for its rows and sets the device
+ *                    error word (8).
+ *   x  device fp16 [K];  y  device [n_selected * rows_per_expert] of y_dtype.
+ * Needs K % 256 == 0 (the M = 1 pipeline).
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, CUDA.
+ */
+QMV_API int qmv_gemv_gather(const qmv_pack *p, int rows_per_expert, const int *d_expert_ids,
+                            int n_selected, const void *x, void *y, int y_dtype, int mode,
+                            void *stream);
+
+/*
  * qmv_unpack_codes -- decode the packed words back to signed int8 codes
  * [N][K] with the same decode routine the matvec kernels use (a check of
  * that routine; not on the hot path).  d_codes_out: device int8, N*K bytes.
