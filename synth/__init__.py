@@ -105,6 +105,17 @@ def codes(seed: int, name: str, N: int, K: int, bits: int, rows=None,
     return out
 
 
+def ternary_codes(seed: int, name: str, N: int, K: int, rows=None,
+                  device="cpu") -> torch.Tensor:
+    """Ternary codes [len(rows) or N, K] (int8), uniform over {-1, 0, 1}
+    (the top 31 bits of each draw, modulo 3, minus 1)."""
+    key = stream_key(seed, name + ".tcodes")
+    r = _row_index(rows, N, device)
+    kk = torch.arange(K, dtype=torch.int64, device=device)
+    u = _lsr(draws(key, r[:, None] * K + kk[None, :]), 33)
+    return (torch.remainder(u, 3) - 1).to(torch.int8)
+
+
 def scales(seed: int, name: str, N: int, G: int, rows=None, device="cpu",
            lo: float = 0.005, hi: float = 0.02) -> torch.Tensor:
     """fp16 scales [len(rows) or N, G], uniform in [lo, hi]."""

@@ -25,16 +25,22 @@ class Mat:
     any rows (regenerated from the same seeded streams, never read back from
     the GPU)."""
 
-    def __init__(self, name, N, K, bits, group, seed=SEED, device_gen=None):
+    def __init__(self, name, N, K, bits, group, seed=SEED, device_gen=None, ternary=False):
         self.name, self.N, self.K, self.bits, self.group, self.seed = name, N, K, bits, group, seed
         self.G = K // group
+        self.ternary = ternary
         big = N * K > (1 << 26) if device_gen is None else device_gen
         gdev = dev() if big else "cpu"
-        codes = synth.codes(seed, name, N, K, bits, device=gdev)
+        codes = self._codes(device=gdev)
         scales = synth.scales(seed, name, N, self.G, device=gdev)
         self.pack = qmv().Pack(N, K, bits, group).pack_weights(codes.to(dev()), scales.to(dev()))
         self._host = None if big else (codes.numpy(), scales.numpy())
         del codes, scales
+
+    def _codes(self, rows=None, device="cpu"):
+        if self.ternary:
+            return synth.ternary_codes(self.seed, self.name, self.N, self.K, rows=rows, device=device)
+        return synth.codes(self.seed, self.name, self.N, self.K, self.bits, rows=rows, device=device)
 
     def host(self, rows=None):
         if rows is None:
@@ -44,7 +50,7 @@ class Mat:
         if self._host is not None:
             c, s = self._host
             return c[rows], s[rows]
-        c = synth.codes(self.seed, self.name, self.N, self.K, self.bits, rows=rows).numpy()
+        c = self._codes(rows=rows).numpy()
         s = synth.scales(self.seed, self.name, self.N, self.G, rows=rows).numpy()
         return c, s
 
