@@ -42,7 +42,6 @@ namespace {
 constexpr uint32_t TC_SPIN = 1u << 22;
 constexpr int ERR_TC_TIMEOUT = 16;
 constexpr int RS = 4;          // K slabs per raw stage (256 codes)
-constexpr int NRAW = 2;        // raw stages
 constexpr int NDEC = 8;        // decode (and epilogue) warps
 constexpr int W_RAW = NDEC, W_MMA = NDEC + 1, W_B = NDEC + 2;   // role warps
 constexpr int TC_THREADS = 32 * (NDEC + 3);
@@ -129,7 +128,7 @@ struct TcArgs {
   int split;               // gridDim.y
 };
 
-template <int MT, int NST>
+template <int MT, int NST, int NRAW>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(TcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_x) {
@@ -390,12 +389,12 @@ static bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int NST>
+template <int MT, int NST, int NRAW>
 static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s, cudaError_t* err) {
   constexpr int STAGE = 128 * 128 + MT * 128;
   const size_t smem = 1024 + (size_t)NST * STAGE + (size_t)NRAW * RAW_BYTES + 256;
   static thread_local int set_dev = -1;
-  auto kern = tc_gemm_kernel<MT, NST>;
+  auto kern = tc_gemm_kernel<MT, NST, NRAW>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
@@ -424,9 +423,20 @@ static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s
   TcArgs a = a0;
   const int nslab = a.K / 64;
   const int sms = dev_info().sms;
+  // split K across CTAs (fp32 output only: the splits add into y) to balance
+  // the waves: the time is about ceil(tiles * split / SMs) CTA-slots of
+  // 1/split of the work each; the smallest such time wins (at least 8 slabs
+  // per split), the smaller split on a tie
   int split = 1;
   if (a.y16 == nullptr) {
-    while (tiles * split * 2 <= sms && nslab / (split * 2) >= 8) split *= 2;
+    double best = 1e30;
+    for (int sp = 1; sp <= 8 && nslab / sp >= 8; ++sp) {
+      const double t = (double)((tiles * sp + sms - 1) / sms) / sp;
+      if (t < best - 1e-9) {
+        best = t;
+        split = sp;
+      }
+    }
   }
   a.split = split;
   // whole raw stages per split, so every box starts on a 16-byte boundary
@@ -460,8 +470,10 @@ int launch_tc_gemm(const GemvArgs& g, int bits, cudaStream_t s, cudaError_t* err
   a.split = 1;
   a.slabs_per_split = g.K / 64;
   const int tiles = (g.N + 127) / 128;
-  if (g.M <= 64) return run_tc<64, 8>(a, g, tiles, s, err);
-  return run_tc<128, 5>(a, g, tiles, s, err);
+  // the raw ring (codes + scales, 4 slabs a stage) keeps about an HBM
+  // latency of weight data in flight; the decoded stages fill the rest
+  if (g.M <= 64) return run_tc<64, 6, 6>(a, g, tiles, s, err);
+  return run_tc<128, 4, 6>(a, g, tiles, s, err);
 }
 
 }  // namespace qmv
