@@ -49,7 +49,7 @@ constexpr int CH_THREADS = 64 + CH_TC;     // + producer warp + fold warp
 constexpr int CH_U = 2;                    // rows per compute thread
 constexpr int CH_SLOT = 24576;             // bytes per ring stage
 constexpr int CH_RMAX = 32;                // rows per group at most
-constexpr int CH_GS = 2048 / 32 + 1;       // fold-buffer row stride (segments of <= 2048 codes)
+constexpr int CH_GS = 2048 / 32 + 4;       // fold-buffer row stride (segments of <= 2048 codes; 16-byte rows)
 constexpr int CH_TBUF = CH_RMAX * CH_GS;   // floats per fold buffer
 constexpr int CH_WS_HEAD = 256;            // workspace bytes before the op table
 constexpr int ERR_GRID_BARRIER = 6, ERR_FOLD_WAIT = 7;

@@ -394,8 +394,14 @@ __device__ __forceinline__ void build_table(const GemvArgs& a, float* y2f, float
     }
     named_bar(bar_id, nt);
     if (tt == 0) {
+      // serial over the blocks, 16-byte loads issued ahead of the adds
       float ss = 0.0f;
-      for (int b = 0; b < NB; ++b) ss = __fadd_rn(ss, bsum[b]);
+      const float4* b4 = reinterpret_cast<const float4*>(bsum);
+#pragma unroll 4
+      for (int q = 0; q < NB / 4; ++q) {
+        const float4 v = b4[q];
+        ss = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(ss, v.x), v.y), v.z), v.w);
+      }
       const float mean = __fdiv_rn(ss, (float)K);
       *inv_sh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
     }
@@ -569,19 +575,18 @@ __device__ __forceinline__ void fold_stage(const GemvArgs& a, const TmaPlan& P, 
   const int NBS = P.KS / 32;
   const int64_t r0 = gr.log0;
   if (lane < gr.rows) {
-    const float* tr = tbr + (size_t)lane * GS;
-    if (!a.perrow) {
-      if (seg == 0) acc = 0.0f;
-#pragma unroll 8
-      for (int b = 0; b < NBS; ++b) acc = __fadd_rn(acc, tr[b]);
-    } else {
-      int b0 = 0;
-      if (seg == 0) {
-        acc = tr[0];
-        b0 = 1;
-      }
-#pragma unroll 8
-      for (int b = b0; b < NBS; ++b) acc = __fadd_rn(acc, tr[b]);
+    // the row's block results, serially (16-byte loads issued ahead of the
+    // dependent adds; rows are GS floats apart, GS a multiple of 4)
+    const float4* tr = reinterpret_cast<const float4*>(tbr + (size_t)lane * GS);
+    if (seg == 0) acc = 0.0f;
+#pragma unroll 4
+    for (int q = 0; q < NBS / 4; ++q) {
+      const float4 v = tr[q];
+      // one scale per row: the row's first block starts the sum as is
+      acc = (a.perrow && seg == 0 && q == 0) ? v.x : __fadd_rn(acc, v.x);
+      acc = __fadd_rn(acc, v.y);
+      acc = __fadd_rn(acc, v.z);
+      acc = __fadd_rn(acc, v.w);
     }
     if (seg == P.NSEG - 1) {
       float out = acc;

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = P.R;
-  const int GS = P.KS / 32 + 1;          // fold-buffer row stride
+  const int GS = P.KS / 32 + 4;          // fold-buffer row stride (16-byte aligned rows)
   const int my_groups = (blockIdx.x < (unsigned)P.ngroups)
                             ? (P.ngroups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
                             : 0;
@@ -225,7 +225,7 @@ static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int U, 
   P->stage_off = (P->ysum_off + (K / 32) * 4 + 127) & ~127;
   P->tbuf_off = tma_round16(P->stage_off + NS * P->stage_bytes);
   {
-    const int fold = 2 * P->R * (P->KS / 32 + 1) * 4;
+    const int fold = 2 * P->R * (P->KS / 32 + 4) * 4;
     const int bsum = (K / 32) * 4;
     P->ids_off = P->tbuf_off + tma_round16(fold > bsum ? fold : bsum);
   }
@@ -386,8 +386,9 @@ static int tma_u(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cudaError_
                  int* occ_only) {
   const int U = P.R / P.RP;
   if (P.Tc > 256) {
-    if (U != 2) return QMV_ERR_UNSUPPORTED;
-    return run_tma<BITS, PERROW, FUSED, EXACT, 2, 576>(a, P, s, err, occ_only);
+    if (U == 2) return run_tma<BITS, PERROW, FUSED, EXACT, 2, 576>(a, P, s, err, occ_only);
+    if (U == 1) return run_tma<BITS, PERROW, FUSED, EXACT, 1, 576>(a, P, s, err, occ_only);
+    return QMV_ERR_UNSUPPORTED;
   }
   if (U == 2) return run_tma<BITS, PERROW, FUSED, EXACT, 2, 320>(a, P, s, err, occ_only);
   if constexpr (BITS != 8)
@@ -416,7 +417,10 @@ static int tma_dispatch(const GemvArgs& a, const TmaPlan& P, cudaStream_t s, cud
 // from the runtime for the exact kernel, block size and shared memory); on a
 // tie, the larger row group.  Candidates: ~256 or ~512 compute threads, and
 // 4 or 2 rows per thread (2 for int8 and for the 512-thread CTAs), with at
-// least 3 row groups per CTA slot when N allows it (load balance).  The
+// least 3 row groups per CTA slot when N allows it (load balance).  A small
+// matrix (fewer than two such groups per CTA slot) may instead take the
+// ~512-thread plan with one row per thread, when that shortens the busiest
+// slot (ceil(groups / slots) stages, each a fixed part plus R rows).  The
 // choice is cached per shape.
 template <int BITS>
 static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
@@ -447,25 +451,48 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   const int sms = dev_info().sms;
   TmaPlan best;
   int best_score = -1;
+  // small matrices (fewer than two full groups per CTA slot): the one-row-
+  // per-thread plan of ~512 compute threads halves the group (and a
+  // thread's serial work) without shrinking the CTA, whose size sets the
+  // prologue's speed; it is taken when its busiest slot has less to do
+  TmaPlan small;
+  int64_t small_cost = -1, best_slots = 1;
   for (int tc : {256, 512}) {
     if (tc_force && tc != tc_force) continue;
-    for (int U : {4, 2}) {
+    for (int U : {4, 2, 1}) {
       if (BITS == 8 && U > 2) continue;
       if (tc > 256 && U > 2) continue;
+      if (tc <= 256 && U < 2) continue;
       TmaPlan P;
       if (!tma_plan(Nl, a.K, BITS, a.perrow != 0, tc, U, &P)) continue;
       if (tma_smem(P, a.K) > (size_t)dev_info().max_smem_optin) continue;
       int occ = 0;
-      if (tma_dispatch<BITS>(a, P, s, err, &occ) != QMV_OK || occ < 1) continue;
+      if (tma_dispatch<BITS>(a, gather_groups(P), s, err, &occ) != QMV_OK || occ < 1) continue;
+      const TmaPlan Pg = gather_groups(P);
+      const int64_t slots = (int64_t)occ * sms;
+      const int64_t cost = ((Pg.ngroups + slots - 1) / slots) * (16 + P.R);
+      if (U == 1) {
+        if (small_cost < 0 || cost < small_cost) {
+          small_cost = cost;
+          small = P;
+        }
+        continue;
+      }
       int score = occ * (P.Tc / 32) * 64 + P.R;
-      if ((int64_t)P.ngroups < 3LL * occ * sms && U > 2) score -= 64 * 64;   // balance
+      if ((int64_t)Pg.ngroups < 3LL * occ * sms && U > 2) score -= 64 * 64;   // balance
       if (score > best_score) {
         best_score = score;
         best = P;
+        best_slots = slots;
       }
     }
   }
   if (best_score < 0) return QMV_ERR_UNSUPPORTED;
+  if (small_cost >= 0) {
+    const TmaPlan Bg = gather_groups(best);
+    const int64_t best_cost = ((Bg.ngroups + best_slots - 1) / best_slots) * (16 + best.R);
+    if ((int64_t)Bg.ngroups < 2 * best_slots && small_cost < best_cost) best = small;
+  }
   cache[next] = Entry{key, best, true};
   next = (next + 1) % 16;
   return tma_dispatch<BITS>(a, gather_groups(best), s, err, nullptr);
