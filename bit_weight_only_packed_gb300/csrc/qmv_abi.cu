@@ -125,9 +125,10 @@ static qmv::GemvArgs base_args(const qmv_pack* p, int M, const void* x, void* y,
 }
 
 // Dispatch: M = 1 -> the bulk-copy pipeline kernel (or the generic one);
-// M <= 32, or any M in exact mode, or int4/int8 -> CUDA-core tiles, 32
-// columns per launch (each column equal to the M = 1 result); M > 32 in fast
-// mode with int2 weights -> tcgen05 tensor-core tiles, 128 columns per
+// M > 32 in fast mode with int2 weights -> tcgen05 tensor-core tiles, 128
+// columns per launch; every other M >= 2 -> CUDA-core M-column tiles, each
+// column equal to the M = 1 result: the pipelined tiles in one launch where
+// they fit (K a multiple of 256, no fused prologue), else 32 columns per
 // launch.
 static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s, int mode) {
   cudaError_t err = cudaSuccess;
@@ -159,6 +160,8 @@ static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s, int mode) {
     if (rc == QMV_ERR_UNSUPPORTED) rc = qmv::launch_gemv_m1(a, bits, s, &err);
     return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
   }
+  rc = qmv::launch_mtile(a, bits, s, &err);
+  if (rc != QMV_ERR_UNSUPPORTED) return rc == QMV_ERR_CUDA ? cuda_fail(err) : rc;
   const int M = a.M;
   const size_t ysz = a.y_f16 ? 2 : 4;
   for (int m0 = 0; m0 < M; m0 += 32) {

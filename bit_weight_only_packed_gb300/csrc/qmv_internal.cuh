@@ -82,6 +82,10 @@ int record_cuda_error(cudaError_t e);
 // M-column tiles on paired fp32 arithmetic (K a multiple of 64, M <= 32);
 // QMV_ERR_UNSUPPORTED when the shape does not fit them.
 int launch_tile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+// M-column tiles on the bulk-copy pipeline (any M >= 2, K a multiple of 256,
+// no fused prologue), every column equal to the M = 1 result;
+// QMV_ERR_UNSUPPORTED when the shape does not fit them.
+int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
 
 
 // Per-kernel launch facts, cached per device: the dynamic shared-memory limit

@@ -1,0 +1,611 @@
+// qmv_mtile.cu -- M-column tiles on the bulk-copy pipeline (M >= 2 token
+// columns, K a multiple of 256, no fused prologue).
+//
+// What they compute ("raw-metal-loop-playbook", prefill-regimes table: keep
+// each output scalar's K-dot in the single-token accumulation order and stage
+// the weights across the M columns): every column is bit-identical to the
+// M = 1 pipeline's result for that column, in the exact form (the oracle's
+// order) and in the fast mode's folded-offset form (see qmv_decode.cuh) --
+// the same per-block chains, block finish and serial fold over the blocks.
+//
+// Layout of the work:
+//   * a tile is R = 32*U weight rows x MC = 4 token columns over the whole K;
+//     a persistent CTA (one per SM) walks its tiles, each in segments of 512
+//     codes;
+//   * the copy warp brings, per segment, the tile's packed codes (one or more
+//     128-byte-swizzled boxes of R rows x 128 bytes), its group-32 scales and
+//     the MC x 512 fp16 activations into a ring of stages;
+//   * two table warps turn the activations into the segment's table (the
+//     M = 1 pipeline's scaled fp32 pairs, the MC columns side by side) and
+//     block sums, into one of two table buffers;
+//   * compute warp w takes 64-code item w of the segment for all R rows: lane
+//     l holds rows l + 32u, decodes each code once and runs the paired-FMA
+//     chains of the MC columns (one 16-byte shared-memory broadcast serves two
+//     columns of U rows); the block results go to one of two fold buffers,
+//     and after its next segment's item each compute thread folds its
+//     (row, column) accumulators over the previous segment's blocks, in order.
+// The roles meet only on mbarriers (stage full/empty, table full/empty, fold
+// buffer full/empty), so a slow warp delays the others by its lag, not by a
+// CTA-wide barrier per segment.  Every wait is bounded; a wait that runs out
+// records an error code in this file's device error word and the CTA winds
+// down.
+#include <cuda.h>
+
+#include "qmv_pipe.cuh"
+
+namespace qmv {
+
+__device__ int g_mt_error = 0;
+
+namespace {
+
+using namespace pipe;
+
+constexpr int MT_NS = 3;                     // ring stages
+constexpr int MT_KS = 512;                   // codes per segment
+constexpr int MT_ITEMS = MT_KS / 64;         // 64-code items per segment (one per compute warp)
+constexpr int MT_BLOCKS = MT_KS / 32;        // 32-code blocks per segment
+constexpr int MT_MC = 4;                     // token columns per tile
+constexpr int MT_CW = MT_ITEMS;              // compute warps
+constexpr int MT_TW = 2;                     // table warps
+constexpr int MT_CT = 32 * MT_CW;            // compute threads
+constexpr int MT_THREADS = 32 * (MT_CW + MT_TW + 1);   // + the copy warp
+constexpr int MT_HDR = 1024;                 // barriers, flags
+constexpr int ERR_MT_TIMEOUT = 32;
+
+// Shared-memory layout of one kernel variant (offsets from a 1024-byte
+// aligned base; the copies with 128-byte swizzle need 1024-byte aligned
+// boxes).
+template <int BITS, int U>
+struct MtLayout {
+  static constexpr int MC = MT_MC;
+  static constexpr int R = 32 * U;                         // rows per tile
+  static constexpr int NBOX = BITS / 2;                    // 128-byte code boxes per row per segment
+  static constexpr int BOX = R * 128;
+  static constexpr int SC_OFF = NBOX * BOX;                // scales: [R][16] fp16
+  static constexpr int X_OFF = SC_OFF + R * 32;            // activations: [2][MC][256] fp16
+  static constexpr int STAGE = (X_OFF + MC * 1024 + 1023) / 1024 * 1024;
+  static constexpr int STAGES_OFF = MT_HDR;
+  // one table: per item 4 octets of 8 steps, a step MC fp32 pairs (the
+  // columns side by side), each octet padded by 16 bytes so that the table
+  // warps' stores of steps 8 apart fall in different banks
+  static constexpr int OCT = 8 * MC + 2;                   // u64 per octet
+  static constexpr int TITEM = 4 * OCT;                    // u64 per item
+  static constexpr int TAB = MT_ITEMS * TITEM * 8;
+  static constexpr int TAB_OFF = STAGES_OFF + MT_NS * STAGE;
+  static constexpr int YSUM = MT_BLOCKS * MC * 4;          // one set of block sums: [block][MC]
+  static constexpr int YSUM_OFF = TAB_OFF + 2 * TAB;
+  static constexpr int TB = MT_BLOCKS * R * MC * 4;        // one fold buffer: [block][R][MC]
+  static constexpr int TB_OFF = YSUM_OFF + 2 * YSUM;
+  static constexpr int BYTES = TB_OFF + 2 * TB;
+  static constexpr int SMEM = BYTES + 1024;                // slack to align the base
+  static constexpr int FA = R * MC / MT_CT;                // (row, column) accumulators per thread
+  static constexpr int RW = R / MT_CW;                     // rows folded per compute warp
+};
+
+struct MtPlan {
+  int tiles;     // row tiles x column chunks
+  int CC;        // column chunks (of MC columns)
+  int NSEG;      // segments per row (ceil(K / 512))
+};
+
+// mbarriers in the header: stage full/empty, table full/empty, fold buffer
+// full/empty
+struct MtBars {
+  uint64_t full[MT_NS], empty[MT_NS];
+  uint64_t tfull[2], tempty[2];
+  uint64_t bfull[2], bempty[2];
+};
+
+template <int BITS, bool FOLD, int U>
+__global__ void __launch_bounds__(MT_THREADS, 1)
+    gemm_mt_kernel(GemvArgs a, MtPlan P, const __grid_constant__ CUtensorMap tm_codes,
+                   const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_x) {
+  using L = MtLayout<BITS, U>;
+  constexpr int R = L::R, MC = L::MC;
+  constexpr int CPW = 32 / BITS, HALF = CPW / 2, WPB = 32 / CPW, NP = 16 / CPW;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  constexpr int CPI = BITS / 2;          // 16-byte chunks per item and row
+  constexpr int IPB = 8 / CPI;           // items per 128-byte box
+  static_assert(MC == 4 && (L::FA == 1 || L::FA == 2) && (R * MC) % MT_CT == 0, "tile shape");
+
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024u - (sa(sm_raw) & 1023u)) & 1023u);
+  MtBars* B = reinterpret_cast<MtBars*>(sm);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(sm + 512);
+  int* err = &g_mt_error;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t perrow = a.perrow;
+
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) {
+    for (int s = 0; s < MT_NS; ++s) {
+      mbar_init(&B->full[s], 1);
+      mbar_init(&B->empty[s], MT_CW + MT_TW);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&B->tfull[b], MT_TW);
+      mbar_init(&B->tempty[b], MT_CW);
+      mbar_init(&B->bfull[b], MT_CW);
+      mbar_init(&B->bempty[b], MT_CW);
+    }
+    *abort_f = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // activations come from the previous kernel, and it may still read y
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ------------------------------------------------------------ copies --
+  if (warp == MT_CW + MT_TW) {
+    if (lane == 0) {
+      const uint32_t tx = (uint32_t)(L::NBOX * L::BOX + (perrow ? 0 : R * 32) + MC * 1024);
+      int g = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < P.tiles && !stop; t += gridDim.x) {
+        const int r0 = (t / P.CC) * R, m0 = (t % P.CC) * MC;
+        for (int s = 0; s < P.NSEG; ++s, ++g) {
+          const int slot = g % MT_NS;
+          if (g >= MT_NS &&
+              !mbar_wait_fast(&B->empty[slot], ((g / MT_NS) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) {
+            stop = true;
+            break;
+          }
+          if (*abort_f) {
+            stop = true;
+            break;
+          }
+          unsigned char* st = sm + L::STAGES_OFF + slot * L::STAGE;
+          mbar_arrive_tx(&B->full[slot], tx);
+#pragma unroll
+          for (int b = 0; b < L::NBOX; ++b) tma_2d(st + b * L::BOX, &tm_codes, s * 8 * BITS + 16 * b, r0, &B->full[slot]);
+          if (!perrow) tma_2d(st + L::SC_OFF, &tm_scales, s * 16, r0, &B->full[slot]);
+          tma_2d(st + L::X_OFF, &tm_x, s * MT_KS, m0, &B->full[slot]);
+          tma_2d(st + L::X_OFF + MC * 512, &tm_x, s * MT_KS + 256, m0, &B->full[slot]);
+        }
+      }
+      // let every copy issued land before the CTA can exit
+      for (int j = (g > MT_NS ? g - MT_NS : 0); j < g; ++j) mbar_drain(&B->full[j % MT_NS], (j / MT_NS) & 1, err);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------- table warps --
+  if (warp >= MT_CW) {
+    const int tt = tid - MT_CT;   // 0 .. 63
+    int g = 0;
+    for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
+      for (int s = 0; s < P.NSEG; ++s, ++g) {
+        const int slot = g % MT_NS, b = g & 1;
+        if (!mbar_wait_fast(&B->full[slot], (g / MT_NS) & 1, abort_f, ERR_MT_TIMEOUT, err)) return;
+        if (g >= 2 && !mbar_wait_fast(&B->tempty[b], ((g >> 1) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) return;
+        const unsigned char* st = sm + L::STAGES_OFF + slot * L::STAGE;
+        const __half* xs = reinterpret_cast<const __half*>(st + L::X_OFF);
+        u64* tab = reinterpret_cast<u64*>(sm + L::TAB_OFF + b * L::TAB);
+        float* ysum = reinterpret_cast<float*>(sm + L::YSUM_OFF + b * L::YSUM);
+        const int items = min(MT_ITEMS, (a.K - s * MT_KS) / 64);
+        // 8 fp16 activations of column m from element k (a multiple of 8)
+        auto chunk = [&](int m, int k, float (&f)[8]) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xs + (k >> 8) * (MC * 256) + m * 256 + (k & 255));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 h2 = u32_as_h2(w[e]);
+            f[2 * e] = __low2float(h2);
+            f[2 * e + 1] = __high2float(h2);
+          }
+        };
+        // task (m, item, quarter): 8 steps of one item for one column, from
+        // two 16-byte chunks of activations; the lanes of a warp walk
+        // (item, quarter) within a column
+        for (int task = tt; task < MC * items * 4; task += 32 * MT_TW) {
+          const int m = task / (items * 4), iq = task % (items * 4), item = iq >> 2, q = iq & 3;
+          const int hq = q & 1, blk = q >> 1;
+          float A[8], Bv[8];
+          if (!FOLD) {
+            chunk(m, 64 * item + 8 * q, A);          // block 0, codes 8q ..
+            chunk(m, 64 * item + 32 + 8 * q, Bv);    // block 1, codes 8q ..
+          } else {
+            const int a0 = 64 * item + 32 * blk + (BITS == 2 ? 8 : 16) * hq;
+            chunk(m, a0, A);
+            chunk(m, a0 + (BITS == 2 ? 16 : 8), Bv);
+          }
+          u64* dst = tab + (size_t)item * L::TITEM + q * L::OCT + m;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float v0, v1, sc;
+            if (!FOLD) {
+              // step k = 8q + i: (code k of block 0, code k of block 1) * 2^-o(k)
+              sc = pow2f(-BITS * (((8 * q + i) % CPW) % HALF));
+              v0 = A[i];
+              v1 = Bv[i];
+            } else {
+              // step 16*blk + CPW*p + j: (code j of word 2p, of word 2p+1)
+              const int j = (8 * hq + i) % CPW;
+              sc = pow2f(FOLD_E - BITS * (j % HALF));
+              if (BITS == 8) {
+                v0 = (i < 4) ? A[i] : Bv[i - 4];
+                v1 = (i < 4) ? A[i + 4] : Bv[i];
+              } else {
+                v0 = A[i];
+                v1 = Bv[i];
+              }
+            }
+            dst[i * MC] = pk(__fmul_rn(v0, sc), __fmul_rn(v1, sc));
+          }
+        }
+        if (FOLD) {
+          // per block, the activation sum in the order of the dots (even and
+          // odd words serially, then added), times 2^(b-1)
+          for (int task = tt; task < MC * 2 * items; task += 32 * MT_TW) {
+            const int m = task / (2 * items), bl = task % (2 * items);
+            float y[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float f[8];
+              chunk(m, 32 * bl + 8 * c, f);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y[8 * c + e] = f[e];
+            }
+            float S0 = 0.0f, S1 = 0.0f;
+#pragma unroll
+            for (int t16 = 0; t16 < 16; ++t16) {
+              const int k0 = 2 * CPW * (t16 / CPW) + t16 % CPW;
+              S0 = __fadd_rn(S0, y[k0]);
+              S1 = __fadd_rn(S1, y[k0 + CPW]);
+            }
+            ysum[bl * MC + m] = __fmul_rn(__fadd_rn(S0, S1), (float)(1 << (BITS - 1)));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&B->tfull[b]);
+          mbar_arrive(&B->empty[slot]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ----------------------------------------------------- compute warps --
+  float acc[L::FA];
+  bool ok = true;
+  // fold the block results of segment gg (its items) into the accumulators:
+  // every compute thread owns FA (row, column) pairs
+  // thread's share of the fold: FA consecutive columns of one row (warp w
+  // folds rows RW*w .. RW*w + RW - 1)
+  const int frow = L::RW * warp + lane % L::RW, fc0 = (lane / L::RW) * L::FA;
+  auto fold = [&](int gg, int its) {
+    const int bb = gg & 1;
+    if (ok) ok = mbar_wait_fast(&B->bfull[bb], (gg >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
+    if (ok) {
+      const float* tb = reinterpret_cast<const float*>(sm + L::TB_OFF + bb * L::TB) + frow * MC + fc0;
+      float v[MT_BLOCKS][L::FA];
+#pragma unroll
+      for (int b = 0; b < MT_BLOCKS; ++b) {
+        if (b < 2 * its) {
+          if (L::FA == 2) {
+            const float2 f2 = *reinterpret_cast<const float2*>(tb + b * R * MC);
+            v[b][0] = f2.x;
+            v[b][L::FA - 1] = f2.y;
+          } else {
+            v[b][0] = tb[b * R * MC];
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < MT_BLOCKS; ++b)
+        if (b < 2 * its)
+#pragma unroll
+          for (int f = 0; f < L::FA; ++f) acc[f] = __fadd_rn(acc[f], v[b][f]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&B->bempty[bb]);
+  };
+
+  int g = 0;
+  for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
+    const int r0 = (t / P.CC) * R, m0 = (t % P.CC) * MC;
+#pragma unroll
+    for (int i = 0; i < L::FA; ++i) acc[i] = 0.0f;
+    int prev_items = 0;
+    for (int s = 0; s < P.NSEG; ++s, ++g) {
+      const int slot = g % MT_NS, b = g & 1;
+      const int items = min(MT_ITEMS, (a.K - s * MT_KS) / 64);
+      if (ok) ok = mbar_wait_fast(&B->full[slot], (g / MT_NS) & 1, abort_f, ERR_MT_TIMEOUT, err);
+      if (ok) ok = mbar_wait_fast(&B->tfull[b], (g >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
+      if (ok && g >= 2) ok = mbar_wait_fast(&B->bempty[b], ((g >> 1) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
+
+      // item `warp` of the segment for all R rows (lane: rows lane + 32u)
+      if (ok && warp < items) {
+        const unsigned char* st = sm + L::STAGES_OFF + slot * L::STAGE;
+        const u64* tabi = reinterpret_cast<const u64*>(sm + L::TAB_OFF + b * L::TAB) + (size_t)warp * L::TITEM;
+        const float* ysum = reinterpret_cast<const float*>(sm + L::YSUM_OFF + b * L::YSUM);
+        float* tb = reinterpret_cast<float*>(sm + L::TB_OFF + b * L::TB);
+        const int item = warp;
+        const unsigned char* cbox = st + (item / IPB) * L::BOX;
+        const int ch0 = (item % IPB) * CPI;
+        u64 wp[U][BITS];   // the item's words as 64-bit pairs (2q, 2q + 1)
+        uint32_t scw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int r = lane + 32 * u;
+#pragma unroll
+          for (int c = 0; c < CPI; ++c) {
+            // 128-byte swizzle: chunk c of row r sits at chunk c ^ (r % 8)
+            const ulonglong2 v =
+                *reinterpret_cast<const ulonglong2*>(cbox + r * 128 + (((ch0 + c) ^ (lane & 7)) << 4));
+            wp[u][2 * c] = v.x;
+            wp[u][2 * c + 1] = v.y;
+          }
+          scw[u] = perrow ? 0u : *reinterpret_cast<const uint32_t*>(st + L::SC_OFF + r * 32 + item * 4);
+        }
+        if (FOLD) {
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            u64 acc2[U][MC];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+              for (int mm = 0; mm < MC; ++mm) acc2[u][mm] = 0ull;
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+              u64 lo[U], hi[U];
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                lo[u] = wp[u][blk * NP + p];
+                hi[u] = lo[u] >> 16;
+              }
+#pragma unroll
+              for (int j = 0; j < CPW; ++j) {
+                const uint32_t m32 = MASK << (BITS * (j % HALF));
+                const u64 mm64 = ((u64)m32 << 32) | m32;
+                u64 v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) v[u] = ((j < HALF) ? lo[u] : hi[u]) & mm64;
+                const int tq = CPW * p + j;   // step 16*blk + tq
+                const u64* yk = tabi + (2 * blk + (tq >> 3)) * L::OCT + (tq & 7) * MC;
+#pragma unroll
+                for (int mm = 0; mm < MC; mm += 2) {
+                  const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
+#pragma unroll
+                  for (int u = 0; u < U; ++u) {
+                    acc2[u][mm] = ffma2(y2.x, v[u], acc2[u][mm]);
+                    acc2[u][mm + 1] = ffma2(y2.y, v[u], acc2[u][mm + 1]);
+                  }
+                }
+              }
+            }
+            const int bl = 2 * item + blk;
+            const float4 bS = *reinterpret_cast<const float4*>(ysum + bl * MC);
+            const float bs[4] = {bS.x, bS.y, bS.z, bS.w};
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const float sc = __half2float(__ushort_as_half((uint16_t)(blk ? (scw[u] >> 16) : (scw[u] & 0xFFFFu))));
+              float o[MC];
+#pragma unroll
+              for (int mm = 0; mm < MC; ++mm) {
+                float pe, po;
+                upk(acc2[u][mm], pe, po);
+                float pb = fold_block(__fadd_rn(pe, po), bs[mm]);
+                if (!perrow) pb = __fmul_rn(pb, sc);
+                o[mm] = pb;
+              }
+              *reinterpret_cast<float4*>(tb + (bl * R + lane + 32 * u) * MC) = make_float4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        } else {
+          uint32_t w[U][2 * WPB];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int q = 0; q < BITS; ++q) {
+              w[u][2 * q] = (uint32_t)wp[u][q];
+              w[u][2 * q + 1] = (uint32_t)(wp[u][q] >> 32);
+            }
+          u64 acc2[U][MC];
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int mm = 0; mm < MC; ++mm) acc2[u][mm] = 0ull;
+#pragma unroll
+          for (int wi = 0; wi < WPB; ++wi) {
+            uint32_t h0[U], h1[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              h0[u] = w[u][wi] >> 16;
+              h1[u] = w[u][WPB + wi] >> 16;
+            }
+#pragma unroll
+            for (int j = 0; j < CPW; ++j) {
+              const int o = BITS * (j % HALF);
+              const float offf = pow2f(23) + (float)(1 << (BITS - 1 + o));
+              u64 v[U];
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                const uint32_t wa = (j < HALF) ? w[u][wi] : h0[u];
+                const uint32_t wb = (j < HALF) ? w[u][WPB + wi] : h1[u];
+                v[u] = decode2(wa, wb, MASK << o, pk(offf, offf));
+              }
+              const int tk = wi * CPW + j;   // step
+              const u64* yk = tabi + (tk >> 3) * L::OCT + (tk & 7) * MC;
+#pragma unroll
+              for (int mm = 0; mm < MC; mm += 2) {
+                const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                  acc2[u][mm] = ffma2(y2.x, v[u], acc2[u][mm]);
+                  acc2[u][mm + 1] = ffma2(y2.y, v[u], acc2[u][mm + 1]);
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const float s_lo = __half2float(__ushort_as_half((uint16_t)(scw[u] & 0xFFFFu)));
+            const float s_hi = __half2float(__ushort_as_half((uint16_t)(scw[u] >> 16)));
+            const int r = lane + 32 * u;
+            float o0[MC], o1[MC];
+#pragma unroll
+            for (int mm = 0; mm < MC; ++mm) {
+              float p0, p1;
+              upk(acc2[u][mm], p0, p1);
+              o0[mm] = perrow ? p0 : __fmul_rn(p0, s_lo);
+              o1[mm] = perrow ? p1 : __fmul_rn(p1, s_hi);
+            }
+            *reinterpret_cast<float4*>(tb + ((2 * item) * R + r) * MC) = make_float4(o0[0], o0[1], o0[2], o0[3]);
+            *reinterpret_cast<float4*>(tb + ((2 * item + 1) * R + r) * MC) = make_float4(o1[0], o1[1], o1[2], o1[3]);
+          }
+        }
+      }
+      // the stage, the table and this warp's share of the fold buffer are done
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&B->empty[slot]);
+        mbar_arrive(&B->tempty[b]);
+        mbar_arrive(&B->bfull[b]);
+      }
+      // the previous segment's fold, one segment late so that warps do not
+      // wait for each other's items; the tile's last segment is folded at
+      // once and the tile stored
+      if (s >= 1) fold(g - 1, prev_items);
+      if (s == P.NSEG - 1) {
+        fold(g, items);
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < L::FA; ++i) {
+            const int64_t n = (int64_t)r0 + frow;
+            const int col = m0 + fc0 + i;
+            if (n < a.N && col < a.M) {
+              float out = acc[i];
+              if (perrow) out = __fadd_rn(0.0f, __fmul_rn(out, __half2float(a.scales[n])));
+              const int64_t o = (int64_t)col * a.N + n;
+              if (a.y_f16)
+                reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(out);
+              else
+                reinterpret_cast<float*>(a.y)[o] = out;
+            }
+          }
+        }
+      }
+      prev_items = items;
+    }
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------- launcher --
+
+int read_mt_error(int clear, int* out) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_mt_error, sizeof(int));
+  if (e != cudaSuccess) return (int)e;
+  if (clear && v) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_mt_error, &z, sizeof(int));
+    if (e != cudaSuccess) return (int)e;
+  }
+  *out = v;
+  return 0;
+}
+
+namespace {
+
+template <int BITS, bool FOLD, int U>
+int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
+  using L = MtLayout<BITS, U>;
+  constexpr int R = L::R, MC = L::MC;
+  auto kern = gemm_mt_kernel<BITS, FOLD, U>;
+  static thread_local KernCache cache;
+  const DevInfo& d = dev_info();
+  if ((size_t)L::SMEM > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
+  int occ = 0;
+  cudaError_t e = prep_kernel(kern, cache, MT_THREADS, L::SMEM, &occ);
+  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  if (occ < 1) return QMV_ERR_UNSUPPORTED;
+  // codes as UINT64 [N][row_bytes/8] (box 16 x R, 128-byte swizzle), scales
+  // as UINT16 [N][K/32] (box 16 x R), activations as FP16 [M][K] (box 256 x
+  // MC); rows past N or M and columns past K are zero-filled
+  const uint64_t row_bytes = (uint64_t)a.K * BITS / 8;
+  CUtensorMap tmc, tms, tmx;
+  if (!enc2d(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT64, a.codes, row_bytes / 8, (uint64_t)a.N, row_bytes, 16, R,
+             CU_TENSOR_MAP_SWIZZLE_128B))
+    return QMV_ERR_UNSUPPORTED;
+  if (a.perrow)
+    tms = tmc;   // unused
+  else if (!enc2d(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)a.G, (uint64_t)a.N,
+                  (uint64_t)a.G * 2, 16, R, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return QMV_ERR_UNSUPPORTED;
+  if (!enc2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 256, MC,
+             CU_TENSOR_MAP_SWIZZLE_NONE))
+    return QMV_ERR_UNSUPPORTED;
+  MtPlan P;
+  P.CC = (a.M + MC - 1) / MC;
+  P.tiles = (int)(((int64_t)a.N + R - 1) / R) * P.CC;
+  P.NSEG = (a.K + MT_KS - 1) / MT_KS;
+  const int grid = P.tiles < d.sms ? P.tiles : d.sms;
+  if (pdl_enabled()) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(MT_THREADS);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, P, tmc, tms, tmx);
+  } else {
+    kern<<<grid, MT_THREADS, L::SMEM, s>>>(a, P, tmc, tms, tmx);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  return QMV_OK;
+}
+
+// Estimated time of a row-tile height (U rows per lane), in SM cycles: whole
+// rounds of tiles over the SMs, each segment about 4*R*MC cycles of paired
+// FMAs (with two rows per lane the broadcast activation loads are as busy as
+// the FMA pipe: +25 %) plus a fixed cost.
+double mt_cost(int N, int M, int K, int U, int sms) {
+  const int R = 32 * U;
+  const int64_t tiles = (((int64_t)N + R - 1) / R) * ((M + MT_MC - 1) / MT_MC);
+  const int64_t rounds = (tiles + sms - 1) / sms;
+  const double seg = 4.0 * R * MT_MC * (U == 2 ? 1.25 : 1.0) + 400.0;
+  return (double)rounds * ((K + MT_KS - 1) / MT_KS) * seg;
+}
+
+template <int BITS, bool FOLD>
+int mt_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
+  if constexpr (BITS == 8) {
+    return run_mt<BITS, FOLD, 2>(a, s, err);   // int8: 16 words a row, two rows per lane
+  } else {
+    const int sms = dev_info().sms;
+    if (mt_cost(a.N, a.M, a.K, 4, sms) <= mt_cost(a.N, a.M, a.K, 2, sms)) return run_mt<BITS, FOLD, 4>(a, s, err);
+    return run_mt<BITS, FOLD, 2>(a, s, err);
+  }
+}
+
+}  // namespace
+
+int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
+  if (a.fused || a.M < 2 || a.K % 256 != 0 || a.gather_rows || a.amax_ws) return QMV_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(a.x) & 15u) != 0) return QMV_ERR_UNSUPPORTED;
+  if (a.folded) {
+    switch (bits) {
+      case 2: return mt_bits<2, true>(a, s, err);
+      case 4: return mt_bits<4, true>(a, s, err);
+      default: return mt_bits<8, true>(a, s, err);
+    }
+  }
+  switch (bits) {
+    case 2: return mt_bits<2, false>(a, s, err);
+    case 4: return mt_bits<4, false>(a, s, err);
+    default: return mt_bits<8, false>(a, s, err);
+  }
+}
+
+}  // namespace qmv

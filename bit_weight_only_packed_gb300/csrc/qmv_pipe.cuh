@@ -612,5 +612,9 @@ __device__ __forceinline__ void fold_stage(const GemvArgs& a, const TmaPlan& P, 
 // [N][row_bytes/8] with a box of (segment bytes / 8) x R, scales as UINT16
 // [N][K/32] with a box of (K_seg / 32) x R.  Host only.
 bool encode_pack_maps(const GemvArgs& a, const pipe::TmaPlan& P, CUtensorMap* tc, CUtensorMap* ts);
+// A 2-D tensor map: `rows` rows of `inner` elements, `row_bytes` apart, a box
+// of box_inner x box_rows, zero fill past the edges (qmv_tc.cu).  Host only.
+bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+           uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
 
 }  // namespace qmv

@@ -100,6 +100,31 @@ __device__ __forceinline__ void tc_tma2d(void* dst, const CUtensorMap* map, int 
       : "memory");
 }
 
+// The same copy with an L2 cache policy (from createpolicy): the streamed
+// weights are marked evict-first and the activation tiles, which every row
+// tile re-reads, evict-last, so the weight stream does not push the
+// activations out of L2.
+__device__ __forceinline__ void tc_tma2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // 64-bit shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
 // rows of 128 bytes stacked in 1024-byte groups of 8 (SBO = 1024 B).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -188,14 +213,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == W_RAW) {
     // ------------------------------------------- TMA: packed codes/scales --
     if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
       int issued = 0;
       for (int i = 0; i < nslab; i += RS) {
         const int j = i / RS, rr = j % NRAW;
         if (j >= NRAW && !tc_wait(&raw_empty[rr], ((j / NRAW) - 1) & 1, abort_f)) break;
         unsigned char* rb = rawbuf + rr * RAW_BYTES;
         tc_mbar_arrive_tx(&raw_full[rr], a.perrow ? RAW_CODES : RAW_BYTES);
-        tc_tma2d(rb, &tm_codes, (slab0 + i) * 4, n0, &raw_full[rr]);
-        if (!a.perrow) tc_tma2d(rb + RAW_CODES, &tm_scales, (slab0 + i) * 2, n0, &raw_full[rr]);
+        tc_tma2d_hint(rb, &tm_codes, (slab0 + i) * 4, n0, &raw_full[rr], pol);
+        if (!a.perrow) tc_tma2d_hint(rb + RAW_CODES, &tm_scales, (slab0 + i) * 2, n0, &raw_full[rr], pol);
         ++issued;
       }
       for (int j = (issued > NRAW ? issued - NRAW : 0); j < issued; ++j)
@@ -204,12 +230,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == W_B) {
     // --------------------------------------------- TMA: activation tiles --
     if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_last();
       int issued = 0;
       for (int i = 0; i < nslab; ++i) {
         const int s = i % NST;
         if (i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f)) break;
         tc_mbar_arrive_tx(&b_full[s], B_BYTES);
-        tc_tma2d(tiles + s * STAGE + A_BYTES, &tm_x, (slab0 + i) * 64, 0, &b_full[s]);
+        tc_tma2d_hint(tiles + s * STAGE + A_BYTES, &tm_x, (slab0 + i) * 64, 0, &b_full[s], pol);
         ++issued;
       }
       for (int i = (issued > NST ? issued - NST : 0); i < issued; ++i)
@@ -377,7 +404,8 @@ static TcEncodeFn tc_encode_fn() {
   return fn;
 }
 
-static bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+// A 2-D tensor map (also used by the M-column pipeline tiles).
+bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
   TcEncodeFn enc = tc_encode_fn();
   if (!enc) return false;

@@ -522,13 +522,17 @@ int launch_gemv_tma(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* er
 
 int read_tc_error(int clear, int* out);
 int read_chain_error(int clear, int* out);
+int read_mt_error(int clear, int* out);
 
 int read_device_error(int clear, int* out) {
-  int t = 0, ch = 0;
+  int t = 0, ch = 0, mt = 0;
   const int et = read_tc_error(clear, &t);
   if (et != 0) return et;
   const int ec = read_chain_error(clear, &ch);
   if (ec != 0) return ec;
+  const int em = read_mt_error(clear, &mt);
+  if (em != 0) return em;
+  if (mt) t = mt;
   if (ch) t = ch;
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_qmv_error, sizeof(int));

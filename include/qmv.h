@@ -36,7 +36,7 @@
  * field holds u = v + 2^(bits-1) for the signed code v, so int2 fields
  * 0,1,2,3 decode to -2,-1,0,1.  Scales are fp16 [N][K/group].
  *
- * Accumulation order (QMV_EXACT, CUDA-core paths, M <= 32 per launch): for
+ * Accumulation order (QMV_EXACT, every CUDA-core path, any M): for
  * each output scalar, each block of 32 consecutive codes is summed serially
  * in k in fp32 (products are exact); with group 32 the block sum is
  * multiplied by its scale (rounded) and added to the accumulator (rounded),
@@ -45,7 +45,7 @@
  * oracle's order, so QMV_EXACT results are bit-identical to it, and every
  * column of an M-tile is bit-identical to the M = 1 result.
  *
- * QMV_FAST (M <= 32): the same blocks, scales and fold, with the code offset
+ * QMV_FAST (CUDA-core paths): the same blocks, scales and fold, with the code offset
  * taken out of the per-code work: each block is summed as sum(y*u) over the
  * unsigned fields u (even and odd words in two serial chains, then added)
  * minus 2^(bits-1) times the block's activation sum formed in the same
@@ -123,12 +123,13 @@ QMV_API int qmv_pack_weights(qmv_pack *p, const int8_t *d_codes_in, const uint16
  * x[m][k] * v[n][k]) * s[n][g] in the order stated at the top of this file.
  * [A19] int2 item (exact products, fp32 in code order); [PLAY] K-order-fixed
  * row for M <= 16 and matrix-unit row for M >= 64.
- *   M            1 .. 4096.  M <= 32 runs the CUDA-core kernels (QMV_EXACT
- *                bit-exact, QMV_FAST within tolerance); M > 32 with QMV_FAST
- *                runs tcgen05 tensor-core tiles for int2 (fp32 accumulate,
- *                hardware order) and the CUDA-core tiles for int4/int8; M > 32
- *                with QMV_EXACT runs the CUDA-core kernels 32 columns at a
- *                time.
+ *   M            1 .. 4096.  Every M runs the CUDA-core kernels (QMV_EXACT
+ *                bit-exact, QMV_FAST within tolerance, each column equal to
+ *                the M = 1 result), except M > 32 with QMV_FAST and int2
+ *                weights, which runs tcgen05 tensor-core tiles (fp32
+ *                accumulate, hardware order, within tolerance).  With K a
+ *                multiple of 256 the M >= 2 CUDA-core tiles take all M
+ *                columns in one launch; otherwise 32 columns per launch.
  *   N, K, bits, group  must equal the pack's (QMV_ERR_SHAPE otherwise).
  *   x            device fp16 [M][K], 16-byte aligned.
  *   y            device [M][N] of y_dtype (fp32, or fp16 = RNE of the fp32
@@ -157,9 +158,10 @@ QMV_API int qmv_fused_rmsnorm_gemv(const qmv_pack *p, int M, const void *x, cons
 /*
  * qmv_chunk_gemm -- a prefill chunk of M tokens against one pack ([PLAY]
  * prefill-regimes table): the same computation as qmv_gemv with the pack's
- * own N, K, bits and group.  M = 4, 8, 16 (and any M <= 32) use the
- * K-order-fixed CUDA-core tiles; M = 64, 128 (any M > 32) in QMV_FAST use
- * tcgen05 tensor-core tiles.
+ * own N, K, bits and group.  M = 4, 8, 16 (and any M <= 32, or any M in
+ * QMV_EXACT, or int4/int8) use the K-order-fixed CUDA-core tiles; M = 64,
+ * 128 (any M > 32) in QMV_FAST with int2 weights use tcgen05 tensor-core
+ * tiles.
  */
 QMV_API int qmv_chunk_gemm(const qmv_pack *p, int M, const void *x, void *y, int y_dtype,
                    int mode, void *stream);
