@@ -232,6 +232,48 @@ def chain_layers(qmv, layers, b, n):
     return ch
 
 
+def prefill_layers(qmv, layers, dev, stream, M, reps):
+    """The layer's four matrices as prefill chunks of M tokens (qmv_chunk_gemm,
+    fast mode, fp16 outputs), rotating over the resident layers: M = 16 runs the
+    K-order-fixed CUDA-core tiles (every column equal to the M = 1 result), M =
+    128 the tensor-core tiles for the int2 matrices and the CUDA-core tiles for
+    int4.  Returns (ms per layer, tokens/s, TFLOP/s)."""
+    import torch
+
+    import synth
+    xs = {K: torch.from_numpy(synth.normal_f16(SEED, f"bench.prefill{M}.{K}", (M, K))).to(dev)
+          for K in sorted({K for _, _, K, _, _, _ in LAYER})}
+    ys = {name: torch.empty(M, N, dtype=torch.float16, device=dev) for name, N, *_ in LAYER}
+
+    def run(li):
+        for name, N, K, *_ in LAYER:
+            qmv.qmv_chunk_gemm(layers[li][name], xs[K], y=ys[name], y_dtype=qmv.QMV_F16,
+                               mode=qmv.QMV_FAST, stream=stream)
+
+    L = len(layers)
+    with torch.cuda.stream(stream):
+        run(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for li in range(L):
+            run(li)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1)) / (reps * L)
+    flops = 2.0 * M * sum(N * K for _, N, K, *_ in LAYER)
+    return ms, M / (ms * 1e-3), flops / (ms * 1e-3) / 1e12
+
+
 def gpu_arm(args, rank, world, local):
     import torch
 
@@ -362,6 +404,14 @@ def gpu_arm(args, rank, world, local):
     chain_info = ch.info()
     ch.close()
 
+    # ---- the same layers as prefill chunks (a9 / a10 rows) ----
+    prefill = {}
+    for M in (16, 128):
+        p_ms, p_tok, p_tf = prefill_layers(qmv, layers, dev, stream, M, max(1, K // (4 * L)))
+        prefill[f"M{M}"] = {"ms_per_layer": round(p_ms, 5), "tok_per_s": round(world * p_tok, 1),
+                            "tflops": round(world * p_tf, 2),
+                            "gbs": round(world * LAYER_BYTES / (p_ms * 1e-3) / 1e9, 1)}
+
     peak, peak_kind = peaks()
     gbs = world * LAYER_BYTES * K / (ms_max * 1e-3) / 1e9
     dom_bytes = packed_bytes(2 * D_FF, D_MODEL, 2, 32)
@@ -402,6 +452,10 @@ def gpu_arm(args, rank, world, local):
                   "grid_barriers": chain_info["barriers"],
                   "note": "same dependent layers as one persistent cooperative launch (qmv_chain_run); "
                           "the headline value uses CUDA graphs with programmatic dependent launch"},
+        "prefill": dict(prefill, note="the layer's four matrices as prefill chunks (qmv_chunk_gemm, "
+                        "fast mode): M=16 on the K-order-fixed CUDA-core tiles (each column equal to "
+                        "M=1), M=128 on tcgen05 tensor tiles (int2) and CUDA-core tiles (int4); "
+                        "weights rotated over the resident layers"),
     }
     return out
 

@@ -47,7 +47,7 @@ constexpr int MT_ITEMS = MT_KS / 64;         // 64-code items per segment (one p
 constexpr int MT_BLOCKS = MT_KS / 32;        // 32-code blocks per segment
 constexpr int MT_MC = 4;                     // token columns per tile
 constexpr int MT_CW = MT_ITEMS;              // compute warps
-constexpr int MT_TW = 2;                     // table warps
+constexpr int MT_TW = 4;                     // table warps (fold and store too)
 constexpr int MT_CT = 32 * MT_CW;            // compute threads
 constexpr int MT_THREADS = 32 * (MT_CW + MT_TW + 1);   // + the copy warp
 constexpr int MT_HDR = 1024;                 // barriers, flags
@@ -79,8 +79,7 @@ struct MtLayout {
   static constexpr int TB_OFF = YSUM_OFF + 2 * YSUM;
   static constexpr int BYTES = TB_OFF + 2 * TB;
   static constexpr int SMEM = BYTES + 1024;                // slack to align the base
-  static constexpr int FA = R * MC / MT_CT;                // (row, column) accumulators per thread
-  static constexpr int RW = R / MT_CW;                     // rows folded per compute warp
+  static constexpr int FC = R * MC / (32 * MT_TW);        // columns folded per table-warp thread (one row)
 };
 
 struct MtPlan {
@@ -107,7 +106,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   constexpr uint32_t MASK = (1u << BITS) - 1u;
   constexpr int CPI = BITS / 2;          // 16-byte chunks per item and row
   constexpr int IPB = 8 / CPI;           // items per 128-byte box
-  static_assert(MC == 4 && (L::FA == 1 || L::FA == 2) && (R * MC) % MT_CT == 0, "tile shape");
+  static_assert(MC == 4 && (L::FC == 4 || L::FC == 2) && R * MC == 32 * MT_TW * L::FC, "tile shape");
 
   extern __shared__ unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (sa(sm_raw) & 1023u)) & 1023u);
@@ -128,7 +127,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
       mbar_init(&B->tfull[b], MT_TW);
       mbar_init(&B->tempty[b], MT_CW);
       mbar_init(&B->bfull[b], MT_CW);
-      mbar_init(&B->bempty[b], MT_CW);
+      mbar_init(&B->bempty[b], MT_TW);
     }
     *abort_f = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -173,9 +172,65 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
 
   // -------------------------------------------------------- table warps --
   if (warp >= MT_CW) {
-    const int tt = tid - MT_CT;   // 0 .. 63
+    const int tt = tid - MT_CT;   // 0 .. 32*MT_TW - 1
+    // The fold, one segment behind the tables: thread tt owns FC columns of
+    // one row of the tile and adds the previous segment's block results in
+    // block order; after a tile's last segment it stores the tile.
+    const int frow = tt % R, fc0 = (tt / R) * L::FC;
+    float acc[L::FC];
+#pragma unroll
+    for (int c = 0; c < L::FC; ++c) acc[c] = 0.0f;
+    int p_items = 0, p_r0 = 0, p_m0 = 0;
+    bool p_last = false;
+    auto fold_prev = [&](int gg) -> bool {
+      const int bb = gg & 1;
+      if (!mbar_wait_fast(&B->bfull[bb], (gg >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) return false;
+      const float* tb = reinterpret_cast<const float*>(sm + L::TB_OFF + bb * L::TB) + frow * MC + fc0;
+      float v[MT_BLOCKS][L::FC];
+#pragma unroll
+      for (int bl = 0; bl < MT_BLOCKS; ++bl)
+        if (bl < 2 * p_items) {
+          if (L::FC == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
+            v[bl][0] = f.x;
+            v[bl][1] = f.y;
+            v[bl][L::FC - 2] = f.z;
+            v[bl][L::FC - 1] = f.w;
+          } else {
+            const float2 f = *reinterpret_cast<const float2*>(tb + bl * R * MC);
+            v[bl][0] = f.x;
+            v[bl][1] = f.y;
+          }
+        }
+#pragma unroll
+      for (int bl = 0; bl < MT_BLOCKS; ++bl)
+        if (bl < 2 * p_items)
+#pragma unroll
+          for (int c = 0; c < L::FC; ++c) acc[c] = __fadd_rn(acc[c], v[bl][c]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B->bempty[bb]);
+      if (p_last) {
+        const int64_t n = (int64_t)p_r0 + frow;
+#pragma unroll
+        for (int c = 0; c < L::FC; ++c) {
+          const int col = p_m0 + fc0 + c;
+          if (n < a.N && col < a.M) {
+            float out = acc[c];
+            if (perrow) out = __fadd_rn(0.0f, __fmul_rn(out, __half2float(a.scales[n])));
+            const int64_t o = (int64_t)col * a.N + n;
+            if (a.y_f16)
+              reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(out);
+            else
+              reinterpret_cast<float*>(a.y)[o] = out;
+          }
+          acc[c] = 0.0f;
+        }
+      }
+      return true;
+    };
     int g = 0;
     for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
+      const int r0 = (t / P.CC) * R, m0 = (t % P.CC) * MC;
       for (int s = 0; s < P.NSEG; ++s, ++g) {
         const int slot = g % MT_NS, b = g & 1;
         if (!mbar_wait_fast(&B->full[slot], (g / MT_NS) & 1, abort_f, ERR_MT_TIMEOUT, err)) return;
@@ -263,53 +318,21 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
           mbar_arrive(&B->tfull[b]);
           mbar_arrive(&B->empty[slot]);
         }
+        if (g >= 1 && !fold_prev(g - 1)) return;
+        p_items = items;
+        p_r0 = r0;
+        p_m0 = m0;
+        p_last = (s == P.NSEG - 1);
       }
     }
+    if (g >= 1) fold_prev(g - 1);
     return;
   }
 
   // ----------------------------------------------------- compute warps --
-  float acc[L::FA];
   bool ok = true;
-  // fold the block results of segment gg (its items) into the accumulators:
-  // every compute thread owns FA (row, column) pairs
-  // thread's share of the fold: FA consecutive columns of one row (warp w
-  // folds rows RW*w .. RW*w + RW - 1)
-  const int frow = L::RW * warp + lane % L::RW, fc0 = (lane / L::RW) * L::FA;
-  auto fold = [&](int gg, int its) {
-    const int bb = gg & 1;
-    if (ok) ok = mbar_wait_fast(&B->bfull[bb], (gg >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
-    if (ok) {
-      const float* tb = reinterpret_cast<const float*>(sm + L::TB_OFF + bb * L::TB) + frow * MC + fc0;
-      float v[MT_BLOCKS][L::FA];
-#pragma unroll
-      for (int b = 0; b < MT_BLOCKS; ++b) {
-        if (b < 2 * its) {
-          if (L::FA == 2) {
-            const float2 f2 = *reinterpret_cast<const float2*>(tb + b * R * MC);
-            v[b][0] = f2.x;
-            v[b][L::FA - 1] = f2.y;
-          } else {
-            v[b][0] = tb[b * R * MC];
-          }
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < MT_BLOCKS; ++b)
-        if (b < 2 * its)
-#pragma unroll
-          for (int f = 0; f < L::FA; ++f) acc[f] = __fadd_rn(acc[f], v[b][f]);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&B->bempty[bb]);
-  };
-
   int g = 0;
   for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
-    const int r0 = (t / P.CC) * R, m0 = (t % P.CC) * MC;
-#pragma unroll
-    for (int i = 0; i < L::FA; ++i) acc[i] = 0.0f;
-    int prev_items = 0;
     for (int s = 0; s < P.NSEG; ++s, ++g) {
       const int slot = g % MT_NS, b = g & 1;
       const int items = min(MT_ITEMS, (a.K - s * MT_KS) / 64);
@@ -466,30 +489,6 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
         mbar_arrive(&B->tempty[b]);
         mbar_arrive(&B->bfull[b]);
       }
-      // the previous segment's fold, one segment late so that warps do not
-      // wait for each other's items; the tile's last segment is folded at
-      // once and the tile stored
-      if (s >= 1) fold(g - 1, prev_items);
-      if (s == P.NSEG - 1) {
-        fold(g, items);
-        if (ok) {
-#pragma unroll
-          for (int i = 0; i < L::FA; ++i) {
-            const int64_t n = (int64_t)r0 + frow;
-            const int col = m0 + fc0 + i;
-            if (n < a.N && col < a.M) {
-              float out = acc[i];
-              if (perrow) out = __fadd_rn(0.0f, __fmul_rn(out, __half2float(a.scales[n])));
-              const int64_t o = (int64_t)col * a.N + n;
-              if (a.y_f16)
-                reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(out);
-              else
-                reinterpret_cast<float*>(a.y)[o] = out;
-            }
-          }
-        }
-      }
-      prev_items = items;
     }
   }
 }
@@ -567,14 +566,15 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
 }
 
 // Estimated time of a row-tile height (U rows per lane), in SM cycles: whole
-// rounds of tiles over the SMs, each segment about 4*R*MC cycles of paired
-// FMAs (with two rows per lane the broadcast activation loads are as busy as
-// the FMA pipe: +25 %) plus a fixed cost.
+// rounds of tiles over the SMs, times the segments per tile, times the
+// measured cost of one segment on GB300 (about 4500 cycles for 128 rows, 2900
+// for 64: a fixed part for the copies, tables, waits and block finishes plus
+// the paired FMAs, which scale with the rows).
 double mt_cost(int N, int M, int K, int U, int sms) {
   const int R = 32 * U;
   const int64_t tiles = (((int64_t)N + R - 1) / R) * ((M + MT_MC - 1) / MT_MC);
   const int64_t rounds = (tiles + sms - 1) / sms;
-  const double seg = 4.0 * R * MT_MC * (U == 2 ? 1.25 : 1.0) + 400.0;
+  const double seg = 1300.0 + 25.0 * R;
   return (double)rounds * ((K + MT_KS - 1) / MT_KS) * seg;
 }
 
