@@ -10,8 +10,12 @@
 // fp32 accumulator lives in tensor memory.
 //
 // One CTA computes a 128-row x MT-token tile (MT = 64 or 128) over a K range
-// (split-K when there are fewer row tiles than SMs; partial tiles are added
-// into y with fp32 reductions).  Roles:
+// (split-K when there are fewer row tiles than SMs: with two splits and fp32
+// output the partial tiles are added into the zeroed y with fp32 atomics,
+// which is order-independent for two terms (0 + a + b == 0 + b + a); otherwise
+// each split stores its partial tile to a stream-ordered fp32 scratch and a
+// second kernel adds the splits in split order, so the result never depends
+// on CTA timing).  Roles:
 //   warp 8 (one thread): TMA of the packed codes and scales of the tile, 4
 //     K-slabs (256 codes) at a time, into a ring of 4 raw stages (16 slabs of
 //     prefetch).
@@ -146,8 +150,9 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 
 struct TcArgs {
   const __half* scales;    // [N][G] (one scale per row when perrow)
-  float* y;                // [M][N] fp32 (reduced into when split > 1)
-  __half* y16;             // [M][N] fp16 output (only without split)
+  float* y;                // [M][N] fp32 output (or null)
+  __half* y16;             // [M][N] fp16 output (or null)
+  float* part;             // [split][M][N] fp32 partial tiles (split > 1, unless atomics)
   int N, K, G, M, perrow;
   int slabs_per_split;     // 64-wide K slabs per CTA
   int split;               // gridDim.y
@@ -350,7 +355,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (m < a.M) {
               const float f = __uint_as_float(v[q]);
               const int64_t o = (int64_t)m * a.N + n;
-              if (a.split > 1)
+              if (a.part)
+                a.part[(int64_t)blockIdx.y * a.M * a.N + o] = f;
+              else if (a.split > 1)
                 atomicAdd(a.y + o, f);
               else if (a.y16)
                 a.y16[o] = __float2half_rn(f);
@@ -404,6 +411,20 @@ static TcEncodeFn tc_encode_fn() {
   return fn;
 }
 
+// Split-K reduction: y[i] = sum of the splits' partials in split order (fp32
+// adds), stored as fp32 or as the RNE fp16 of that sum.
+__global__ void tc_reduce_kernel(const float* __restrict__ part, int split, int64_t total, float* y,
+                                 __half* y16) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  float v = part[i];
+  for (int sp = 1; sp < split; ++sp) v = __fadd_rn(v, part[(int64_t)sp * total + i]);
+  if (y16)
+    y16[i] = __float2half_rn(v);
+  else
+    y[i] = v;
+}
+
 // A 2-D tensor map (also used by the M-column pipeline tiles).
 bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
@@ -451,12 +472,12 @@ static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s
   TcArgs a = a0;
   const int nslab = a.K / 64;
   const int sms = dev_info().sms;
-  // split K across CTAs (fp32 output only: the splits add into y) to balance
-  // the waves: the time is about ceil(tiles * split / SMs) CTA-slots of
-  // 1/split of the work each; the smallest such time wins (at least 8 slabs
-  // per split), the smaller split on a tie
+  // split K across CTAs to balance the waves: the time is about
+  // ceil(tiles * split / SMs) CTA-slots of 1/split of the work each; the
+  // smallest such time wins (at least 8 slabs per split), the smaller split
+  // on a tie
   int split = 1;
-  if (a.y16 == nullptr) {
+  {
     double best = 1e30;
     for (int sp = 1; sp <= 8 && nslab / sp >= 8; ++sp) {
       const double t = (double)((tiles * sp + sms - 1) / sms) / sp;
@@ -473,12 +494,28 @@ static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s
     --split;
     a.split = split;
   }
-  if (split > 1) {
-    e = cudaMemsetAsync(a.y, 0, (size_t)a.M * a.N * sizeof(float), s);
+  a.part = nullptr;
+  const int64_t total = (int64_t)a.M * a.N;
+  const bool atomics = split == 2 && a.y16 == nullptr;
+  if (atomics) {
+    e = cudaMemsetAsync(a.y, 0, (size_t)total * sizeof(float), s);
+    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  } else if (split > 1) {
+    // stream-ordered scratch for the partial tiles (from the device's
+    // default memory pool; freed on the stream after the reduction)
+    e = cudaMallocAsync(reinterpret_cast<void**>(&a.part), (size_t)split * total * sizeof(float), s);
     if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   }
   kern<<<dim3(tiles, split), TC_THREADS, smem, s>>>(a, tmc, tms, tmx);
   e = cudaGetLastError();
+  if (a.part) {
+    if (e == cudaSuccess) {
+      tc_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a.part, split, total, a.y, a.y16);
+      e = cudaGetLastError();
+    }
+    const cudaError_t ef = cudaFreeAsync(a.part, s);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   return QMV_OK;
 }

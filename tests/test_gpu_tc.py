@@ -40,14 +40,39 @@ def test_tensor_tiles_fp16_output():
     assert within_tol(y.cpu().float().numpy(), ref, 2e-3)
 
 
-def test_tensor_tiles_repeatable_without_split():
+@pytest.mark.parametrize("N,K", [(4096, 1024), (2048, 8192), (28672, 4096)])
+def test_tensor_tiles_repeatable(N, K):
+    """split-K partials are added in split order by a second kernel: the same
+    call gives the same bits every time (16 to 224 row tiles, splits 1 to 8)"""
     q = qmv()
-    m = Mat("tc_rep", 4096, 1024, 2, 32)          # 32 row tiles: no split
-    x, _, _ = acts("tc_rep", 128, 1024)
-    a = q.qmv_chunk_gemm(m.pack, to_dev(x))
-    b = q.qmv_chunk_gemm(m.pack, to_dev(x))
+    m = Mat(f"tc_rep{N}x{K}", N, K, 2, 32)
+    x, _, _ = acts(f"tc_rep{N}", 128, K)
+    xd = to_dev(x)
+    ys = [q.qmv_chunk_gemm(m.pack, xd) for _ in range(3)]
     torch.cuda.synchronize()
-    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    for y in ys[1:]:
+        assert torch.equal(y.view(torch.int32), ys[0].view(torch.int32))
+    assert q.qmv_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("M", [64, 128])
+def test_tensor_tiles_split_fp16_is_rne_of_fp32(M):
+    """down-projection shape (16 row tiles, split K): the fp16 output is the RNE
+    of the fp32 output, and both are within tolerance of the oracle"""
+    q = qmv()
+    N, K = 2048, 8192
+    m = Mat("tc_split16", N, K, 2, 32)
+    x, _, _ = acts(f"tc_split16m{M}", M, K)
+    xd = to_dev(x)
+    y = q.qmv_chunk_gemm(m.pack, xd, mode=q.QMV_FAST)
+    y16 = q.qmv_chunk_gemm(m.pack, xd, y_dtype=q.QMV_F16, mode=q.QMV_FAST)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy()
+    assert np.array_equal(y16.cpu().numpy().view(np.uint16), oracle.f32_to_f16(got))
+    rows = np.arange(0, N, 7)
+    codes, scales = m.host(rows)
+    ref = oracle.gemv(codes, scales, 32, x)
+    assert within_tol(got[:, rows], ref), max_rel_err(got[:, rows], ref)
 
 
 @pytest.mark.parametrize("bits,M", [(4, 64), (8, 40), (2, 48)])
