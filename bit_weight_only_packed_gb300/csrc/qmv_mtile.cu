@@ -1,5 +1,5 @@
 // qmv_mtile.cu -- M-column tiles on the bulk-copy pipeline (M >= 2 token
-// columns, K a multiple of 256, no fused prologue).
+// columns, K a multiple of 256).
 //
 // What they compute ("raw-metal-loop-playbook", prefill-regimes table: keep
 // each output scalar's K-dot in the single-token accumulation order and stage
@@ -24,6 +24,12 @@
 //     columns of U rows); the block results go to one of two fold buffers,
 //     and after its next segment's item each compute thread folds its
 //     (row, column) accumulators over the previous segment's blocks, in order.
+// With the fused residual-add + RMSNorm prologue, a small kernel first forms
+// each column's h = fp16(x + r) (stored to h_out), its sum of squares in the
+// oracle's order and the normalised fp16 activations y = fp16((h*inv)*gamma)
+// into a stream-ordered scratch, once per column instead of once per row
+// tile; the tiles then run on that y, which is what the fused definition
+// feeds the matvec.
 // The roles meet only on mbarriers (stage full/empty, table full/empty, fold
 // buffer full/empty), so a slow warp delays the others by its lag, not by a
 // CTA-wide barrier per segment.  Every wait is bounded; a wait that runs out
@@ -32,6 +38,7 @@
 #include <cuda.h>
 
 #include "qmv_pipe.cuh"
+#include "qmv_prologue.cuh"
 
 namespace qmv {
 
@@ -495,6 +502,46 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
 
 }  // namespace
 
+namespace {
+
+// The fused prologue for M >= 2 columns, one CTA per column: block sums of
+// squares of h (serial inside each 32-element block; h stored to h_out),
+// their serial sum, inv = 1/sqrt(ss/K + eps) in IEEE fp32 steps, and
+// yn = fp16((h * inv) * gamma).
+__global__ void __launch_bounds__(256) rms_prologue_kernel(GemvArgs a, __half* yn) {
+  extern __shared__ float bsum[];   // K/32 block sums
+  __shared__ float inv_sh;
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // x and r may come from the previous kernel, h_out may still be read by it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int K = a.K, NB = K / 32, m = blockIdx.x;
+  const __half* x = a.x + (int64_t)m * K;
+  const __half* r = a.r + (int64_t)m * K;
+  __half* h_out = a.h_out ? a.h_out + (int64_t)m * K : nullptr;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) bsum[b] = block_sumsq(x, r, 32 * b, h_out);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float ss = 0.0f;
+    for (int b = 0; b < NB; ++b) ss = __fadd_rn(ss, bsum[b]);
+    inv_sh = rms_inv(ss, K, a.eps);
+  }
+  __syncthreads();
+  const float inv = inv_sh;
+  for (int k = 8 * threadIdx.x; k < K; k += 8 * blockDim.x) {
+    const uint4 xv = ldg16(reinterpret_cast<const uint4*>(x + k));
+    const uint4 rv = ldg16(reinterpret_cast<const uint4*>(r + k));
+    const uint4 gv = ldg16(reinterpret_cast<const uint4*>(a.gamma + k));
+    uint16_t yy[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) yy[e] = __half_as_ushort(norm_h(add_h(h_of(xv, e), h_of(rv, e)), inv, h_of(gv, e)));
+    uint4 out;
+    memcpy(&out, yy, 16);
+    *reinterpret_cast<uint4*>(yn + (int64_t)m * K + k) = out;
+  }
+}
+
+}  // namespace
+
 // ------------------------------------------------------------- launcher --
 
 int read_mt_error(int clear, int* out) {
@@ -591,9 +638,61 @@ int mt_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
 
 }  // namespace
 
+static int launch_mtile_plain(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+
 int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
-  if (a.fused || a.M < 2 || a.K % 256 != 0 || a.gather_rows || a.amax_ws) return QMV_ERR_UNSUPPORTED;
+  if (a.M < 2 || a.K % 256 != 0 || a.gather_rows || a.amax_ws) return QMV_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(a.x) & 15u) != 0) return QMV_ERR_UNSUPPORTED;
+  if (!a.fused) return launch_mtile_plain(a, bits, s, err);
+  // fused prologue: the normalised activations into a stream-ordered scratch
+  // (the device's default memory pool), then the plain tiles on them
+  __half* yn = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&yn), (size_t)a.M * a.K * sizeof(__half), s);
+  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  const size_t psm = (size_t)(a.K / 32) * sizeof(float);
+  if (psm > 48 * 1024) {
+    e = cudaFuncSetAttribute(rms_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
+  }
+  if (e == cudaSuccess) {
+    if (pdl_enabled()) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.gridDim = dim3(a.M);
+      cfg.blockDim = dim3(256);
+      cfg.dynamicSmemBytes = psm;
+      cfg.stream = s;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, rms_prologue_kernel, a, yn);
+    } else {
+      rms_prologue_kernel<<<a.M, 256, psm, s>>>(a, yn);
+      e = cudaGetLastError();
+    }
+  }
+  int rc = QMV_OK;
+  if (e != cudaSuccess) {
+    *err = e;
+    rc = QMV_ERR_CUDA;
+  } else {
+    GemvArgs b = a;
+    b.x = yn;
+    b.fused = 0;
+    b.r = nullptr;
+    b.gamma = nullptr;
+    b.h_out = nullptr;
+    rc = launch_mtile_plain(b, bits, s, err);
+  }
+  const cudaError_t ef = cudaFreeAsync(yn, s);
+  if (rc == QMV_OK && ef != cudaSuccess) {
+    *err = ef;
+    rc = QMV_ERR_CUDA;
+  }
+  return rc;
+}
+
+static int launch_mtile_plain(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
   if (a.folded) {
     switch (bits) {
       case 2: return mt_bits<2, true>(a, s, err);

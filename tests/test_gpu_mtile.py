@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (Mat, acts, bits_equal, first_diff, max_rel_err, sample_rows, to_dev,
+from gpu_util import (EPS, Mat, acts, bits_equal, first_diff, max_rel_err, sample_rows, to_dev,
                       within_tol, qmv)
 
 pytestmark = pytest.mark.gpu
@@ -109,4 +109,33 @@ def test_mtile_full_size_sampled(name, N, K, M):
     assert bits_equal(gf[0], y1[0].cpu().numpy()[0])
     assert bits_equal(gf[M - 1], y1[1].cpu().numpy()[0])
     assert within_tol(gf[:, rows], ref), max_rel_err(gf[:, rows], ref)
+    assert q.qmv_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("N,K,bits,group,M", [(1000, 2048, 2, 32, 16), (333, 2304, 4, 32, 5),
+                                              (130, 1024, 2, 1024, 8), (200, 5376, 8, 32, 3),
+                                              (4100, 4096, 2, 32, 32)])
+def test_mtile_fused_prologue(N, K, bits, group, M):
+    """fused residual-add + RMSNorm before the tiles: h bit-exact, the exact
+    mode bit-exact against the oracle, and every fast-mode column equal to the
+    fused fast M = 1 result for that column"""
+    q = qmv()
+    m = Mat(f"mfu{N}x{K}b{bits}g{group}", N, K, bits, group)
+    x, r, g = acts(f"mfu{N}x{K}m{M}", M, K, outliers=(K == 5376))
+    xd, rd, gd = to_dev(x), to_dev(r), to_dev(g)
+    h = torch.empty(M, K, dtype=torch.float16, device="cuda")
+    ye = q.qmv_fused_rmsnorm_gemv(m.pack, xd, rd, gd, EPS, h_out=h, mode=q.QMV_EXACT)
+    yf = q.qmv_fused_rmsnorm_gemv(m.pack, xd, rd, gd, EPS, mode=q.QMV_FAST)
+    y1 = [q.qmv_fused_rmsnorm_gemv(m.pack, xd[i:i + 1].contiguous(), rd[i:i + 1].contiguous(), gd, EPS,
+                                   mode=q.QMV_FAST) for i in range(M)]
+    torch.cuda.synchronize()
+    codes, scales = m.host()
+    h_ref, _, ref = oracle.fused_rmsnorm_gemv(codes, scales, group, x, r, g, EPS)
+    assert np.array_equal(h.cpu().numpy().view(np.uint16), h_ref)
+    got = ye.cpu().numpy()
+    assert bits_equal(got, ref), first_diff(got, ref)
+    gf = yf.cpu().numpy()
+    for i in range(M):
+        assert bits_equal(gf[i], y1[i].cpu().numpy()[0]), i
+    assert within_tol(gf, ref), max_rel_err(gf, ref)
     assert q.qmv_device_error(clear=True) == 0
