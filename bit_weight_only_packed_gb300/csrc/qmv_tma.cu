@@ -479,6 +479,11 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
         continue;
       }
       int score = occ * (P.Tc / 32) * 64 + P.R;
+      // int4 is bound by the activation-table loads, which four rows per lane
+      // halve: on large int4 matrices that beats a second CTA per SM (one
+      // CTA of 224 compute threads at U = 4 against two of 256 at U = 2 on
+      // the 262144 x 5376 lm_head: 4.82 against 4.24 TB/s)
+      if (BITS == 4 && U == 4) score += 16 * 64;
       if ((int64_t)Pg.ngroups < 3LL * occ * sms && U > 2) score -= 64 * 64;   // balance
       if (score > best_score) {
         best_score = score;
