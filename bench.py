@@ -232,32 +232,15 @@ def chain_layers(qmv, layers, b, n):
     return ch
 
 
-def prefill_layers(qmv, layers, dev, stream, M, reps):
-    """The layer's four matrices as prefill chunks of M tokens (qmv_chunk_gemm,
-    fast mode, fp16 outputs), rotating over the resident layers: M = 16 runs the
-    K-order-fixed CUDA-core tiles (every column equal to the M = 1 result), M =
-    128 the tensor-core tiles for the int2 matrices and the CUDA-core tiles for
-    int4.  Returns (ms per layer, tokens/s, TFLOP/s)."""
+def _graph_time(stream, build, reps):
+    """Capture build() once as a CUDA graph, replay it reps times; ms per replay."""
     import torch
-
-    import synth
-    xs = {K: torch.from_numpy(synth.normal_f16(SEED, f"bench.prefill{M}.{K}", (M, K))).to(dev)
-          for K in sorted({K for _, _, K, _, _, _ in LAYER})}
-    ys = {name: torch.empty(M, N, dtype=torch.float16, device=dev) for name, N, *_ in LAYER}
-
-    def run(li):
-        for name, N, K, *_ in LAYER:
-            qmv.qmv_chunk_gemm(layers[li][name], xs[K], y=ys[name], y_dtype=qmv.QMV_F16,
-                               mode=qmv.QMV_FAST, stream=stream)
-
-    L = len(layers)
     with torch.cuda.stream(stream):
-        run(0)
+        build()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for li in range(L):
-            run(li)
+        build()
     with torch.cuda.stream(stream):
         g.replay()
     torch.cuda.synchronize()
@@ -269,9 +252,112 @@ def prefill_layers(qmv, layers, dev, stream, M, reps):
             g.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    ms = reduce_max(e0.elapsed_time(e1)) / (reps * L)
-    flops = 2.0 * M * sum(N * K for _, N, K, *_ in LAYER)
-    return ms, M / (ms * 1e-3), flops / (ms * 1e-3) / 1e12
+    return reduce_max(e0.elapsed_time(e1)) / reps
+
+
+# Chunked-prefill sweep on the int2 FFN at d_model 4096: gate/up (two
+# 14336 x 4096 matrices as one pack) and down 4096 x 14336, group 32.
+FFN4 = [("gateup", 2 * 14336, 4096), ("down", 4096, 14336)]
+FFN4_MS = (1, 4, 8, 16, 64, 128)
+
+
+def prefill_sweep(qmv, dev, stream, copies=4, reps=8):
+    """The FFN's two matrices as chunks of M tokens (qmv_chunk_gemm, fast
+    mode, fp16 outputs), weights rotated over `copies` resident sets (> L2):
+    M <= 16 (and 32) run the K-order-fixed CUDA-core tiles, every column equal
+    to the M = 1 result; M >= 64 the tcgen05 tensor tiles.  Per M: us per FFN,
+    tokens/s, effective GB/s, TFLOP/s."""
+    import torch
+
+    import synth
+    sets = []
+    for c in range(copies):
+        st = {}
+        for name, N, K in FFN4:
+            codes = synth.codes(SEED, f"ffn4.{c}.{name}", N, K, 2, device=dev)
+            scales = synth.scales(SEED, f"ffn4.{c}.{name}", N, K // 32, device=dev)
+            st[name] = qmv.Pack(N, K, 2, 32).pack_weights(codes, scales)
+            del codes, scales
+        sets.append(st)
+    nbytes = sum(packed_bytes(N, K, 2, 32) for _, N, K in FFN4)
+    flop1 = 2.0 * sum(N * K for _, N, K in FFN4)
+    out = {}
+    for M in FFN4_MS:
+        xs = {K: torch.from_numpy(synth.normal_f16(SEED, f"bench.ffn4.{M}.{K}", (M, K))).to(dev)
+              for _, _, K in FFN4}
+        ys = {name: torch.empty(M, N, dtype=torch.float16, device=dev) for name, N, _ in FFN4}
+
+        def build():
+            for st in sets:
+                for name, N, K in FFN4:
+                    qmv.qmv_chunk_gemm(st[name], xs[K], y=ys[name], y_dtype=qmv.QMV_F16,
+                                       mode=qmv.QMV_FAST, stream=stream)
+
+        ms = _graph_time(stream, build, reps) / copies
+        out[f"M{M}"] = {"us_per_ffn": round(ms * 1e3, 2), "tok_per_s": round(M / (ms * 1e-3), 1),
+                        "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                        "tflops": round(M * flop1 / (ms * 1e-3) / 1e12, 2)}
+    del sets
+    return out, nbytes
+
+
+# One full decode token, M = 1: 30 layers shaped as the decode layer with d_ff
+# 16384, each followed by an int8 per-row-scaled 2048 x 2048 embedding
+# projection, then the int2 lm_head 262144 x 2048.
+TOKEN_LAYERS = 30
+TOKEN_LAYER = [("qkv", 2560, D_MODEL, 4, 32, True), ("o", D_MODEL, D_MODEL, 4, 32, False),
+               ("gateup", 2 * 16384, D_MODEL, 2, 32, True), ("down", D_MODEL, 16384, 2, 32, False),
+               ("emb", D_MODEL, D_MODEL, 8, D_MODEL, False)]
+LM_HEAD = ("lm_head", 262144, D_MODEL, 2, 32)
+
+
+def token_chain(qmv, dev, stream, reps=4):
+    """One decode token through the whole chain (5 matvecs a layer x 30 + the
+    lm_head), each matvec reading the previous one's output, as one CUDA graph
+    with programmatic dependent launch.  Returns (ms per token, packed bytes
+    per token)."""
+    import torch
+
+    import synth
+    layers = []
+    for li in range(TOKEN_LAYERS):
+        lay = {}
+        for name, N, K, bits, group, _ in TOKEN_LAYER:
+            codes = synth.codes(SEED, f"tok.L{li}.{name}", N, K, bits, device=dev)
+            scales = synth.scales(SEED, f"tok.L{li}.{name}", N, K // group, device=dev)
+            lay[name] = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
+            del codes, scales
+        layers.append(lay)
+    name, N, K, bits, group = LM_HEAD
+    codes = synth.codes(SEED, "tok.lm_head", N, K, bits, device=dev)
+    scales = synth.scales(SEED, "tok.lm_head", N, K // group, device=dev)
+    head = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
+    del codes, scales
+    nbytes = TOKEN_LAYERS * sum(packed_bytes(N, K, b, g) for _, N, K, b, g, _ in TOKEN_LAYER) + \
+        packed_bytes(N, K, bits, group)
+    f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
+    x = torch.from_numpy(synth.normal_f16(SEED, "tok.x", (1, D_MODEL))).to(dev)
+    r = torch.from_numpy(synth.normal_f16(SEED, "tok.r", (1, D_MODEL))).to(dev)
+    g1 = torch.from_numpy(synth.normal_f16(SEED, "tok.g1", (D_MODEL,), mean=1.0, std=0.1)).to(dev)
+    g2 = torch.from_numpy(synth.normal_f16(SEED, "tok.g2", (D_MODEL,), mean=1.0, std=0.1)).to(dev)
+    h, yq, yo, ygu, yd = f16(D_MODEL), f16(2560), f16(D_MODEL), f16(2 * 16384), f16(D_MODEL)
+    logits = torch.empty(1, N, dtype=torch.float32, device=dev)
+
+    def build():
+        for lay in layers:
+            qmv.qmv_fused_rmsnorm_gemv(lay["qkv"], x, r, g1, 1e-6, h_out=h, y=yq, y_dtype=qmv.QMV_F16,
+                                       mode=qmv.QMV_FAST, stream=stream)
+            qmv.qmv_gemv(lay["o"], yq[:, :D_MODEL], y=yo, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
+            qmv.qmv_fused_rmsnorm_gemv(lay["gateup"], yo, h, g2, 1e-6, h_out=r, y=ygu, y_dtype=qmv.QMV_F16,
+                                       mode=qmv.QMV_FAST, stream=stream)
+            qmv.qmv_gemv(lay["down"], ygu[:, :16384], y=yd, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST,
+                         stream=stream)
+            qmv.qmv_gemv(lay["emb"], yd, y=x, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
+        qmv.qmv_gemv(head, x, y=logits, mode=qmv.QMV_FAST, stream=stream)
+
+    ms = _graph_time(stream, build, reps)
+    del layers, head
+    return ms, nbytes
 
 
 def gpu_arm(args, rank, world, local):
@@ -404,13 +490,11 @@ def gpu_arm(args, rank, world, local):
     chain_info = ch.info()
     ch.close()
 
-    # ---- the same layers as prefill chunks (a9 / a10 rows) ----
-    prefill = {}
-    for M in (16, 128):
-        p_ms, p_tok, p_tf = prefill_layers(qmv, layers, dev, stream, M, max(1, K // (4 * L)))
-        prefill[f"M{M}"] = {"ms_per_layer": round(p_ms, 5), "tok_per_s": round(world * p_tok, 1),
-                            "tflops": round(world * p_tf, 2),
-                            "gbs": round(world * LAYER_BYTES / (p_ms * 1e-3) / 1e9, 1)}
+    # ---- the other configurations, outside the timed region ----
+    tok_ms, tok_bytes = token_chain(qmv, dev, stream)
+    torch.cuda.empty_cache()
+    prefill, ffn_bytes = prefill_sweep(qmv, dev, stream)
+    torch.cuda.empty_cache()
 
     peak, peak_kind = peaks()
     gbs = world * LAYER_BYTES * K / (ms_max * 1e-3) / 1e9
@@ -452,10 +536,17 @@ def gpu_arm(args, rank, world, local):
                   "grid_barriers": chain_info["barriers"],
                   "note": "same dependent layers as one persistent cooperative launch (qmv_chain_run); "
                           "the headline value uses CUDA graphs with programmatic dependent launch"},
-        "prefill": dict(prefill, note="the layer's four matrices as prefill chunks (qmv_chunk_gemm, "
-                        "fast mode): M=16 on the K-order-fixed CUDA-core tiles (each column equal to "
-                        "M=1), M=128 on tcgen05 tensor tiles (int2) and CUDA-core tiles (int4); "
-                        "weights rotated over the resident layers"),
+        "token": {"workload": "one decode token, M=1: 30 layers (fused RMSNorm+qkv int4 2560x2048, o int4 "
+                              "2048x2048, fused RMSNorm+gate/up int2 32768x2048, down int2 2048x16384, "
+                              "int8 per-row embedding projection 2048x2048) + int2 lm_head 262144x2048",
+                  "bytes_per_token": tok_bytes, "ms_per_token": round(tok_ms, 4),
+                  "tok_per_s": round(world * 1e3 / tok_ms, 1),
+                  "gbs": round(world * tok_bytes / (tok_ms * 1e-3) / 1e9, 1),
+                  "launches_per_token": 5 * TOKEN_LAYERS + 1},
+        "prefill": dict(prefill, workload="chunked prefill on the int2 FFN, d_model 4096: gate/up "
+                        "28672x4096 + down 4096x14336 (bytes per FFN %d), qmv_chunk_gemm fast mode; "
+                        "M<=16 on the K-order-fixed CUDA-core tiles (each column equal to M=1), M>=64 on "
+                        "tcgen05 tensor tiles; 4 weight sets rotated (> L2)" % ffn_bytes),
     }
     return out
 
