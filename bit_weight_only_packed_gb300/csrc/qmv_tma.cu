@@ -451,10 +451,15 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   const int sms = dev_info().sms;
   TmaPlan best;
   int best_score = -1;
-  // small matrices (fewer than two full groups per CTA slot): the one-row-
-  // per-thread plan of ~512 compute threads halves the group (and a
-  // thread's serial work) without shrinking the CTA, whose size sets the
-  // prologue's speed; it is taken when its busiest slot has less to do
+  // small matrices (fewer than two full groups per CTA slot): a plan with
+  // half-size groups (16 rows) -- one row per thread on 512 compute threads,
+  // or, when K spans six or more segments, two rows per thread on 256 --
+  // spreads the rows over more CTAs; it is taken when its busiest slot has
+  // less to do.  Measured under graphs with programmatic dependent launch:
+  // two rows per thread amortise each of many stages better (down
+  // 2048x16384 int2 in a 30-layer token: 977 against 928 tok/s for the
+  // token), while with up to four segments the 512-thread CTA is faster
+  // (down 2048x8192 int2 in the decode layer: 22.75 against 23.65 us)
   TmaPlan small;
   int64_t small_cost = -1, best_slots = 1;
   for (int tc : {256, 512}) {
@@ -471,12 +476,12 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
       const TmaPlan Pg = gather_groups(P);
       const int64_t slots = (int64_t)occ * sms;
       const int64_t cost = ((Pg.ngroups + slots - 1) / slots) * (16 + P.R);
-      if (U == 1) {
-        if (small_cost < 0 || cost < small_cost) {
+      if (U == 1 || (U == 2 && tc == 256 && P.R <= 16 && P.NSEG >= 6)) {
+        if (small_cost < 0 || cost < small_cost || (cost == small_cost && U == 2)) {
           small_cost = cost;
           small = P;
         }
-        continue;
+        if (U == 1) continue;
       }
       int score = occ * (P.Tc / 32) * 64 + P.R;
       // int4 is bound by the activation-table loads, which four rows per lane
