@@ -475,12 +475,17 @@ static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s
   // split K across CTAs to balance the waves: the time is about
   // ceil(tiles * split / SMs) CTA-slots of 1/split of the work each; the
   // smallest such time wins (at least 8 slabs per split), the smaller split
-  // on a tie
+  // on a tie.  A split that needs the scratch and the reduction kernel (fp16
+  // output, or more than two splits) must save a third of the time: the
+  // partial tiles' round trip costs about 15 us on a 28672 x 4096 M = 128
+  // tile set (two splits, fp16: 94 us against 79 us for fp32 atomics)
   int split = 1;
   {
     double best = 1e30;
     for (int sp = 1; sp <= 8 && nslab / sp >= 8; ++sp) {
-      const double t = (double)((tiles * sp + sms - 1) / sms) / sp;
+      double t = (double)((tiles * sp + sms - 1) / sms) / sp;
+      const bool scratch = sp > 1 && (sp > 2 || a.y16 != nullptr);
+      if (scratch) t *= 1.5;
       if (t < best - 1e-9) {
         best = t;
         split = sp;
