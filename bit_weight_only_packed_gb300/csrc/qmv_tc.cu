@@ -15,18 +15,20 @@
 // which is order-independent for two terms (0 + a + b == 0 + b + a); otherwise
 // each split stores its partial tile to a stream-ordered fp32 scratch and a
 // second kernel adds the splits in split order, so the result never depends
-// on CTA timing).  Roles:
+// on CTA timing).  A pipeline stage carries KSUB 64-code slabs (4 for MT =
+// 64, 2 for MT = 128): one hand-off between the roles per 64*KSUB codes.
+// Roles:
 //   warp 8 (one thread): TMA of the packed codes and scales of the tile, 4
-//     K-slabs (256 codes) at a time, into a ring of 4 raw stages (16 slabs of
-//     prefetch).
-//   warp 10 (one thread): TMA of the activation tile of each 64-wide K slab
-//     straight into the MMA operand stage, with a 128-byte-swizzle tensor map
-//     (the K-major layout the MMA reads).
+//     K-slabs (256 codes) at a time, into a ring of raw stages.
+//   warp 10 (one thread): TMA of the activation sub-tiles of each stage's
+//     slabs straight into the MMA operand stage, with a 128-byte-swizzle
+//     tensor map (the K-major layout the MMA reads).
 //   warps 0..7: decode.  Threads r and 128 + r turn the two 32-code blocks of
-//     row r of a slab into fp16 weights w = v*s (half2 magic decode,
+//     row r of each slab into fp16 weights w = v*s (half2 magic decode,
 //     re-paired into natural k order) and write them into the stage's
-//     128-byte-swizzled K-major A tile.  At the end they are the epilogue:
-//     tcgen05.ld of their TMEM lane quarter, half of the tile's columns each.
+//     128-byte-swizzled K-major A sub-tiles.  At the end they are the
+//     epilogue: tcgen05.ld of their TMEM lane quarter, half of the tile's
+//     columns each.
 //   warp 9 (one thread): allocates the accumulator in tensor memory and issues
 //     tcgen05.mma (M=128, N=MT, K=16; four per slab), releasing each stage with
 //     tcgen05.commit on its mbarrier.
@@ -96,15 +98,8 @@ __device__ __noinline__ void tc_drain(uint64_t* b, uint32_t parity) {
   atomicCAS(&g_tc_error, 0, ERR_TC_TIMEOUT);
 }
 
-__device__ __forceinline__ void tc_tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// The same copy with an L2 cache policy (from createpolicy): the streamed
+// A 2-D tensor copy global -> shared with an L2 cache policy (from
+// createpolicy): the streamed
 // weights are marked evict-first and the activation tiles, which every row
 // tile re-reads, evict-last, so the weight stream does not push the
 // activations out of L2.
@@ -158,13 +153,19 @@ struct TcArgs {
   int split;               // gridDim.y
 };
 
-template <int MT, int NST, int NRAW>
+// KSUB 64-code slabs per pipeline stage: each stage holds KSUB weight
+// sub-tiles (128 rows x 64 fp16 each) and KSUB activation sub-tiles (MT x 64
+// fp16 each), so the roles hand a stage over once per 64*KSUB codes.
+template <int MT, int NST, int NRAW, int KSUB>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(TcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_x) {
-  constexpr int A_BYTES = 128 * 128;              // 128 rows x 64 fp16
-  constexpr int B_BYTES = MT * 128;               // MT tokens x 64 fp16
+  constexpr int A_SUB = 128 * 128;                // 128 rows x 64 fp16
+  constexpr int B_SUB = MT * 128;                 // MT tokens x 64 fp16
+  constexpr int A_BYTES = KSUB * A_SUB;
+  constexpr int B_BYTES = KSUB * B_SUB;
   constexpr int STAGE = A_BYTES + B_BYTES;
+  static_assert(RS % KSUB == 0, "a stage's slabs come from one raw stage");
   constexpr uint32_t IDESC = (1u << 4)               // D = f32
                              | ((uint32_t)(MT >> 3) << 17)  // N
                              | ((uint32_t)(128 >> 4) << 24);  // M
@@ -187,7 +188,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * 128;
   const int slab0 = blockIdx.y * a.slabs_per_split;
-  const int nslab = min(a.slabs_per_split, a.K / 64 - slab0);
+  const int nslab = min(a.slabs_per_split, a.K / 64 - slab0);   // a multiple of RS
+  const int nstage = nslab / KSUB;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -237,11 +239,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_last();
       int issued = 0;
-      for (int i = 0; i < nslab; ++i) {
+      for (int i = 0; i < nstage; ++i) {
         const int s = i % NST;
         if (i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f)) break;
         tc_mbar_arrive_tx(&b_full[s], B_BYTES);
-        tc_tma2d_hint(tiles + s * STAGE + A_BYTES, &tm_x, (slab0 + i) * 64, 0, &b_full[s], pol);
+#pragma unroll
+        for (int u = 0; u < KSUB; ++u)
+          tc_tma2d_hint(tiles + s * STAGE + A_BYTES + u * B_SUB, &tm_x, (slab0 + i * KSUB + u) * 64, 0,
+                        &b_full[s], pol);
         ++issued;
       }
       for (int i = (issued > NST ? issued - NST : 0); i < issued; ++i)
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == W_MMA) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      for (int i = 0; i < nslab; ++i) {
+      for (int i = 0; i < nstage; ++i) {
         const int s = i % NST;
         if (!tc_wait(&a_full[s], (i / NST) & 1, abort_f)) break;
         if (!tc_wait(&b_full[s], (i / NST) & 1, abort_f)) break;
@@ -258,9 +263,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t abase = smem_u32(tiles + s * STAGE);
         const uint32_t bbase = abase + A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = sw128_desc(abase + 32 * kk);
-          const uint64_t bd = sw128_desc(bbase + 32 * kk);
+        for (int kk = 0; kk < 4 * KSUB; ++kk) {
+          const uint64_t ad = sw128_desc(abase + (kk >> 2) * A_SUB + 32 * (kk & 3));
+          const uint64_t bd = sw128_desc(bbase + (kk >> 2) * B_SUB + 32 * (kk & 3));
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
           asm volatile(
               "{\n\t.reg .pred p;\n\t"
@@ -286,50 +291,61 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t prs = a.perrow && n0 + row < a.N
                              ? (uint32_t)__half_as_ushort(__ldg(a.scales + n0 + row))
                              : 0u;
-    for (int i = 0; i < nslab; ++i) {
-      const int j = i / RS, rr = j % NRAW, sub = i % RS;
+    for (int i = 0; i < nstage; ++i) {
       const int s = i % NST;
-      if (sub == 0 && !tc_wait(&raw_full[rr], (j / NRAW) & 1, abort_f)) break;
       if (i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f)) break;
-      const unsigned char* rb = rawbuf + rr * RAW_BYTES;
-      const uint2 cw = *reinterpret_cast<const uint2*>(rb + row * (RS * 16) + sub * 16 + blk * 8);
-      uint32_t sb = prs;
-      if (!a.perrow)
-        sb = *reinterpret_cast<const uint16_t*>(rb + RAW_CODES + row * (RS * 4) + sub * 4 + blk * 2);
-      const __half2 s2 = u32_as_h2(sb | (sb << 16));
-      unsigned char* A = tiles + s * STAGE;
-      const uint32_t words[2] = {cw.x, cw.y};
-#pragma unroll
-      for (int wj = 0; wj < 2; ++wj) {
-        const int wi = 2 * blk + wj;
-        __half2 vp[8];
-        decode_word<2>(words[wj], vp);   // vp[i] = (v_i, v_{i+8})
-        uint32_t o[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // natural order: (v_2q, v_2q+1) and (v_8+2q, v_9+2q)
-          const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&vp[2 * q]);
-          const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&vp[2 * q + 1]);
-          const __half2 lo = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x5410)), s2);   // exact
-          const __half2 hi = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x7632)), s2);
-          o[q] = *reinterpret_cast<const uint32_t*>(&lo);
-          o[4 + q] = *reinterpret_cast<const uint32_t*>(&hi);
+      bool ok = true;
+#pragma unroll 1
+      for (int u = 0; u < KSUB; ++u) {
+        const int sl = i * KSUB + u;   // slab
+        const int j = sl / RS, rr = j % NRAW, sub = sl % RS;
+        if (sub == 0 && !tc_wait(&raw_full[rr], (j / NRAW) & 1, abort_f)) {
+          ok = false;
+          break;
         }
-        *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+        const unsigned char* rb = rawbuf + rr * RAW_BYTES;
+        const uint2 cw = *reinterpret_cast<const uint2*>(rb + row * (RS * 16) + sub * 16 + blk * 8);
+        uint32_t sb = prs;
+        if (!a.perrow)
+          sb = *reinterpret_cast<const uint16_t*>(rb + RAW_CODES + row * (RS * 4) + sub * 4 + blk * 2);
+        const __half2 s2 = u32_as_h2(sb | (sb << 16));
+        unsigned char* A = tiles + s * STAGE + u * A_SUB;
+        const uint32_t words[2] = {cw.x, cw.y};
+#pragma unroll
+        for (int wj = 0; wj < 2; ++wj) {
+          const int wi = 2 * blk + wj;
+          __half2 vp[8];
+          decode_word<2>(words[wj], vp);   // vp[i] = (v_i, v_{i+8})
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            // natural order: (v_2q, v_2q+1) and (v_8+2q, v_9+2q)
+            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&vp[2 * q]);
+            const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&vp[2 * q + 1]);
+            const __half2 lo = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x5410)), s2);   // exact
+            const __half2 hi = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x7632)), s2);
+            o[q] = *reinterpret_cast<const uint32_t*>(&lo);
+            o[4 + q] = *reinterpret_cast<const uint32_t*>(&hi);
+          }
+          *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
       }
+      if (!ok) break;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
         tc_mbar_arrive(&a_full[s]);
-        if (sub == RS - 1 || i == nslab - 1) tc_mbar_arrive(&raw_empty[rr]);
+        // the stage's last slab ends a raw stage (RS is a multiple of KSUB)
+        const int last = i * KSUB + KSUB - 1;
+        if (last % RS == RS - 1) tc_mbar_arrive(&raw_empty[(last / RS) % NRAW]);
       }
     }
 
     // --------------------------------------------------------- epilogue --
     // warp w reads TMEM lanes 32*(w%4) .. +31 (its lane quarter), columns of
     // its half of the tile's tokens
-    if (nslab > 0 && tc_wait(done, 0, abort_f)) {
+    if (nstage > 0 && tc_wait(done, 0, abort_f)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int q4 = warp & 3;
       const int r = 32 * q4 + lane;
@@ -438,12 +454,12 @@ bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int NST, int NRAW>
+template <int MT, int NST, int NRAW, int KSUB>
 static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s, cudaError_t* err) {
-  constexpr int STAGE = 128 * 128 + MT * 128;
+  constexpr int STAGE = KSUB * (128 * 128 + MT * 128);
   const size_t smem = 1024 + (size_t)NST * STAGE + (size_t)NRAW * RAW_BYTES + 256;
   static thread_local int set_dev = -1;
-  auto kern = tc_gemm_kernel<MT, NST, NRAW>;
+  auto kern = tc_gemm_kernel<MT, NST, NRAW, KSUB>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
@@ -542,8 +558,13 @@ int launch_tc_gemm(const GemvArgs& g, int bits, cudaStream_t s, cudaError_t* err
   const int tiles = (g.N + 127) / 128;
   // the raw ring (codes + scales, 4 slabs a stage) keeps about an HBM
   // latency of weight data in flight; the decoded stages fill the rest
-  if (g.M <= 64) return run_tc<64, 6, 6>(a, g, tiles, s, err);
-  return run_tc<128, 4, 6>(a, g, tiles, s, err);
+  // stages of several 64-code slabs: the roles' hand-offs, not the data
+  // paths, set the pace (0.46 us a slab with every copy, decode and MMA
+  // removed), so a stage carries four slabs for M <= 64 (two stages of
+  // 96 KB) and two for M = 128 (three stages of 64 KB); a two-slab raw ring
+  // keeps a code and scale copy in flight
+  if (g.M <= 64) return run_tc<64, 2, 2, 4>(a, g, tiles, s, err);
+  return run_tc<128, 3, 2, 2>(a, g, tiles, s, err);
 }
 
 }  // namespace qmv
