@@ -11,10 +11,10 @@
 // How (building blocks in qmv_pipe.cuh):
 //   * Rows are processed in groups of R rows, each in NSEG segments of K.  A
 //     producer warp moves each (group, segment) -- R rows of codes and their
-//     group-32 scales -- into a ring of NS shared-memory stages with two 2-D
-//     tensor copies completing on the stage's "full" mbarrier.  It runs ahead
-//     of the math by up to NS stages and starts before the prologue, since
-//     weights do not depend on the activations.
+//     group-32 scales -- into a ring of M1_NS shared-memory stages with two
+//     2-D tensor copies completing on the stage's "full" mbarrier.  It runs
+//     ahead of the math by up to M1_NS stages and starts before the prologue,
+//     since weights do not depend on the activations.
 //   * Compute warps: thread t owns one 64-code item (two 32-code blocks) of
 //     RP rows in parallel, U rows after another, reading the item's
 //     activations from a shared-memory table pre-scaled per bit offset.  Exact
@@ -36,15 +36,23 @@ __device__ int g_qmv_error = 0;
 
 using namespace pipe;
 
+// Copy-ring stages and fold buffers of this kernel: three of each (against
+// four stages and two fold buffers: the decode layer 923.6 -> 934.8 GB/s and
+// the int4 262144 x 5376 lm_head 4.82 -> 4.94 TB/s) -- a third fold buffer
+// lets the compute warps run two stages ahead of the fold warp, and the
+// smaller ring pays for it in shared memory.
+constexpr int M1_NS = 3, M1_TB = 3;
+static_assert(8 * (2 * M1_NS + 2 * M1_TB) <= 96, "the kernel's mbarriers end below its flags at byte 96");
+
 template <int BITS, bool PERROW, bool FUSED, bool EXACT, int U, int MAXT>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     gemv_tma_kernel(GemvArgs a, TmaPlan P, const __grid_constant__ CUtensorMap tm_codes,
                     const __grid_constant__ CUtensorMap tm_scales) {
   extern __shared__ __align__(128) unsigned char sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
-  uint64_t* empty = full + NS;
-  uint64_t* tfull = empty + NS;
-  uint64_t* tempty = tfull + 2;
+  uint64_t* empty = full + M1_NS;
+  uint64_t* tfull = empty + M1_NS;
+  uint64_t* tempty = tfull + M1_TB;
   volatile int* abort_f = reinterpret_cast<volatile int*>(sm + 96);
   float* inv_sh = reinterpret_cast<float*>(sm + 100);
   float* y2f = reinterpret_cast<float*>(sm + P.y_off);     // activation table
@@ -75,11 +83,11 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   if (threadIdx.x == 0) {
     // consumers arrive once per warp (lane 0, after __syncwarp orders the
     // lanes' shared-memory accesses before its release)
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < M1_NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], P.Tc / 32);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < M1_TB; ++b) {
       mbar_init(&tfull[b], P.Tc / 32);
       mbar_init(&tempty[b], 1);
     }
@@ -102,8 +110,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     int seg = 0;
     int64_t g = blockIdx.x;
     for (int i = 0; i < my_stages; ++i) {
-      const int s = i & (NS - 1);
-      if (i >= NS && !mbar_wait_fast(&empty[s], ((i / NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY, err)) break;
+      const int s = i % M1_NS;
+      if (i >= M1_NS && !mbar_wait_fast(&empty[s], ((i / M1_NS) - 1) & 1, abort_f, ERR_TIMEOUT_EMPTY, err)) break;
       if (*abort_f) break;
       const int64_t r0 = group_rows(a, R, g, ids_sh).phys0;
       // one box of R rows x one segment: rows past N are zero-filled, the
@@ -123,8 +131,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     }
     // let every copy this warp issued land before the CTA can exit
     if (lane == 0)
-      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-        mbar_drain(&full[j % NS], (j / NS) & 1, err);
+      for (int j = (issued > M1_NS ? issued - M1_NS : 0); j < issued; ++j)
+        mbar_drain(&full[j % M1_NS], (j / M1_NS) & 1, err);
     return;
   }
 
@@ -146,8 +154,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
     int seg = 0;
     int64_t g = blockIdx.x;
     for (int i = 0; i < my_stages; ++i) {
-      const int tb = i & 1;
-      if (!mbar_wait_fast(&tfull[tb], (i >> 1) & 1, abort_f, ERR_TIMEOUT_TFULL, err)) break;
+      const int tb = i % M1_TB;
+      if (!mbar_wait_fast(&tfull[tb], (i / M1_TB) & 1, abort_f, ERR_TIMEOUT_TFULL, err)) break;
       const GroupRows gr = group_rows(a, R, g, ids_sh);
       if (!gr.ok && lane == 0 && seg == 0) atomicCAS(err, 0, ERR_BAD_EXPERT);
       fold_stage(a, P, tbuf + (size_t)tb * R * GS, GS, lane, gr, seg, acc, a.amax_ws ? &best : nullptr);
@@ -172,10 +180,10 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 320) ? 2 : 1)
   int seg = 0;
   int64_t g = blockIdx.x;
   for (int i = 0; i < my_stages; ++i) {
-    const int s = i & (NS - 1);
-    const int tb = i & 1;
-    if (!mbar_wait_fast(&full[s], (i / NS) & 1, abort_f, ERR_TIMEOUT_FULL, err)) break;
-    if (i >= 2 && !mbar_wait_fast(&tempty[tb], ((i >> 1) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY, err)) break;
+    const int s = i % M1_NS;
+    const int tb = i % M1_TB;
+    if (!mbar_wait_fast(&full[s], (i / M1_NS) & 1, abort_f, ERR_TIMEOUT_FULL, err)) break;
+    if (i >= M1_TB && !mbar_wait_fast(&tempty[tb], ((i / M1_TB) - 1) & 1, abort_f, ERR_TIMEOUT_TEMPTY, err)) break;
     const int rows = a.gather_rows ? group_rows(a, R, g, ids_sh).rows
                                    : (int)min((int64_t)R, (int64_t)a.N - g * R);
     if (active)
@@ -223,9 +231,9 @@ static bool tma_plan(int N, int K, int bits, bool perrow, int tc_target, int U, 
   P->y_off = 128;
   P->ysum_off = P->y_off + (K / 64) * YS * 8;
   P->stage_off = (P->ysum_off + (K / 32) * 4 + 127) & ~127;
-  P->tbuf_off = tma_round16(P->stage_off + NS * P->stage_bytes);
+  P->tbuf_off = tma_round16(P->stage_off + M1_NS * P->stage_bytes);
   {
-    const int fold = 2 * P->R * (P->KS / 32 + 4) * 4;
+    const int fold = M1_TB * P->R * (P->KS / 32 + 4) * 4;
     const int bsum = (K / 32) * 4;
     P->ids_off = P->tbuf_off + tma_round16(fold > bsum ? fold : bsum);
   }
