@@ -370,7 +370,14 @@ def gpu_arm(args, rank, world, local):
     L = args.layers
     layers = build_layers(L, dev)
     hin = host_inputs()
-    b = {k: torch.from_numpy(hin[k]).to(dev) for k in ("x", "r", "g1", "g2")}
+    # x, r, g1, g2 side by side in one device buffer (views), so that an
+    # end-to-end step moves its inputs with one host->device copy and its two
+    # outputs (x, r) with one device->host copy
+    io = torch.empty(4 * D_MODEL, dtype=torch.float16, device=dev)
+    b = {k: io[i * D_MODEL:(i + 1) * D_MODEL].view(1, D_MODEL) if k in ("x", "r") else io[i * D_MODEL:(i + 1) * D_MODEL]
+         for i, k in enumerate(("x", "r", "g1", "g2"))}
+    for k in ("x", "r", "g1", "g2"):
+        b[k].copy_(torch.from_numpy(hin[k]).reshape(b[k].shape))
     f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
     b.update(h=f16(D_MODEL), y_qkv=f16(2560), y_o=f16(D_MODEL), y_gu=f16(2 * D_FF))
     K, W = args.steps, args.warmup
@@ -438,18 +445,16 @@ def gpu_arm(args, rank, world, local):
     ms_max = reduce_max(ms)
 
     # ---- end to end through the public API: pinned host -> device -> host ----
-    pin = {k: torch.from_numpy(hin[k]).pin_memory() for k in ("x", "r", "g1", "g2")}
-    outs = {k: torch.empty(b[k].shape, dtype=b[k].dtype).pin_memory() for k in ("x", "r")}
-    h2d = sum(v.numel() * v.element_size() for v in pin.values())
-    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    pin = torch.from_numpy(np.concatenate([hin[k].reshape(-1) for k in ("x", "r", "g1", "g2")])).pin_memory()
+    outs = torch.empty(2 * D_MODEL, dtype=torch.float16).pin_memory()   # x, r
+    h2d = pin.numel() * pin.element_size()
+    d2h = outs.numel() * outs.element_size()
     KE = max(3, K // 2)
 
     def e2e_step(li):
-        for k, v in pin.items():
-            b[k].copy_(v, non_blocking=True)
+        io.copy_(pin, non_blocking=True)
         run_layer(qmv, layers[li], b, stream)
-        for k, v in outs.items():
-            v.copy_(b[k], non_blocking=True)
+        outs.copy_(io[:2 * D_MODEL], non_blocking=True)
 
     # one graph per layer: the copies are memcpy nodes, run again on every replay
     g_e2e = []
