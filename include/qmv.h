@@ -17,7 +17,14 @@
  *
  * Conventions (all entry points):
  *   - Every pointer named d_* or described as "device" is a CUDA device
- *     pointer owned by the caller.  The library allocates no device memory.
+ *     pointer owned by the caller.  The library allocates no device memory of
+ *     its own, with two stream-ordered exceptions: the tensor-core tiles' split-K
+ *     partial tiles (M > 32 in QMV_FAST with int2 weights, when the K split
+ *     needs more than two splits or fp16 output) and the fused prologue's
+ *     normalised activations for M >= 2 (M x K fp16).  Both come from the
+ *     device's default memory pool with cudaMallocAsync on the call's stream
+ *     and go back with cudaFreeAsync on the same stream after use; an
+ *     allocation failure returns QMV_ERR_CUDA.
  *   - fp16 values are IEEE binary16 bit patterns (uint16_t / __half).
  *   - Matrices are row-major with no padding.  Activations are M x K (row m is
  *     column m of the matvec, i.e. token m); outputs are M x N.
