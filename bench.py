@@ -301,21 +301,21 @@ def prefill_sweep(qmv, dev, stream, copies=4, reps=8):
     return out, nbytes
 
 
-# One full decode token, M = 1: 30 layers shaped as the decode layer with d_ff
-# 16384, each followed by an int8 per-row-scaled 2048 x 2048 embedding
-# projection, then the int2 lm_head 262144 x 2048.
+# One full decode token, M = 1: the per-layer-embedding projection (one int8
+# per-row-scaled 2048 x 2048 matvec per token), 30 layers shaped as the decode
+# layer with d_ff 16384, then the int2 lm_head 262144 x 2048.
 TOKEN_LAYERS = 30
 TOKEN_LAYER = [("qkv", 2560, D_MODEL, 4, 32, True), ("o", D_MODEL, D_MODEL, 4, 32, False),
-               ("gateup", 2 * 16384, D_MODEL, 2, 32, True), ("down", D_MODEL, 16384, 2, 32, False),
-               ("emb", D_MODEL, D_MODEL, 8, D_MODEL, False)]
+               ("gateup", 2 * 16384, D_MODEL, 2, 32, True), ("down", D_MODEL, 16384, 2, 32, False)]
+PLE = ("ple", D_MODEL, D_MODEL, 8, D_MODEL)
 LM_HEAD = ("lm_head", 262144, D_MODEL, 2, 32)
 
 
 def token_chain(qmv, dev, stream, reps=4):
-    """One decode token through the whole chain (5 matvecs a layer x 30 + the
-    lm_head), each matvec reading the previous one's output, as one CUDA graph
-    with programmatic dependent launch.  Returns (ms per token, packed bytes
-    per token)."""
+    """One decode token through the whole chain (the embedding projection, 4
+    matvecs a layer x 30, the lm_head), each matvec reading the previous one's
+    output, as one CUDA graph with programmatic dependent launch.  Returns (ms
+    per token, packed bytes per token)."""
     import torch
 
     import synth
@@ -328,35 +328,39 @@ def token_chain(qmv, dev, stream, reps=4):
             lay[name] = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
             del codes, scales
         layers.append(lay)
-    name, N, K, bits, group = LM_HEAD
-    codes = synth.codes(SEED, "tok.lm_head", N, K, bits, device=dev)
-    scales = synth.scales(SEED, "tok.lm_head", N, K // group, device=dev)
-    head = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
-    del codes, scales
-    nbytes = TOKEN_LAYERS * sum(packed_bytes(N, K, b, g) for _, N, K, b, g, _ in TOKEN_LAYER) + \
-        packed_bytes(N, K, bits, group)
+    def one(spec, tag):
+        _, N, K, bits, group = spec
+        codes = synth.codes(SEED, tag, N, K, bits, device=dev)
+        scales = synth.scales(SEED, tag, N, K // group, device=dev)
+        return qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
+    ple = one(PLE, "tok.ple")
+    head = one(LM_HEAD, "tok.lm_head")
+    N = LM_HEAD[1]
+    nbytes = TOKEN_LAYERS * sum(packed_bytes(N_, K_, b, g) for _, N_, K_, b, g, _ in TOKEN_LAYER) + \
+        packed_bytes(*PLE[1:]) + packed_bytes(*LM_HEAD[1:])
     f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
     x = torch.from_numpy(synth.normal_f16(SEED, "tok.x", (1, D_MODEL))).to(dev)
     r = torch.from_numpy(synth.normal_f16(SEED, "tok.r", (1, D_MODEL))).to(dev)
     g1 = torch.from_numpy(synth.normal_f16(SEED, "tok.g1", (D_MODEL,), mean=1.0, std=0.1)).to(dev)
     g2 = torch.from_numpy(synth.normal_f16(SEED, "tok.g2", (D_MODEL,), mean=1.0, std=0.1)).to(dev)
-    h, yq, yo, ygu, yd = f16(D_MODEL), f16(2560), f16(D_MODEL), f16(2 * 16384), f16(D_MODEL)
+    e = torch.from_numpy(synth.normal_f16(SEED, "tok.embed", (1, D_MODEL))).to(dev)
+    h, yq, yo, ygu = f16(D_MODEL), f16(2560), f16(D_MODEL), f16(2 * 16384)
     logits = torch.empty(1, N, dtype=torch.float32, device=dev)
 
     def build():
+        qmv.qmv_gemv(ple, e, y=x, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
         for lay in layers:
             qmv.qmv_fused_rmsnorm_gemv(lay["qkv"], x, r, g1, 1e-6, h_out=h, y=yq, y_dtype=qmv.QMV_F16,
                                        mode=qmv.QMV_FAST, stream=stream)
             qmv.qmv_gemv(lay["o"], yq[:, :D_MODEL], y=yo, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
             qmv.qmv_fused_rmsnorm_gemv(lay["gateup"], yo, h, g2, 1e-6, h_out=r, y=ygu, y_dtype=qmv.QMV_F16,
                                        mode=qmv.QMV_FAST, stream=stream)
-            qmv.qmv_gemv(lay["down"], ygu[:, :16384], y=yd, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST,
+            qmv.qmv_gemv(lay["down"], ygu[:, :16384], y=x, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST,
                          stream=stream)
-            qmv.qmv_gemv(lay["emb"], yd, y=x, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
         qmv.qmv_gemv(head, x, y=logits, mode=qmv.QMV_FAST, stream=stream)
 
     ms = _graph_time(stream, build, reps)
-    del layers, head
+    del layers, head, ple
     return ms, nbytes
 
 
@@ -541,13 +545,14 @@ def gpu_arm(args, rank, world, local):
                   "grid_barriers": chain_info["barriers"],
                   "note": "same dependent layers as one persistent cooperative launch (qmv_chain_run); "
                           "the headline value uses CUDA graphs with programmatic dependent launch"},
-        "token": {"workload": "one decode token, M=1: 30 layers (fused RMSNorm+qkv int4 2560x2048, o int4 "
-                              "2048x2048, fused RMSNorm+gate/up int2 32768x2048, down int2 2048x16384, "
-                              "int8 per-row embedding projection 2048x2048) + int2 lm_head 262144x2048",
+        "token": {"workload": "one decode token, M=1: int8 per-row per-layer-embedding projection "
+                              "2048x2048, 30 layers (fused RMSNorm+qkv int4 2560x2048, o int4 2048x2048, "
+                              "fused RMSNorm+gate/up int2 32768x2048, down int2 2048x16384), int2 lm_head "
+                              "262144x2048",
                   "bytes_per_token": tok_bytes, "ms_per_token": round(tok_ms, 4),
                   "tok_per_s": round(world * 1e3 / tok_ms, 1),
                   "gbs": round(world * tok_bytes / (tok_ms * 1e-3) / 1e9, 1),
-                  "launches_per_token": 5 * TOKEN_LAYERS + 1},
+                  "launches_per_token": 4 * TOKEN_LAYERS + 2},
         "prefill": dict(prefill, workload="chunked prefill on the int2 FFN, d_model 4096: gate/up "
                         "28672x4096 + down 4096x14336 (bytes per FFN %d), qmv_chunk_gemm fast mode; "
                         "M<=16 on the K-order-fixed CUDA-core tiles (each column equal to M=1), M>=64 on "
