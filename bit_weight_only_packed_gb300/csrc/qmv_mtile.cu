@@ -15,15 +15,17 @@
 //   * the copy warp brings, per segment, the tile's packed codes (one or more
 //     128-byte-swizzled boxes of R rows x 128 bytes), its group-32 scales and
 //     the MC x 512 fp16 activations into a ring of stages;
-//   * two table warps turn the activations into the segment's table (the
+//   * four table warps turn the activations into the segment's table (the
 //     M = 1 pipeline's scaled fp32 pairs, the MC columns side by side) and
-//     block sums, into one of two table buffers;
+//     block sums, into one of two table buffers; one segment behind, they
+//     also fold: each thread owns one row's (row, column) accumulators and
+//     adds the previous segment's block results in block order, and stores
+//     the tile after its last segment;
 //   * compute warp w takes 64-code item w of the segment for all R rows: lane
 //     l holds rows l + 32u, decodes each code once and runs the paired-FMA
 //     chains of the MC columns (one 16-byte shared-memory broadcast serves two
-//     columns of U rows); the block results go to one of two fold buffers,
-//     and after its next segment's item each compute thread folds its
-//     (row, column) accumulators over the previous segment's blocks, in order.
+//     columns of U rows); the block results go to one of two fold buffers
+//     (one 16-byte store per row), so the compute warps only decode and FMA.
 // With the fused residual-add + RMSNorm prologue, a small kernel first forms
 // each column's h = fp16(x + r) (stored to h_out), its sum of squares in the
 // oracle's order and the normalised fp16 activations y = fp16((h*inv)*gamma)
