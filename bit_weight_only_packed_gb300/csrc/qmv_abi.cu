@@ -198,7 +198,6 @@ int qmv_fused_rmsnorm_gemv(const qmv_pack* p, int M, const void* x, const void* 
   int rc = check_common(p, M, x, y, y_dtype, mode);
   if (rc != QMV_OK) return rc;
   if (!residual || !gamma) return QMV_ERR_INVALID_ARG;
-  if (M > 32) return QMV_ERR_UNSUPPORTED;
   if (!(eps >= 0.0f)) return QMV_ERR_INVALID_ARG;
   if (!aligned(residual, 16) || !aligned(gamma, 16) || (h_out && !aligned(h_out, 16)))
     return QMV_ERR_ALIGNMENT;

@@ -155,8 +155,10 @@ QMV_API int qmv_gemv(const qmv_pack *p, int M, int N, int K, int bits, int group
  *   y16 = fp16((h * inv) * gamma); then y = matvec(y16) as qmv_gemv.
  *   x, residual  device fp16 [M][K]; gamma device fp16 [K]; 16-byte aligned.
  *   h_out        nullable device fp16 [M][K]: receives h (the next residual).
- *   M            1 .. 32.
- * Errors: as qmv_gemv; M > 32 gives QMV_ERR_UNSUPPORTED.
+ *   M            1 .. 4096; every column runs the CUDA-core kernels (the
+ *                fused prologue never takes the tensor-core tiles), each
+ *                column equal to the M = 1 result.
+ * Errors: as qmv_gemv.
  */
 QMV_API int qmv_fused_rmsnorm_gemv(const qmv_pack *p, int M, const void *x, const void *residual,
                            const void *gamma, float eps, void *h_out, void *y,

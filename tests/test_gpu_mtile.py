@@ -139,3 +139,45 @@ def test_mtile_fused_prologue(N, K, bits, group, M):
         assert bits_equal(gf[i], y1[i].cpu().numpy()[0]), i
     assert within_tol(gf, ref), max_rel_err(gf, ref)
     assert q.qmv_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("N,K,bits,group", [(150, 1024, 2, 32), (90, 320, 4, 32)])
+def test_fused_above_32_columns(N, K, bits, group):
+    """the fused prologue at M = 40: the pipelined tiles (K % 256 == 0) and the
+    plain tiles in 32-column launches (K % 256 != 0) -- h and y bit-exact
+    against the oracle in exact mode, fast columns equal to fused fast M = 1"""
+    q = qmv()
+    M = 40
+    m = Mat(f"fu40.{N}x{K}b{bits}", N, K, bits, group)
+    x, r, g = acts(f"fu40.{N}x{K}", M, K)
+    xd, rd, gd = to_dev(x), to_dev(r), to_dev(g)
+    h = torch.empty(M, K, dtype=torch.float16, device="cuda")
+    ye = q.qmv_fused_rmsnorm_gemv(m.pack, xd, rd, gd, EPS, h_out=h, mode=q.QMV_EXACT)
+    yf = q.qmv_fused_rmsnorm_gemv(m.pack, xd, rd, gd, EPS, mode=q.QMV_FAST)
+    y1 = [q.qmv_fused_rmsnorm_gemv(m.pack, xd[i:i + 1].contiguous(), rd[i:i + 1].contiguous(), gd, EPS,
+                                   mode=q.QMV_FAST) for i in (0, M - 1)]
+    torch.cuda.synchronize()
+    codes, scales = m.host()
+    h_ref, _, ref = oracle.fused_rmsnorm_gemv(codes, scales, group, x, r, g, EPS)
+    assert np.array_equal(h.cpu().numpy().view(np.uint16), h_ref)
+    assert bits_equal(ye.cpu().numpy(), ref), first_diff(ye.cpu().numpy(), ref)
+    gf = yf.cpu().numpy()
+    assert bits_equal(gf[0], y1[0].cpu().numpy()[0])
+    assert bits_equal(gf[M - 1], y1[1].cpu().numpy()[0])
+    assert within_tol(gf, ref), max_rel_err(gf, ref)
+
+
+def test_mtile_max_columns():
+    """M = 4096 (the largest chunk the ABI takes) on a small matrix: 1024 column
+    chunks of one row tile each; exact mode bit-exact against the oracle"""
+    q = qmv()
+    N, K, M = 100, 256, 4096
+    m = Mat("mtmax", N, K, 2, 32)
+    x, _, _ = acts("mtmax", M, K)
+    y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_EXACT)
+    torch.cuda.synchronize()
+    codes, scales = m.host()
+    ref = oracle.gemv(codes, scales, 32, x)
+    got = y.cpu().numpy()
+    assert bits_equal(got, ref), first_diff(got, ref)
+    assert q.qmv_device_error(clear=True) == 0
