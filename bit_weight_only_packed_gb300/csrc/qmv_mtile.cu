@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   constexpr uint32_t MASK = (1u << BITS) - 1u;
   constexpr int CPI = BITS / 2;          // 16-byte chunks per item and row
   constexpr int IPB = 8 / CPI;           // items per 128-byte box
-  static_assert(MC == 4 && (L::FC == 4 || L::FC == 2) && R * MC == 32 * MT_TW * L::FC, "tile shape");
+  static_assert(MC == 4 && (L::FC == 4 || L::FC == 2 || L::FC == 1) && R * MC == 32 * MT_TW * L::FC,
+                "tile shape");
 
   extern __shared__ unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (sa(sm_raw) & 1023u)) & 1023u);
@@ -199,16 +200,18 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
 #pragma unroll
       for (int bl = 0; bl < MT_BLOCKS; ++bl)
         if (bl < 2 * p_items) {
-          if (L::FC == 4) {
+          if constexpr (L::FC == 4) {
             const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
             v[bl][0] = f.x;
             v[bl][1] = f.y;
-            v[bl][L::FC - 2] = f.z;
-            v[bl][L::FC - 1] = f.w;
-          } else {
+            v[bl][2] = f.z;
+            v[bl][3] = f.w;
+          } else if constexpr (L::FC == 2) {
             const float2 f = *reinterpret_cast<const float2*>(tb + bl * R * MC);
             v[bl][0] = f.x;
             v[bl][1] = f.y;
+          } else {
+            v[bl][0] = tb[bl * R * MC];
           }
         }
 #pragma unroll
@@ -618,7 +621,8 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
 // rounds of tiles over the SMs, times the segments per tile, times the
 // measured cost of one segment on GB300 (about 4500 cycles for 128 rows, 2900
 // for 64: a fixed part for the copies, tables, waits and block finishes plus
-// the paired FMAs, which scale with the rows).
+// the paired FMAs, which scale with the rows; 32-row tiles are priced on the
+// same line).
 double mt_cost(int N, int M, int K, int U, int sms) {
   const int R = 32 * U;
   const int64_t tiles = (((int64_t)N + R - 1) / R) * ((M + MT_MC - 1) / MT_MC);
@@ -629,13 +633,20 @@ double mt_cost(int N, int M, int K, int U, int sms) {
 
 template <int BITS, bool FOLD>
 int mt_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
-  if constexpr (BITS == 8) {
-    return run_mt<BITS, FOLD, 2>(a, s, err);   // int8: 16 words a row, two rows per lane
-  } else {
-    const int sms = dev_info().sms;
-    if (mt_cost(a.N, a.M, a.K, 4, sms) <= mt_cost(a.N, a.M, a.K, 2, sms)) return run_mt<BITS, FOLD, 4>(a, s, err);
-    return run_mt<BITS, FOLD, 2>(a, s, err);
+  // rows per lane: 4 (not for int8: 16 words a row), 2, or 1 (32-row tiles,
+  // for matrices with too few 64-row tiles to cover the SMs), by the cost model
+  const int sms = dev_info().sms;
+  int best = 2;
+  double bc = mt_cost(a.N, a.M, a.K, 2, sms);
+  if (BITS != 8 && mt_cost(a.N, a.M, a.K, 4, sms) <= bc) {
+    best = 4;
+    bc = mt_cost(a.N, a.M, a.K, 4, sms);
   }
+  if (mt_cost(a.N, a.M, a.K, 1, sms) < bc) best = 1;
+  if (best == 1) return run_mt<BITS, FOLD, 1>(a, s, err);
+  if constexpr (BITS != 8)
+    if (best == 4) return run_mt<BITS, FOLD, 4>(a, s, err);
+  return run_mt<BITS, FOLD, 2>(a, s, err);
 }
 
 }  // namespace
