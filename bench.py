@@ -20,6 +20,13 @@ launch stream), i.e. effective GB/s; `tok_per_s_equiv` = layers per second.
 `e2e` is the same metric with the step's activations copied host->device from
 pinned memory and the outputs read back inside the timed region.
 
+Outside the timed region the line also reports: `chain` (the same layers as
+one persistent cooperative launch), `token` (one full decode token: the int8
+per-layer-embedding projection, 30 layers with d_ff 16384 and the int2
+lm_head 262144 x 2048, 1,274,941,440 bytes, 122 dependent launches in one
+graph) and `prefill` (the int2 FFN at d_model 4096 as chunks of M = 1, 4, 8,
+16, 64, 128 tokens).
+
 `--impl reference` times the CPU oracle (single-threaded C, the definition
 the GPU path is checked against) on a bounded sample of the same workload.
 """
