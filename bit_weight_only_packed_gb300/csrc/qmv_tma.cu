@@ -451,11 +451,6 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
         k.fused == key.fused && k.folded == key.folded && k.gather == key.gather && k.dev == key.dev)
       return tma_dispatch<BITS>(a, gather_groups(cache[i].p), s, err, nullptr);
   }
-  static const int tc_force = [] {
-    const char* e = getenv("QMV_TC");
-    const int v = e ? atoi(e) : 0;
-    return (v >= 128 && v <= 512) ? v : 0;
-  }();
   const int sms = dev_info().sms;
   TmaPlan best;
   int best_score = -1;
@@ -471,7 +466,6 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   TmaPlan small;
   int64_t small_cost = -1, best_slots = 1;
   for (int tc : {256, 512}) {
-    if (tc_force && tc != tc_force) continue;
     for (int U : {4, 2, 1}) {
       if (BITS == 8 && U > 2) continue;
       if (tc > 256 && U > 2) continue;
