@@ -96,6 +96,20 @@ def test_serial_order_inside_block():
     # [A, e x4, -A]: fp32 result 0 although the exact value is 2^-8
     y = [A] + [E] * 4 + [-A] + [0.0] * 26
     assert _one_row(y, [1] * 32, [1.0], 32) == 0.0
+    # [A, 0 x15, e x16]: one 32-code chain absorbs all sixteen e -> A.
+    # (two 16-code chains added would keep 16e = 2^-6: A + 2^-6.)
+    y = [A] + [0.0] * 15 + [E] * 16
+    assert _one_row(y, [1] * 32, [1.0], 32) == A
+
+
+def test_blocks_inside_a_long_group():
+    # group == K == 64 is summed as two 32-code blocks, then the block sums
+    # are added: [A, 0 x31, e x32] -> block 1 is 32e = 2^-5 exactly and
+    # A + 2^-5 is representable.  One serial chain over all 64 codes would
+    # absorb every e and give A.  With group 32 the two groups add the same way.
+    y = [A] + [0.0] * 31 + [E] * 32
+    assert _one_row(y, [1] * 64, [1.0], 64) == A + 2.0 ** -5
+    assert _one_row(y, [1] * 64, [1.0, 1.0], 32) == A + 2.0 ** -5
 
 
 def test_serial_order_over_groups():

@@ -100,3 +100,10 @@ def test_sumsq_block_order(orc):
     h = np.array([2048.0] + [2.0 ** -7] * 31 + [0.25] * 32, F16)
     assert orc.sumsq(h, order=0) == 2.0 ** 22 + 2
     assert orc.sumsq(h, order=1) == 2.0 ** 22
+    # The block is 32 values long: h16..31 = 0.25 (squares 2^-4) sit in
+    # block 0 behind h0^2 = 2^22 and are each absorbed -> 2^22.  A 16-value
+    # block would sum them first to 1 and give 2^22 + 1.
+    h = np.array([2048.0] + [0.0] * 15 + [0.25] * 16, F16)
+    assert orc.sumsq(h, order=0) == 2.0 ** 22
+    hb, yb = orc.fused_residual_rmsnorm(h, np.zeros(32, F16), np.ones(32, F16), EPS)
+    assert np.array_equal(yb[0], orc.rmsnorm(h, np.ones(32, F16), EPS, order=0))
