@@ -58,6 +58,20 @@ def test_unpack_every_word_byte(orc, bits):
                                   u.astype(np.int64) - (1 << (bits - 1)))
 
 
+def test_int2_every_half_word(orc):
+    # all 2^16 patterns of either 16-bit half of an int2 word: eight codes,
+    # code j of the half at bits 2j..2j+1, value field - 2
+    pat = np.arange(1 << 16, dtype=np.uint32)
+    j = np.arange(8, dtype=np.uint32)
+    want = ((pat[:, None] >> (2 * j)) & 3).astype(np.int64) - 2
+    for half in (0, 1):
+        words = (pat << (16 * half)).reshape(-1, 1)
+        codes = orc.unpack(words, 16, 2).astype(np.int64)
+        assert np.array_equal(codes[:, 8 * half:8 * half + 8], want)
+        assert np.all(codes[:, 8 * (1 - half):8 * (1 - half) + 8] == -2)
+        assert np.array_equal(orc.pack(codes.astype(np.int8), 2), words)
+
+
 def test_int2_values_are_minus2_to_1(orc):
     codes = orc.unpack(np.array([[0xE4E4E4E4]], np.uint32), 16, 2)
     assert sorted(set(codes[0].tolist())) == [-2, -1, 0, 1]
