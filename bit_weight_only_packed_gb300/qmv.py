@@ -104,6 +104,28 @@ def _dptr(t):
     return t.data_ptr()
 
 
+_YDT = {QMV_F32: torch.float32, QMV_F16: torch.float16}
+
+
+def _need(name, t, dtype, n):
+    """The tensor behind a pointer argument has the dtype the kernels read or
+    write and at least the n elements they touch from its start.  The ABI
+    takes bare pointers and cannot check sizes, so this is checked here,
+    before any call.  A y_dtype outside QMV_F32/QMV_F16 skips the dtype
+    check; the ABI rejects that value itself."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.numel() < n:
+        raise ValueError(f"{name}: needs at least {n} elements, has {t.numel()}")
+
+
+def _need_bytes(name, t, n):
+    if t.numel() * t.element_size() < n:
+        raise ValueError(f"{name}: needs at least {n} bytes, has {t.numel() * t.element_size()}")
+
+
 class Pack:
     """A packed weight matrix: the host descriptor plus the device buffers
     (allocated with torch) that hold the packed codes and scales."""
@@ -148,6 +170,11 @@ def qmv_create_pack(N: int, K: int, bits: int, group: int) -> Pack:
 
 
 def qmv_pack_weights(p: Pack, codes, scales, d_codes, d_scales, stream=None):
+    G = p.K // p.group
+    _need("codes", codes, torch.int8, p.N * p.K)
+    _need("scales", scales, torch.float16, p.N * G)
+    _need_bytes("d_codes", d_codes, p.codes_bytes)
+    _need_bytes("d_scales", d_scales, p.scales_bytes)
     _check("qmv_pack_weights", _lib.qmv_pack_weights(
         p.handle, _dptr(codes), _dptr(scales), _dptr(d_codes), _dptr(d_scales), _stream(stream)))
 
@@ -161,6 +188,8 @@ def _out(y, M, N, y_dtype, like):
 
 def qmv_gemv(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None, M=None):
     M = x.shape[0] if (M is None and x.dim() == 2) else (M or 1)
+    _need("x", x, torch.float16, M * p.K)
+    _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
     _check("qmv_gemv", _lib.qmv_gemv(p.handle, M, p.N, p.K, p.bits, p.group, _dptr(x), _dptr(y),
                                      y_dtype, mode, _stream(stream)))
@@ -169,6 +198,8 @@ def qmv_gemv(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None, M=
 
 def qmv_chunk_gemm(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None):
     M = x.shape[0]
+    _need("x", x, torch.float16, M * p.K)
+    _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
     _check("qmv_chunk_gemm", _lib.qmv_chunk_gemm(p.handle, M, _dptr(x), _dptr(y), y_dtype, mode,
                                                  _stream(stream)))
@@ -178,6 +209,11 @@ def qmv_chunk_gemm(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=No
 def qmv_fused_rmsnorm_gemv(p: Pack, x, residual, gamma, eps=1e-6, h_out=None, y=None,
                            y_dtype=QMV_F32, mode=QMV_FAST, stream=None):
     M = x.shape[0] if x.dim() == 2 else 1
+    _need("x", x, torch.float16, M * p.K)
+    _need("residual", residual, torch.float16, M * p.K)
+    _need("gamma", gamma, torch.float16, p.K)
+    _need("h_out", h_out, torch.float16, M * p.K)
+    _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
     _check("qmv_fused_rmsnorm_gemv", _lib.qmv_fused_rmsnorm_gemv(
         p.handle, M, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out), _dptr(y),
@@ -189,6 +225,9 @@ def qmv_gemv_gather(p: Pack, rows_per_expert: int, expert_ids, x, y=None, y_dtyp
                     mode=QMV_FAST, stream=None):
     """y [1, n_selected * rows_per_expert]: the selected experts' rows times x."""
     n = expert_ids.numel()
+    _need("expert_ids", expert_ids, torch.int32, n)
+    _need("x", x, torch.float16, p.K)
+    _need("y", y, _YDT.get(y_dtype), n * rows_per_expert)
     y = _out(y, 1, n * rows_per_expert, y_dtype, x)
     _check("qmv_gemv_gather", _lib.qmv_gemv_gather(p.handle, rows_per_expert, _dptr(expert_ids), n,
                                                    _dptr(x), _dptr(y), y_dtype, mode, _stream(stream)))
@@ -204,6 +243,14 @@ def qmv_gemv_argmax(p: Pack, x, workspace, residual=None, gamma=None, eps=1e-6, 
                     y_dtype=QMV_F32, mode=QMV_FAST, stream=None, index=None, value=None):
     """(index, value) device tensors of the greedy token; y (logits) is stored
     only if given."""
+    _need("x", x, torch.float16, p.K)
+    _need("residual", residual, torch.float16, p.K)
+    _need("gamma", gamma, torch.float16, p.K)
+    _need("h_out", h_out, torch.float16, p.K)
+    _need("y", y, _YDT.get(y_dtype), p.N)
+    _need("index", index, torch.int32, 1)
+    _need("value", value, torch.float32, 1)
+    _need_bytes("workspace", workspace, _lib.qmv_argmax_workspace_bytes())
     if index is None:
         index = torch.empty(1, dtype=torch.int32, device=x.device)
     if value is None:
@@ -217,6 +264,7 @@ def qmv_gemv_argmax(p: Pack, x, workspace, residual=None, gamma=None, eps=1e-6, 
 def qmv_unpack_codes(p: Pack, out=None, stream=None):
     if out is None:
         out = torch.empty((p.N, p.K), dtype=torch.int8, device=p.words.device)
+    _need("out", out, torch.int8, p.N * p.K)
     _check("qmv_unpack_codes", _lib.qmv_unpack_codes(p.handle, _dptr(out), _stream(stream)))
     return out
 
@@ -266,6 +314,8 @@ class Chain:
         self._keep = []
 
     def add_gemv(self, p: Pack, x, y, y_dtype=QMV_F32, mode=QMV_FAST):
+        _need("x", x, torch.float16, p.K)
+        _need("y", y, _YDT.get(y_dtype), p.N)
         _check("qmv_chain_add_gemv", _lib.qmv_chain_add_gemv(self.handle, p.handle, _dptr(x), _dptr(y),
                                                              y_dtype, mode))
         self._keep += [p, x, y]
@@ -273,6 +323,11 @@ class Chain:
 
     def add_fused_rmsnorm_gemv(self, p: Pack, x, residual, gamma, eps, h_out, y, y_dtype=QMV_F32,
                                mode=QMV_FAST):
+        _need("x", x, torch.float16, p.K)
+        _need("residual", residual, torch.float16, p.K)
+        _need("gamma", gamma, torch.float16, p.K)
+        _need("h_out", h_out, torch.float16, p.K)
+        _need("y", y, _YDT.get(y_dtype), p.N)
         _check("qmv_chain_add_fused_rmsnorm_gemv", _lib.qmv_chain_add_fused_rmsnorm_gemv(
             self.handle, p.handle, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out),
             _dptr(y), y_dtype, mode))

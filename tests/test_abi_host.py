@@ -85,3 +85,46 @@ def test_status_strings(q):
         assert q.qmv_status_string(s) and q.qmv_status_string(s) != "unknown status"
     assert q.qmv_status_string(-99) == "unknown status"
     assert q.qmv_last_cuda_error() == 0
+
+
+def test_binding_checks_tensors_before_any_call(q):
+    # The ABI takes bare pointers, so the binding checks the dtype and size of
+    # every tensor first: a short or mistyped buffer is rejected on the host
+    # (these tensors live on the CPU; no call reaches the library or a device).
+    import torch
+    f16 = lambda *s: torch.zeros(*s, dtype=torch.float16)
+    p = q.Pack(64, 128, 2, 32)
+    x = f16(1, 128)
+    cases = [
+        (lambda: q.qmv_gemv(p, torch.zeros(1, 128)), "x: expected torch.float16"),
+        (lambda: q.qmv_gemv(p, f16(1, 64)), "x: needs at least 128"),
+        (lambda: q.qmv_gemv(p, x, y=torch.zeros(1, 32)), "y: needs at least 64"),
+        (lambda: q.qmv_gemv(p, x, y=torch.zeros(1, 64), y_dtype=q.QMV_F16), "y: expected torch.float16"),
+        (lambda: q.qmv_chunk_gemm(p, f16(4, 100)), "x: needs at least 512"),
+        (lambda: q.qmv_fused_rmsnorm_gemv(p, f16(2, 128), f16(1, 128), f16(128)), "residual: needs at least 256"),
+        (lambda: q.qmv_fused_rmsnorm_gemv(p, x, x, f16(64)), "gamma: needs at least 128"),
+        (lambda: q.qmv_fused_rmsnorm_gemv(p, x, x, f16(128), h_out=f16(100)), "h_out: needs at least 128"),
+        (lambda: q.qmv_gemv_gather(p, 16, torch.zeros(2, dtype=torch.int64), x), "expert_ids: expected torch.int32"),
+        (lambda: q.qmv_gemv_gather(p, 16, torch.zeros(2, dtype=torch.int32), x, y=torch.zeros(31)),
+         "y: needs at least 32"),
+        (lambda: q.qmv_gemv_argmax(p, x, torch.zeros(8, dtype=torch.uint8)), "workspace: needs at least 16 bytes"),
+        (lambda: q.qmv_gemv_argmax(p, x, torch.zeros(16, dtype=torch.uint8),
+                                   index=torch.zeros(1, dtype=torch.int64)), "index: expected torch.int32"),
+        (lambda: q.qmv_pack_weights(p, torch.zeros(64, 128, dtype=torch.int16), f16(64, 4),
+                                    torch.zeros(512, dtype=torch.int32), f16(256)), "codes: expected torch.int8"),
+        (lambda: q.qmv_pack_weights(p, torch.zeros(64, 128, dtype=torch.int8), f16(64, 4),
+                                    torch.zeros(511, dtype=torch.int32), f16(256)), "d_codes: needs at least 2048 bytes"),
+        (lambda: q.qmv_unpack_codes(p, out=torch.zeros(64, 127, dtype=torch.int8)), "out: needs at least 8192"),
+    ]
+    ch = q.Chain.__new__(q.Chain)          # no workspace: the checks come first
+    ch.handle, ch._keep = None, []
+    cases += [
+        (lambda: ch.add_gemv(p, f16(1, 100), torch.zeros(1, 64)), "x: needs at least 128"),
+        (lambda: ch.add_fused_rmsnorm_gemv(p, x, x, f16(128), 1e-6, None, f16(1, 64)), "y: expected torch.float32"),
+    ]
+    for call, msg in cases:
+        with pytest.raises(ValueError, match=msg):
+            call()
+    # a well-formed call gets past the checks and stops at the device pointer
+    with pytest.raises(ValueError, match="contiguous CUDA tensor"):
+        q.qmv_gemv(p, x, y=torch.zeros(1, 64))
