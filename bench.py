@@ -598,7 +598,10 @@ def oracle_layer(oracle, hin, mats):
     oracle.gemv(c, s, g, act)
 
 
-def cpu_baseline(budget_s: float = 10.0, frac_rows: int = 4):
+def cpu_baseline(budget_s: float = 12.0, frac_rows: int = 4):
+    """The oracle, as it stands, timed on one host core over a bounded sample
+    of the decode layer: passes over the row sample until budget_s seconds of
+    CPU work have run."""
     import oracle
     oracle.build()
     hin, mats = oracle_sample(frac_rows)
@@ -609,7 +612,7 @@ def cpu_baseline(budget_s: float = 10.0, frac_rows: int = 4):
         oracle_layer(oracle, hin, mats)
         n += 1
         dt = time.perf_counter() - t0
-        if dt >= budget_s or n >= 200:
+        if dt >= budget_s:
             break
     return {"value": round(sample_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
