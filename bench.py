@@ -61,6 +61,9 @@ def packed_bytes(N, K, bits, group):
     return N * K * bits // 8 + N * (K // group) * 2
 
 
+# what the path reads and computes in: the JSON line's "dtype" is the
+# arithmetic type (fp32 sums of exact products), this names the formats
+FORMATS = "int2/int4 codes, fp16 scales and activations, fp32 accumulation"
 LAYER_BYTES = sum(packed_bytes(N, K, b, g) for _, N, K, b, g, _ in LAYER)
 
 
@@ -528,11 +531,12 @@ def gpu_arm(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int2/int4 codes, fp16 act, f32 accum",
+        "dtype": "f32",
         "data": "synthetic (seeded SplitMix64 codes/scales, Box-Muller fp16 activations)",
         "config": {"workload": "synthetic decode layer, M=1, d_model 2048, d_ff 8192: "
                                "fused RMSNorm+qkv int4 2560x2048, o int4 2048x2048, "
                                "fused RMSNorm+gate/up int2 16384x2048, down int2 2048x8192",
+                   "formats": FORMATS,
                    "layer_bytes": LAYER_BYTES, "resident_layers": L,
                    "resident_bytes": LAYER_BYTES * L,
                    "l2": "inputs larger than L2 (distinct layer weights rotated per step)",
@@ -642,8 +646,9 @@ def reference_arm(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int2/int4 codes, fp16 act, f32 accum", "data": "synthetic",
-        "config": {"workload": "synthetic decode layer, M=1, d_model 2048, d_ff 8192 (row sample)"},
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "synthetic decode layer, M=1, d_model 2048, d_ff 8192 (row sample)",
+                   "formats": FORMATS},
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
