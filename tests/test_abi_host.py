@@ -128,3 +128,35 @@ def test_binding_checks_tensors_before_any_call(q):
     # a well-formed call gets past the checks and stops at the device pointer
     with pytest.raises(ValueError, match="contiguous CUDA tensor"):
         q.qmv_gemv(p, x, y=torch.zeros(1, 64))
+
+
+def test_header_is_plain_c_and_links(q, tmp_path):
+    # A C99 program that includes only include/qmv.h, links libqmv.so and
+    # uses the host-only entry points (no device is touched).
+    import subprocess
+    src = tmp_path / "abi_c.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "qmv.h"
+int main(void) {
+    qmv_pack *p = NULL;
+    size_t cb = 0, sb = 0;
+    int N = 0, K = 0, bits = 0, group = 0;
+    if (qmv_create_pack(&p, 48, 256, 4, 32, &cb, &sb) != QMV_OK) return 1;
+    if (cb != 48 * 256 / 2 || sb != 48 * 8 * 2) return 2;
+    if (qmv_pack_info(p, &N, &K, &bits, &group) != QMV_OK) return 3;
+    if (N != 48 || K != 256 || bits != 4 || group != 32) return 4;
+    if (qmv_gemv(p, 1, 48, 256, 4, 32, NULL, NULL, QMV_F32, QMV_FAST, NULL) != QMV_ERR_INVALID_ARG) return 5;
+    if (qmv_destroy_pack(p) != QMV_OK) return 6;
+    printf("%s\n", qmv_status_string(QMV_ERR_SHAPE));
+    return 0;
+}
+''')
+    exe = tmp_path / "abi_c"
+    libdir = os.path.dirname(q.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-lqmv", f"-Wl,-rpath,{libdir}"],
+                   check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert r.stdout.strip() == q.qmv_status_string(q.QMV_ERR_SHAPE)
