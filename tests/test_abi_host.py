@@ -160,3 +160,30 @@ int main(void) {
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stderr)
     assert r.stdout.strip() == q.qmv_status_string(q.QMV_ERR_SHAPE)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    # The binding module, copied where no _lib/libqmv.so sits beside it,
+    # raises at import: there is no fallback of any kind.
+    import importlib.util
+    import shutil
+    src = os.path.join(ROOT, "bit_weight_only_packed_gb300", "qmv.py")
+    shutil.copy(src, tmp_path / "qmv_nolib.py")
+    spec = importlib.util.spec_from_file_location("qmv_nolib", tmp_path / "qmv_nolib.py")
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError, match="libqmv.so is not built"):
+        spec.loader.exec_module(mod)
+
+
+def test_product_never_touches_the_oracle():
+    # The library and its binding neither import nor load the oracle, the
+    # generator or scratch files; the oracle is test infrastructure only.
+    pkg = os.path.join(ROOT, "bit_weight_only_packed_gb300")
+    bad = re.compile(r"\b(import\s+oracle|from\s+oracle|import\s+synth|from\s+synth|liboracle|_work)\b")
+    for dirpath, _, files in os.walk(pkg):
+        if "__pycache__" in dirpath or "_lib" in dirpath:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not bad.search(text), (f, bad.search(text).group(0))
