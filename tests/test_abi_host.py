@@ -187,3 +187,12 @@ def test_product_never_touches_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not bad.search(text), (f, bad.search(text).group(0))
+
+
+def test_oracle_shares_no_code_with_the_library():
+    # The oracle includes only the C standard headers and imports nothing of
+    # the library; the two sides share only the input generator.
+    c = open(os.path.join(ROOT, "oracle", "qmv_oracle.c")).read()
+    assert sorted(set(re.findall(r'#include\s*[<"]([^>"]+)[>"]', c))) == ["math.h", "stdint.h", "string.h"]
+    py = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert "bit_weight_only_packed_gb300" not in py and "qmv.h" not in py and "import synth" not in py
