@@ -195,4 +195,6 @@ def test_oracle_shares_no_code_with_the_library():
     c = open(os.path.join(ROOT, "oracle", "qmv_oracle.c")).read()
     assert sorted(set(re.findall(r'#include\s*[<"]([^>"]+)[>"]', c))) == ["math.h", "stdint.h", "string.h"]
     py = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
-    assert "bit_weight_only_packed_gb300" not in py and "qmv.h" not in py and "import synth" not in py
+    imports = re.findall(r"^\s*(?:from\s+(\S+)\s+import|import\s+(\S+))", py, re.M)
+    mods = {a or b for a, b in imports}
+    assert not {m for m in mods if m.split(".")[0] in ("bit_weight_only_packed_gb300", "synth", "bench")}, mods
