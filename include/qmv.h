@@ -299,7 +299,7 @@ QMV_API int qmv_chain_create(qmv_chain **out, int max_ops, void *d_workspace,
  * qmv_chain_create_no_alloc -- an empty chain whose barrier words and op table
  * live in the library's own scratch array (a file-scope device array, one per
  * device, room for 1024 ops), so neither the caller nor the library allocates
- * device memory for it.  The paper has no counterpart: it is an interface
+ * device memory for it.  The source pages have no counterpart: it is an interface
  * variant of qmv_chain_create.  The array's address is looked up once per
  * device; the chain must run on the device that was current here.  Every run
  * clears the barrier words; a run after another chain used the array re-copies
