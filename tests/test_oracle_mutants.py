@@ -45,6 +45,11 @@ MUTANTS = [
     ("f32_to_f16_overflow_edge", "fp16", [("if (e > 15)", "if (e > 16)", None)]),
     ("f32_to_f16_normal_edge", "fp16", [("if (e >= -14)", "if (e >= -15)", None)]),
     ("f32_to_f16_subnormal_shift", "fp16", [("int shift = -e - 1;", "int shift = -e - 2;", None)]),
+    ("f16_nan_payload_dropped", "fp16", [("sign | 0x7F800000u | (m << 13)", "sign | 0x7F800000u", None)]),
+    ("f32_to_f16_nan_to_inf", "fp16", [("(uint16_t)(sign | 0x7E00u | ((ax >> 13) & 0x3FFu))",
+                                        "(uint16_t)(sign | 0x7C00u)", None)]),
+    ("f32_to_f16_underflow_sign_lost", "fp16", [("return sign;                     /* below half",
+                                                 "return 0;                        /* below half", None)]),
     # packer and decoder
     ("pack_twos_complement", "pack", [("int u = v + bias;", "int u = v;", None)]),
     ("pack_msb_first", "pack", [("<< (bits * (int)(k % per_word))",
