@@ -81,6 +81,11 @@ MUTANTS = [
     ("fused_gamma_dropped", "norm", [("float b = a * orc_f16_to_f32(gamma[k]);", "float b = a;", 1)]),
     ("rmsnorm_one_plus_gamma", "norm", [("float b = a * orc_f16_to_f32(gamma[k]);",
                                          "float b = a * (1.0f + orc_f16_to_f32(gamma[k]));", 0)]),
+    ("norm_scale_before_normalise", "norm", [
+        ("float a = orc_f16_to_f32(h[k]) * inv;", "float a = orc_f16_to_f32(h[k]) * orc_f16_to_f32(gamma[k]);", None),
+        ("float b = a * orc_f16_to_f32(gamma[k]);", "float b = a * inv;", 0),
+        ("float a = hv * inv;", "float a = hv * orc_f16_to_f32(gamma[k]);", None),
+        ("float b = a * orc_f16_to_f32(gamma[k]);", "float b = a * inv;", 0)]),
     # matvec
     ("gemv_block_term_dropped", "gemv", [("p = p + prod;", "p = prod;", None)]),
     ("gemv_blocks_not_added", "gemv", [("if (b0 == g0) q = p; else q = q + p;", "q = p;", None)]),

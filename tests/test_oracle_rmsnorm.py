@@ -107,3 +107,21 @@ def test_sumsq_block_order(orc):
     assert orc.sumsq(h, order=0) == 2.0 ** 22
     hb, yb = orc.fused_residual_rmsnorm(h, np.zeros(32, F16), np.ones(32, F16), EPS)
     assert np.array_equal(yb[0], orc.rmsnorm(h, np.ones(32, F16), EPS, order=0))
+
+
+def test_normalise_then_scale_order(orc):
+    # y = fp16((h * inv) * gamma): the product with inv comes first.  With
+    # h = [3, 13] (K = 2), eps = 0 and gamma0 = 1557/1024, each step exactly:
+    #   ss = 178, mean = 89, rt = RN(sqrt 89) = 4946123 * 2^-19,
+    #   inv = RN(1 / rt) = 14227051 * 2^-27,
+    #   h0 * inv = 42681153 * 2^-27 -> RN 666893 * 2^-21,
+    #   times gamma0 = 1038352401 * 2^-31 -> RN 16224256 * 2^-25 = 1980.5 * 2^-12,
+    # exactly halfway between two fp16 values: ties to even give 1980 * 2^-12.
+    # The other order, RN(h0 * gamma0) = 4671 * 2^-10 times inv, rounds to
+    # 16224257 * 2^-25, above the halfway point, and would give 1981 * 2^-12.
+    h = np.array([3.0, 13.0], F16)
+    g = np.array([1557 / 1024, 1.0], F16)
+    y = orc.rmsnorm(h, g, 0.0).view(F16)
+    assert float(y[0]) == 1980 * 2.0 ** -12
+    _, yb = orc.fused_residual_rmsnorm(h, np.zeros(2, F16), g, 0.0)
+    assert float(yb[0].view(F16)[0]) == 1980 * 2.0 ** -12
