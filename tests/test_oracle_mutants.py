@@ -76,6 +76,10 @@ MUTANTS = [
     ("rms_eps_dropped", "norm", [("float t = mean + eps;", "float t = mean;", None)]),
     ("rms_mean_over_k_minus_1", "norm", [("float mean = ss / (float)K;",
                                           "float mean = ss / (float)(K - 1);", None)]),
+    ("inv_in_double", "norm", [("float inv = 1.0f / rt;", "float inv = (float)(1.0 / sqrt((double)t));", None),
+                               ("inv = 1.0f / rt;", "inv = (float)(1.0 / sqrt((double)t));", 0)]),
+    ("mean_by_reciprocal", "norm", [("float mean = ss / (float)K;", "float mean = ss * (1.0f / (float)K);", None),
+                                    ("mean = ss / (float)K;", "mean = ss * (1.0f / (float)K);", 0)]),
     ("fused_sqrt_dropped", "norm", [("inv = 1.0f / rt;", "inv = 1.0f / t;", 1)]),
     ("rmsnorm_gamma_dropped", "norm", [("float b = a * orc_f16_to_f32(gamma[k]);", "float b = a;", 0)]),
     ("fused_gamma_dropped", "norm", [("float b = a * orc_f16_to_f32(gamma[k]);", "float b = a;", 1)]),

@@ -125,3 +125,22 @@ def test_normalise_then_scale_order(orc):
     assert float(y[0]) == 1980 * 2.0 ** -12
     _, yb = orc.fused_residual_rmsnorm(h, np.zeros(2, F16), g, 0.0)
     assert float(yb[0].view(F16)[0]) == 1980 * 2.0 ** -12
+
+
+def test_inv_steps_each_rounded_in_fp32(orc):
+    # mean = RN(ss / K), then RN(sqrt), then RN(1 / rt), each one fp32
+    # operation.  With h = [7, 0, 5] (K = 3), eps = 0, gamma0 = 1485/1024:
+    #   ss = 74, mean = RN(74/3) = 12932437 * 2^-19,
+    #   rt = RN(sqrt mean) = 2603905 * 2^-19, inv = RN(1 / rt) = 13512157 * 2^-26,
+    #   h0 * inv = 94585099 * 2^-26 -> RN 11823137 * 2^-23,
+    #   times gamma0 = 17557358445 * 2^-33 -> RN 8572929 * 2^-22,
+    # just above the fp16 halfway point 1046.5 * 2^-9: y0 = 1047 * 2^-9.
+    # inv from a double-precision 1/sqrt (13512156 * 2^-26) or a mean taken as
+    # ss * RN(1/3) (inv 13512155 * 2^-26) both give h0 * inv = 11823136 * 2^-23
+    # and a product exactly on the halfway point: ties to even, 1046 * 2^-9.
+    h = np.array([7.0, 0.0, 5.0], F16)
+    g = np.array([1485 / 1024, 1.0, 1.0], F16)
+    y = orc.rmsnorm(h, g, 0.0).view(F16)
+    assert float(y[0]) == 1047 * 2.0 ** -9
+    _, yb = orc.fused_residual_rmsnorm(h, np.zeros(3, F16), g, 0.0)
+    assert float(yb[0].view(F16)[0]) == 1047 * 2.0 ** -9
