@@ -71,6 +71,9 @@ MUTANTS = [
     ("sumsq_term_dropped", "norm", [("blk = blk + sq;", "blk = sq;", 0)]),
     ("fused_sumsq_term_dropped", "norm", [("blk = blk + sq;", "blk = sq;", 1)]),
     ("sumsq_blocks_not_added", "norm", [("ss = ss + blk;", "ss = blk;", 0)]),
+    ("norm_serial_sum_of_squares", "norm", [("float inv = orc_rms_inv(orc_sumsq(h, K, order), K, eps);",
+                                             "float inv = orc_rms_inv(orc_sumsq(h, K, 1), K, eps);", None),
+                                            ("blk = blk + sq;", "ss = ss + sq;", 1)]),
     ("fused_ragged_block_lost", "norm", [("if ((k + 1) % ORC_BLOCK == 0 || k + 1 == K) {",
                                           "if ((k + 1) % ORC_BLOCK == 0) {", None)]),
     ("rms_eps_dropped", "norm", [("float t = mean + eps;", "float t = mean;", None)]),

@@ -144,3 +144,24 @@ def test_inv_steps_each_rounded_in_fp32(orc):
     assert float(y[0]) == 1047 * 2.0 ** -9
     _, yb = orc.fused_residual_rmsnorm(h, np.zeros(3, F16), g, 0.0)
     assert float(yb[0].view(F16)[0]) == 1047 * 2.0 ** -9
+
+
+def test_norm_uses_the_blocked_sum_of_squares(orc):
+    # RMSNorm itself sums the squares in blocks of 32, then over the blocks,
+    # not in one serial chain.  h0 = 100, h1..31 = 0, h32..63 = 27/64 (K = 64),
+    # eps = 0, gamma0 = 1757/1024:
+    #   blocked: ss = 10000 + 32 * 729/4096 = 1280729 * 2^-7,
+    #     mean = 1280729 * 2^-13, rt = 3277733 * 2^-18, inv = 5367181 * 2^-26,
+    #     h0 * inv -> 16772441 * 2^-21, times gamma0 -> 14389247 * 2^-20,
+    #     one fp32 ulp below the fp16 halfway point 1756.5 * 2^-7: y0 = 1756 * 2^-7;
+    #   one serial chain rounds each 729/4096 added to 10000 down to 182/1024:
+    #     ss = 160091 * 2^-4, inv = 5367183 * 2^-26, product 14389253 * 2^-20,
+    #     above the halfway point, which would give 1757 * 2^-7.
+    h = np.array([100.0] + [0.0] * 31 + [27 / 64] * 32, F16)
+    g = np.ones(64, F16)
+    g[0] = 1757 / 1024
+    assert orc.sumsq(h, order=0) == 1280729 * 2.0 ** -7
+    y = orc.rmsnorm(h, g, 0.0).view(F16)
+    assert float(y[0]) == 1756 * 2.0 ** -7
+    _, yb = orc.fused_residual_rmsnorm(h, np.zeros(64, F16), g, 0.0)
+    assert float(yb[0].view(F16)[0]) == 1756 * 2.0 ** -7
