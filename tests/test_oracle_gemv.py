@@ -112,6 +112,18 @@ def test_blocks_inside_a_long_group():
     assert _one_row(y, [1] * 64, [1.0, 1.0], 32) == A + 2.0 ** -5
 
 
+def test_block_sums_of_a_group_added_in_fp32():
+    # group == K == 128: four 32-code blocks whose sums are A, e, e, e.  Added
+    # serially in fp32, each e (a quarter of the spacing at A) is absorbed:
+    # the group's dot is A.  Kept in a wider type, the three e would reach
+    # three quarters of a spacing and round up to A + 2^-8.
+    K = 128
+    y = np.zeros(K)
+    y[0] = A
+    y[32] = y[64] = y[96] = E
+    assert _one_row(y, [1] * K, [1.0], K) == A
+
+
 def test_serial_order_over_groups():
     # eight groups, each with one live term: group partials A, e, e, ... in
     # order -> every e absorbed; reversed placement -> A + 2^-7

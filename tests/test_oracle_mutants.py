@@ -105,6 +105,7 @@ MUTANTS = [
                                         "acc = fmaf(q, orc_f16_to_f32(scales[n * G + g]), acc); (void)t;",
                                         None)]),
     ("gemv_block_in_double", "gemv", [("float p = 0.0f;", "double p = 0.0;", None)]),
+    ("gemv_group_dot_in_double", "gemv", [("float q = 0.0f;", "double q = 0.0;", None)]),
     ("gemv_group_one_chain", "gemv", [("b0 < g1; b0 += ORC_BLOCK)", "b0 < g1; b0 = g1)", None),
                                       ("b0 + ORC_BLOCK < g1 ? b0 + ORC_BLOCK : g1", "g1", None)]),
     ("block_of_16", "gemv", [("#define ORC_BLOCK 32", "#define ORC_BLOCK 16", None)]),
