@@ -22,7 +22,7 @@
 //     0x4B000000 = 2^23 + u*2^o), one paired subtract gives v*2^o, and one
 //     paired FMA advances both blocks' serial sums.  Folded form: one 64-bit
 //     AND per field pair and one paired FMA.
-//   * Block sums (scaled) go to a double-buffered fold buffer; a dedicated
+//   * Block sums (scaled) go to a ring of M1_TB fold buffers; a dedicated
 //     fold warp adds them serially per row (one lane per row) and writes y,
 //     so the compute warps never wait at a CTA-wide barrier.
 //   * Every mbarrier wait is bounded; on timeout the kernel records an error
