@@ -60,3 +60,29 @@ def test_reference_arm_line():
         assert k in line
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gpu_arm_line_has_every_contract_key():
+    # The GPU arm only runs on a GPU, so its JSON line is checked statically:
+    # the dict literal gpu_arm returns carries every key the bench contract
+    # names (nested ones too), and main() adds the CPU baseline at N = 1.
+    import ast
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    fn = next(n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name == "gpu_arm")
+    out = next(n.value for n in ast.walk(fn) if isinstance(n, ast.Assign)
+               and any(isinstance(t, ast.Name) and t.id == "out" for t in n.targets)
+               and isinstance(n.value, ast.Dict))
+
+    def keys(d):
+        return {k.value: v for k, v in zip(d.keys, d.values) if isinstance(k, ast.Constant)}
+
+    top = keys(out)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "e2e", "clocks", "gpu_launches"):
+        assert k in top, k
+    assert {"bound", "achieved", "peak", "unit", "frac", "traffic"} <= set(keys(top["roofline"]))
+    assert {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"} <= set(keys(top["e2e"]))
+    assert "workload" in keys(top["config"]) and "l2" in keys(top["config"])
+    main = next(n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name == "main")
+    assert "cpu_baseline" in ast.unparse(main)
