@@ -86,3 +86,27 @@ def test_gpu_arm_line_has_every_contract_key():
     assert "workload" in keys(top["config"]) and "l2" in keys(top["config"])
     main = next(n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name == "main")
     assert "cpu_baseline" in ast.unparse(main)
+
+
+@pytest.mark.parametrize("path", ["bench.py", "__graft_entry__.py",
+                                  "bit_weight_only_packed_gb300/qmv.py"])
+def test_no_undefined_global_names(path):
+    # Much of this code runs only on a GPU; a name read as a global in any
+    # function (closures resolved) must be defined at module level or be a
+    # builtin, so a typo cannot wait for the GPU run to surface.
+    import builtins
+    import symtable
+    top = symtable.symtable(open(os.path.join(ROOT, path)).read(), path, "exec")
+    defined = {s.get_name() for s in top.get_symbols() if s.is_assigned() or s.is_imported()}
+    defined |= set(dir(builtins)) | {"__file__", "__name__"}
+    bad = []
+
+    def walk(t):
+        for s in t.get_symbols():
+            if s.is_global() and s.is_referenced() and s.get_name() not in defined:
+                bad.append((t.get_name(), s.get_name()))
+        for c in t.get_children():
+            walk(c)
+
+    walk(top)
+    assert not bad, bad
