@@ -1,6 +1,7 @@
 """Host-side logic of bench.py without a GPU: the max-over-ranks timing and
 barrier across two gloo ranks (the N > 1 replica path), and the reference
 arm's JSON line (the CPU oracle)."""
+import glob
 import json
 import os
 import socket
@@ -88,8 +89,13 @@ def test_gpu_arm_line_has_every_contract_key():
     assert "cpu_baseline" in ast.unparse(main)
 
 
-@pytest.mark.parametrize("path", ["bench.py", "__graft_entry__.py",
-                                  "bit_weight_only_packed_gb300/qmv.py"])
+GPU_ONLY_SOURCES = ["bench.py", "__graft_entry__.py", "bit_weight_only_packed_gb300/qmv.py",
+                    "synth/__init__.py", "oracle/__init__.py", "tests/gpu_util.py",
+                    "tests/test_zz_no_alloc.py"] + sorted(
+    os.path.relpath(p, ROOT) for p in glob.glob(os.path.join(ROOT, "tests", "test_gpu_*.py")))
+
+
+@pytest.mark.parametrize("path", GPU_ONLY_SOURCES)
 def test_no_undefined_global_names(path):
     # Much of this code runs only on a GPU; a name read as a global in any
     # function (closures resolved) must be defined at module level or be a
