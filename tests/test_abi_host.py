@@ -198,3 +198,24 @@ def test_oracle_shares_no_code_with_the_library():
     imports = re.findall(r"^\s*(?:from\s+(\S+)\s+import|import\s+(\S+))", py, re.M)
     mods = {a or b for a, b in imports}
     assert not {m for m in mods if m.split(".")[0] in ("bit_weight_only_packed_gb300", "synth", "bench")}, mods
+
+
+def test_binding_signatures_match_the_header():
+    # every ctypes signature has as many arguments as the C declaration, and
+    # pointer parameters are passed as pointers (a mismatch would only show as
+    # a corrupted call on a GPU)
+    import ctypes
+    from bit_weight_only_packed_gb300 import qmv as q
+    txt = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = re.findall(r"QMV_API\s+([\w\s\*]*?)\b(qmv_\w+)\s*\(([^)]*)\)\s*;", txt)
+    assert len(decls) == len(q.SIGNATURES)
+    for _ret, name, params in decls:
+        ps = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
+        _, argtypes = q.SIGNATURES[name]
+        assert len(ps) == len(argtypes), (name, ps, argtypes)
+        for p, a in zip(ps, argtypes):
+            if "*" in p:
+                assert a is ctypes.c_void_p or issubclass(a, ctypes._Pointer), (name, p, a)
+            elif p.split()[0] in ("int", "float", "size_t"):
+                want = {"int": ctypes.c_int, "float": ctypes.c_float, "size_t": ctypes.c_size_t}[p.split()[0]]
+                assert a is want, (name, p, a)
