@@ -209,9 +209,12 @@ def test_binding_signatures_match_the_header():
     txt = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
     decls = re.findall(r"QMV_API\s+([\w\s\*]*?)\b(qmv_\w+)\s*\(([^)]*)\)\s*;", txt)
     assert len(decls) == len(q.SIGNATURES)
-    for _ret, name, params in decls:
+    for ret, name, params in decls:
         ps = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
-        _, argtypes = q.SIGNATURES[name]
+        restype, argtypes = q.SIGNATURES[name]
+        ret = " ".join(ret.split())
+        want_ret = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char *": ctypes.c_char_p}[ret]
+        assert restype is want_ret, (name, ret, restype)
         assert len(ps) == len(argtypes), (name, ps, argtypes)
         for p, a in zip(ps, argtypes):
             if "*" in p:
