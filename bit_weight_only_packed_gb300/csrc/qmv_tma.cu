@@ -452,7 +452,7 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
       return tma_dispatch<BITS>(a, gather_groups(cache[i].p), s, err, nullptr);
   }
   const int sms = dev_info().sms;
-  TmaPlan best;
+  TmaPlan best{};
   int best_score = -1;
   // small matrices (fewer than two full groups per CTA slot): a plan with
   // half-size groups (16 rows) -- one row per thread on 512 compute threads,
@@ -463,7 +463,7 @@ static int tma_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   // 2048x16384 int2 in a 30-layer token: 977 against 928 tok/s for the
   // token), while with up to four segments the 512-thread CTA is faster
   // (down 2048x8192 int2 in the decode layer: 22.75 against 23.65 us)
-  TmaPlan small;
+  TmaPlan small{};
   int64_t small_cost = -1, best_slots = 1;
   for (int tc : {256, 512}) {
     for (int U : {4, 2, 1}) {
