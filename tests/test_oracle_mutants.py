@@ -48,6 +48,9 @@ MUTANTS = [
     ("f16_nan_payload_dropped", "fp16", [("sign | 0x7F800000u | (m << 13)", "sign | 0x7F800000u", None)]),
     ("f32_to_f16_nan_to_inf", "fp16", [("(uint16_t)(sign | 0x7E00u | ((ax >> 13) & 0x3FFu))",
                                         "(uint16_t)(sign | 0x7C00u)", None)]),
+    ("f32_to_f16_inf_sign_lost", "fp16", [("return (uint16_t)(sign | 0x7C00u);\n", "return (uint16_t)(0x7C00u);\n", 0)]),
+    ("f32_to_f16_carry_lost", "fp16", [("            hv += 1;                     /* a carry",
+                                        "            hv = (hv & ~0x3FFu) | ((hv + 1) & 0x3FFu);  /* a carry", None)]),
     ("f32_to_f16_underflow_sign_lost", "fp16", [("return sign;                     /* below half",
                                                  "return 0;                        /* below half", None)]),
     # packer and decoder
@@ -60,6 +63,8 @@ MUTANTS = [
     ("pack_range_off_by_one", "pack", [("v >= bias", "v > bias", None)]),
     ("pack_word_index", "pack", [("words[n * wpr + k / per_word] |=",
                                   "words[n * wpr + k % wpr] |=", None)]),
+    ("unpack_mask_wide", "pack", [("(w >> (bits * (int)(k % per_word))) & mask;",
+                                   "(w >> (bits * (int)(k % per_word))) & (mask | (mask << 1));", None)]),
     # residual add + RMSNorm
     ("residual_sign", "norm", [("orc_f16_to_f32(x[k]) + orc_f16_to_f32(r[k])",
                                 "orc_f16_to_f32(x[k]) - orc_f16_to_f32(r[k])", None)]),
@@ -111,6 +116,9 @@ MUTANTS = [
     ("block_of_16", "gemv", [("#define ORC_BLOCK 32", "#define ORC_BLOCK 16", None)]),
     # argmax
     ("argmax_last_max", "argmax", [("y[n] > y[best]", "y[n] >= y[best]", None)]),
+    ("argmax_best_starts_at_0", "argmax", [("int64_t best = -1;", "int64_t best = 0;", None)]),
+    ("argmax_value_of_last", "argmax", [("*max_out = y[best];", "*max_out = y[N - 1];", None)]),
+    ("argmax_abs_compare", "argmax", [("y[n] > y[best]", "fabsf(y[n]) > fabsf(y[best])", None)]),
     ("argmax_nan_not_skipped", "argmax", [("if (y[n] != y[n]) continue;", "(void)0;", None)]),
 ]
 
