@@ -31,6 +31,7 @@
 //     the chain's device error word and marks the CTA aborted; its warps then
 //     skip the remaining work but still reach every named barrier, the
 //     producer lets its copies land, and the kernel returns.
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -456,7 +457,12 @@ int qmv_chain_create(qmv_chain** out, int max_ops, void* d_workspace, size_t wor
   return QMV_OK;
 }
 
-// the chain whose op table the scratch array of each device holds
+// Host bookkeeping of the library's scratch array, one entry per device: its
+// device address (looked up once) and the chain whose op table it holds.
+// Chains on several host threads read and update both, so every access takes
+// g_static_mu.
+static std::mutex g_static_mu;
+static void* g_static_addr[64];
 static const qmv_chain* g_static_owner[64];
 
 int qmv_chain_create_no_alloc(qmv_chain** out, int max_ops) {
@@ -466,13 +472,20 @@ int qmv_chain_create_no_alloc(qmv_chain** out, int max_ops) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return qmv::record_cuda_error(e);
   if (dev < 0 || dev >= 64) return QMV_ERR_UNSUPPORTED;
-  // the scratch array's address on this device (set-up, per device)
-  static void* addr[64];
-  if (!addr[dev]) {
-    e = cudaGetSymbolAddress(&addr[dev], qmv::g_chain_scratch);
-    if (e != cudaSuccess) return qmv::record_cuda_error(e);
+  void* addr = nullptr;
+  {
+    // the scratch array's address on this device (set-up, once per device)
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      e = cudaGetSymbolAddress(&g_static_addr[dev], qmv::g_chain_scratch);
+      if (e != cudaSuccess) {
+        g_static_addr[dev] = nullptr;
+        return qmv::record_cuda_error(e);
+      }
+    }
+    addr = g_static_addr[dev];
   }
-  const int rc = qmv_chain_create(out, max_ops, addr[dev], sizeof(qmv::g_chain_scratch));
+  const int rc = qmv_chain_create(out, max_ops, addr, sizeof(qmv::g_chain_scratch));
   if (rc == QMV_OK) (*out)->static_dev = dev;
   return rc;
 }
@@ -564,20 +577,35 @@ int qmv_chain_run(qmv_chain* c, void* stream) {
   if (c->ops.empty()) return QMV_OK;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
+  // the scratch array's owner is read and set under the lock, together with
+  // the upload it decides on, so two host threads agree on whose table is there
+  std::unique_lock<std::mutex> lock(g_static_mu, std::defer_lock);
   if (c->static_dev >= 0) {
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return record_cuda_error(e);
     if (dev != c->static_dev) return QMV_ERR_INVALID_ARG;
+    lock.lock();
     if (g_static_owner[dev] != c) c->dirty = true;   // another chain's table is there
   }
   if (c->dirty) {
-    e = cudaMemcpy(c->d_ws + CH_WS_HEAD, c->ops.data(), c->ops.size() * sizeof(ChainOp),
-                   cudaMemcpyHostToDevice);
+    // The op table goes up on the run's own stream, so it lands after the
+    // work queued there before (an earlier run that still reads the table)
+    // and before this run's kernel.  The source is pageable host memory:
+    // the copy stages it before returning, so later edits of the chain
+    // cannot reach the device copy.  A capture would record a copy from
+    // pageable memory, which is not allowed: refuse it.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    if (cap != cudaStreamCaptureStatusNone) return QMV_ERR_UNSUPPORTED;
+    e = cudaMemcpyAsync(c->d_ws + CH_WS_HEAD, c->ops.data(), c->ops.size() * sizeof(ChainOp),
+                        cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return record_cuda_error(e);
     c->dirty = false;
     if (c->static_dev >= 0) g_static_owner[c->static_dev] = c;
   }
+  if (lock.owns_lock()) lock.unlock();
   const ChainLayout L = chain_layout(c->max_K);
   static thread_local int set_dev = -1;
   static thread_local int set_smem = 0;
@@ -627,7 +655,10 @@ int qmv_chain_info(const qmv_chain* c, int* n_ops, int* n_barriers, int* smem_by
 
 int qmv_chain_destroy(qmv_chain* c) {
   if (!chain_ok(c)) return QMV_ERR_INVALID_ARG;
-  if (c->static_dev >= 0 && g_static_owner[c->static_dev] == c) g_static_owner[c->static_dev] = nullptr;
+  if (c->static_dev >= 0) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_owner[c->static_dev] == c) g_static_owner[c->static_dev] = nullptr;
+  }
   c->magic = 0;
   delete c;
   return QMV_OK;

@@ -300,12 +300,15 @@ QMV_API int qmv_chain_create(qmv_chain **out, int max_ops, void *d_workspace,
  * live in the library's own scratch array (a file-scope device array, one per
  * device, room for 1024 ops), so neither the caller nor the library allocates
  * device memory for it.  The source pages have no counterpart: it is an interface
- * variant of qmv_chain_create.  The array's address is looked up once per
- * device; the chain must run on the device that was current here.  Every run
- * clears the barrier words; a run after another chain used the array re-copies
- * this chain's op table.  Chains made this way share the array: runs of two of
- * them that overlap in time race (and so would a run overlapping its own
- * earlier run on another stream).
+ * variant of qmv_chain_create.  The array's address is looked up here, once per
+ * device (host bookkeeping behind a lock, so chains may be made and run from
+ * several host threads); the chain must run on the device that was current
+ * here.  Every run clears the barrier words; a run after another chain used
+ * the array re-copies this chain's op table on the run's stream, so runs of
+ * such chains queued one after another on one stream are ordered.  Chains
+ * made this way share the array: runs of two of them that overlap in time
+ * on the GPU (different streams) race, and so would a run overlapping its
+ * own earlier run on another stream.
  * Errors: INVALID_ARG (NULL, max_ops < 1), UNSUPPORTED (max_ops > 1024), CUDA.
  */
 QMV_API int qmv_chain_create_no_alloc(qmv_chain **out, int max_ops);
@@ -326,12 +329,15 @@ QMV_API int qmv_chain_add_fused_rmsnorm_gemv(qmv_chain *c, const qmv_pack *p, co
 /*
  * qmv_chain_run -- run every op of the chain, in order, as one cooperative
  * launch of one CTA per SM on `stream` (INVALID_ARG for a chain from
- * qmv_chain_create_no_alloc run on another device).  The first run after ops were added
- * copies the op table to the workspace synchronously; later runs only clear
- * the barrier words (an async memset) and launch, and can be captured in a
- * CUDA graph.  Two runs of chains that share a workspace must not overlap.
- * A bounded device wait that runs out shows in qmv_device_error.
- * Errors: INVALID_ARG, UNSUPPORTED (kernel does not fit an SM), CUDA.
+ * qmv_chain_create_no_alloc run on another device).  The first run after ops
+ * were added copies the op table to the workspace with an asynchronous copy
+ * on `stream` (ordered after the work queued there before); a run that needs
+ * that copy while `stream` is capturing returns UNSUPPORTED.  Later runs only
+ * clear the barrier words (an async memset) and launch.  Two runs of chains
+ * that share a workspace must not overlap on the GPU.  A bounded device wait
+ * that runs out shows in qmv_device_error.
+ * Errors: INVALID_ARG, UNSUPPORTED (kernel does not fit an SM, or a table
+ * copy during stream capture), CUDA.
  */
 QMV_API int qmv_chain_run(qmv_chain *c, void *stream);
 

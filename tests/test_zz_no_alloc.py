@@ -50,6 +50,31 @@ def test_no_alloc_chain_equals_workspace_chain_twice():
     assert q.qmv_device_error(clear=True) == 0
 
 
+def test_no_alloc_chains_alternate_on_one_stream():
+    """Two no-alloc chains queued one after another on a side stream (no
+    synchronisation between the runs): each run's op-table copy is ordered on
+    that stream after the other chain's kernel, so both keep their results."""
+    q = qmv()
+    A = Mat("na2.A", 2048, 2048, 2, 32)
+    B = Mat("na2.B", 2560, 2048, 4, 32)
+    x = to_dev(acts("na2", 1, 2048)[0])
+    ya = torch.zeros(1, 2048, dtype=torch.float32, device="cuda")
+    yb = torch.zeros(1, 2560, dtype=torch.float32, device="cuda")
+    ca = q.Chain(1, no_alloc=True).add_gemv(A.pack, x, ya)
+    cb = q.Chain(1, no_alloc=True).add_gemv(B.pack, x, yb)
+    ref_a, ref_b = q.qmv_gemv(A.pack, x), q.qmv_gemv(B.pack, x)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(4):
+            ca.run(s)
+            cb.run(s)
+    s.synchronize()
+    assert torch.equal(_bits(ya), _bits(ref_a))
+    assert torch.equal(_bits(yb), _bits(ref_b))
+    assert q.qmv_device_error(clear=True) == 0
+
+
 def test_no_alloc_rejects_oversize():
     q = qmv()
     with pytest.raises(q.QmvError) as e:
