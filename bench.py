@@ -1,34 +1,33 @@
 """Benchmark: effective HBM GB/s of the weight-only mixed-bit decode matvecs.
 
-Workload (one "step"): one synthetic decode layer at M = 1, d_model 2048 --
-  residual-add + RMSNorm fused into the q/k/v matvec  (int4, 2560 x 2048, group 32)
-  o_proj                                             (int4, 2048 x 2048, group 32)
-  residual-add + RMSNorm fused into gate/up          (int2, 16384 x 2048, group 32)
-  down                                               (int2, 2048 x 8192, group 32)
-= 21,037,056 packed bytes (codes + fp16 scales) per layer, 4 kernel launches.
-Each matvec reads the previous one's fp16 output, as in a decode loop (the
-attention and the gated activation between them are not part of this path:
-o_proj reads the first 2048 q/k/v outputs, down the first 8192 gate/up
-outputs), and a layer's outputs (down's y, the residual h2) are the next
-layer's inputs.
-`--layers L` distinct layers are resident (default 32, 673 MB, > 5x L2) and
-the steps walk through them in turn, so every step reads its weights from
-HBM (inputs larger than L2; no flush needed).
+Timed step: ONE FULL DECODE TOKEN at M = 1 (the synthetic mixed-bit model of
+30 layers, d_model 2048, d_ff 16384), every matvec reading the previous one's
+output, as one CUDA graph with programmatic dependent launch:
+  int8 per-row-scaled per-layer-embedding projection 2048 x 2048 (once)
+  30 x [ residual-add + RMSNorm fused into q/k/v   int4 2560 x 2048, group 32
+         o_proj                                   int4 2048 x 2048
+         residual-add + RMSNorm fused into gate/up int2 32768 x 2048
+         down                                     int2 2048 x 16384 ]
+  lm_head                                          int2 262144 x 2048, group 32
+= 1,274,941,440 packed bytes (codes + fp16 scales) per token, 122 launches.
+The weights (1.27 GB) are ten times the L2, so every step reads them from HBM.
+K steps replay the token graph exactly K times, whatever K is.
 
-value = packed bytes of all timed steps / device time (CUDA events on the
-launch stream), i.e. effective GB/s; `tok_per_s_equiv` = layers per second.
-`e2e` is the same metric with the step's activations copied host->device from
-pinned memory and the outputs read back inside the timed region.
+value = packed bytes of the K tokens / device time (CUDA events on the launch
+stream, max over ranks): effective GB/s.  `tok_per_s_equiv` = tokens / s.
+`step_ms` gives the median, p10 and p90 of the per-step times.  `e2e` is the
+same metric with the token's inputs (embedding row, residual) copied host ->
+device from pinned memory and the fp32 logits copied back inside every step.
 
-Outside the timed region the line also reports: `chain` (the same layers as
-one persistent cooperative launch), `token` (one full decode token: the int8
-per-layer-embedding projection, 30 layers with d_ff 16384 and the int2
-lm_head 262144 x 2048, 1,274,941,440 bytes, 122 dependent launches in one
-graph) and `prefill` (the int2 FFN at d_model 4096 as chunks of M = 1, 4, 8,
-16, 64, 128 tokens).
+Outside the timed region, each with the median, p10 and p90 of interleaved
+repeats: `c1` (the fused RMSNorm + int2 1024 x 1024 matvec, 512 resident
+copies), `c2` (the decode layer at d_ff 8192, 32 resident layers), `c4` (the
+int2 FFN at d_model 4096 as prefill chunks of M = 1..128), `c5` (the mixed
+int4/int8 set at d_model 5376 for M = 1, 8, 32) and `chain` (the decode layers
+as one persistent launch).
 
-`--impl reference` times the CPU oracle (single-threaded C, the definition
-the GPU path is checked against) on a bounded sample of the same workload.
+`--impl reference` times the CPU oracle (single-threaded C, the definition the
+GPU path is checked against) on a bounded row sample of the same token.
 """
 from __future__ import annotations
 
@@ -45,25 +44,41 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
-D_MODEL, D_FF = 2048, 8192
-LAYER = [  # name, N, K, bits, group, fused prologue
-    ("qkv", 2560, D_MODEL, 4, 32, True),
-    ("o", D_MODEL, D_MODEL, 4, 32, False),
-    ("gateup", 2 * D_FF, D_MODEL, 2, 32, True),
-    ("down", D_MODEL, D_FF, 2, 32, False),
-]
-DOMINANT = "gateup"
 METRIC = "effective HBM GB/s (% of GB300 peak) and equiv. decode tok/s per weight set"
 SEED = 20261202
+EPS = 1e-6
+D_MODEL = 2048
+
+# the full decode token (the timed step)
+TOKEN_LAYERS = 30
+TOKEN_FF = 16384
+TOKEN_LAYER = [  # name, N, K, bits, group, fused prologue
+    ("qkv", 2560, D_MODEL, 4, 32, True),
+    ("o", D_MODEL, D_MODEL, 4, 32, False),
+    ("gateup", 2 * TOKEN_FF, D_MODEL, 2, 32, True),
+    ("down", D_MODEL, TOKEN_FF, 2, 32, False),
+]
+PLE = ("ple", D_MODEL, D_MODEL, 8, D_MODEL)
+LM_HEAD = ("lm_head", 262144, D_MODEL, 2, 32)
+DOMINANT = "gateup"
+
+# the decode layer at d_ff 8192 (block c2)
+LAYER_FF = 8192
+LAYER = [("qkv", 2560, D_MODEL, 4, 32, True), ("o", D_MODEL, D_MODEL, 4, 32, False),
+         ("gateup", 2 * LAYER_FF, D_MODEL, 2, 32, True), ("down", D_MODEL, LAYER_FF, 2, 32, False)]
+
+# what the path reads and computes in: the JSON line's "dtype" is the
+# arithmetic type (fp32 sums of exact products), this names the formats
+FORMATS = "int2/int4/int8 codes, fp16 scales and activations, fp32 accumulation"
 
 
 def packed_bytes(N, K, bits, group):
     return N * K * bits // 8 + N * (K // group) * 2
 
 
-# what the path reads and computes in: the JSON line's "dtype" is the
-# arithmetic type (fp32 sums of exact products), this names the formats
-FORMATS = "int2/int4 codes, fp16 scales and activations, fp32 accumulation"
+TOKEN_BYTES = (TOKEN_LAYERS * sum(packed_bytes(N, K, b, g) for _, N, K, b, g, _ in TOKEN_LAYER)
+               + packed_bytes(*PLE[1:]) + packed_bytes(*LM_HEAD[1:]))
+TOKEN_LAUNCHES = 4 * TOKEN_LAYERS + 2
 LAYER_BYTES = sum(packed_bytes(N, K, b, g) for _, N, K, b, g, _ in LAYER)
 
 
@@ -90,6 +105,13 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def stats(ms_list):
+    """median, p10, p90 of a list of times (ms)"""
+    a = np.asarray(ms_list, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
 
 
 def dist_init():
@@ -140,6 +162,7 @@ class Clocks:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
                                        "-lms", "100", "-i", str(self.idx())],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)   # let the sampler start before the timed work
         except Exception:
             self.p = None
 
@@ -179,35 +202,150 @@ class Clocks:
                 "samples": len(mhz)}
 
 
-# ----------------------------------------------------------------- GPU arm --
+# ----------------------------------------------------------- GPU helpers --
 
-def build_layers(L, dev):
+def make_pack(qmv, dev, tag, N, K, bits, group):
+    import synth
+    codes = synth.codes(SEED, tag, N, K, bits, device=dev)
+    scales = synth.scales(SEED, tag, N, K // group, device=dev)
+    p = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
+    del codes, scales
+    return p
+
+
+def dev_f16(dev, tag, shape, mean=0.0, std=1.0, outliers=False):
     import torch
 
     import synth
-    from bit_weight_only_packed_gb300 import qmv
-    layers = []
-    for li in range(L):
-        lay = {}
-        for name, N, K, bits, group, fused in LAYER:
-            codes = synth.codes(SEED, f"L{li}.{name}", N, K, bits, device=dev)
-            scales = synth.scales(SEED, f"L{li}.{name}", N, K // group, device=dev)
-            lay[name] = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
-            del codes, scales
-        layers.append(lay)
+    a = synth.normal_f16(SEED, tag, shape, mean=mean, std=std, outlier_every=1000 if outliers else 0)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def capture(stream, fn, warm=2):
+    """Run fn() `warm` times (first calls set kernel attributes), then capture
+    it once as a CUDA graph on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
     torch.cuda.synchronize()
-    return layers
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    return g
 
 
-def host_inputs():
-    import synth
-    x = synth.normal_f16(SEED, "bench.x", (1, D_MODEL))
-    r = synth.normal_f16(SEED, "bench.r", (1, D_MODEL))
-    g1 = synth.normal_f16(SEED, "bench.g1", (D_MODEL,), mean=1.0, std=0.1)
-    g2 = synth.normal_f16(SEED, "bench.g2", (D_MODEL,), mean=1.0, std=0.1)
-    attn = synth.normal_f16(SEED, "bench.attn", (1, D_MODEL))
-    act = synth.normal_f16(SEED, "bench.act", (1, D_FF))
-    return dict(x=x, r=r, g1=g1, g2=g2, attn=attn, act=act)
+def replay_timed(stream, g, reps):
+    """reps replays of g, one event pair around each: list of ms."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def interleaved(stream, items, rounds):
+    """items: {name: graph}.  `rounds` rounds, each replaying every graph once
+    in turn (A/B interleaving): {name: [ms per replay]}."""
+    out = {k: [] for k in items}
+    for _ in range(rounds):
+        for k, g in items.items():
+            out[k] += replay_timed(stream, g, 1)
+    return out
+
+
+# ------------------------------------------------------ the decode token --
+
+class Token:
+    """One decode token's packs and buffers (config: 30 layers, d_model 2048,
+    d_ff 16384, the embedding projection and the int2 lm_head)."""
+
+    def __init__(self, qmv, dev):
+        import torch
+
+        import synth
+        self.qmv = qmv
+        self.layers = [{name: make_pack(qmv, dev, f"tok.L{li}.{name}", N, K, b, g)
+                        for name, N, K, b, g, _ in TOKEN_LAYER} for li in range(TOKEN_LAYERS)]
+        self.ple = make_pack(qmv, dev, "tok.ple", *PLE[1:])
+        self.head = make_pack(qmv, dev, "tok.lm_head", *LM_HEAD[1:])
+        f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
+        # the token's inputs side by side (embedding row e, residual r), so an
+        # end-to-end step moves them with one host -> device copy
+        self.io = torch.empty(2 * D_MODEL, dtype=torch.float16, device=dev)
+        self.e = self.io[:D_MODEL].view(1, D_MODEL)
+        self.r = self.io[D_MODEL:].view(1, D_MODEL)
+        self.host_in = np.concatenate([synth.normal_f16(SEED, "tok.embed", (D_MODEL,)),
+                                       synth.normal_f16(SEED, "tok.r", (D_MODEL,))])
+        self.io.copy_(torch.from_numpy(self.host_in))
+        self.g1 = dev_f16(dev, "tok.g1", (D_MODEL,), mean=1.0, std=0.1)
+        self.g2 = dev_f16(dev, "tok.g2", (D_MODEL,), mean=1.0, std=0.1)
+        self.x, self.h, self.yq, self.yo = f16(D_MODEL), f16(D_MODEL), f16(2560), f16(D_MODEL)
+        self.ygu = f16(2 * TOKEN_FF)
+        self.logits = torch.empty(1, LM_HEAD[1], dtype=torch.float32, device=dev)
+
+    def run(self, stream):
+        """ple -> 30 x (fused qkv -> o -> fused gate/up -> down) -> lm_head:
+        122 launches, each reading the previous one's output."""
+        q = self.qmv
+        F16, FAST = q.QMV_F16, q.QMV_FAST
+        q.qmv_gemv(self.ple, self.e, y=self.x, y_dtype=F16, mode=FAST, stream=stream)
+        for lay in self.layers:
+            q.qmv_fused_rmsnorm_gemv(lay["qkv"], self.x, self.r, self.g1, EPS, h_out=self.h, y=self.yq,
+                                     y_dtype=F16, mode=FAST, stream=stream)
+            q.qmv_gemv(lay["o"], self.yq[:, :D_MODEL], y=self.yo, y_dtype=F16, mode=FAST, stream=stream)
+            q.qmv_fused_rmsnorm_gemv(lay["gateup"], self.yo, self.h, self.g2, EPS, h_out=self.r, y=self.ygu,
+                                     y_dtype=F16, mode=FAST, stream=stream)
+            q.qmv_gemv(lay["down"], self.ygu[:, :TOKEN_FF], y=self.x, y_dtype=F16, mode=FAST, stream=stream)
+        q.qmv_gemv(self.head, self.x, y=self.logits, mode=FAST, stream=stream)
+
+    def run_dominant(self, stream):
+        """The 30 fused RMSNorm + gate/up launches alone (same buffers)."""
+        q = self.qmv
+        for lay in self.layers:
+            q.qmv_fused_rmsnorm_gemv(lay["gateup"], self.yo, self.h, self.g2, EPS, h_out=self.r, y=self.ygu,
+                                     y_dtype=q.QMV_F16, mode=q.QMV_FAST, stream=stream)
+
+
+# ------------------------------------------------------------ side blocks --
+
+def block_c1(qmv, dev, copies=512):
+    """Config 1: fused residual + RMSNorm + int2 1024 x 1024 (group 32), M = 1,
+    over `copies` resident packs (168 MB > L2), launched back to back."""
+    import torch
+    N = K = 1024
+    packs = [make_pack(qmv, dev, f"c1.{i}", N, K, 2, 32) for i in range(copies)]
+    x = dev_f16(dev, "c1.x", (1, K))
+    r = dev_f16(dev, "c1.r", (1, K))
+    g = dev_f16(dev, "c1.g", (K,), mean=1.0, std=0.1)
+    h = torch.empty(1, K, dtype=torch.float16, device=dev)
+    y = torch.empty(1, N, dtype=torch.float32, device=dev)
+
+    def fn(stream):
+        for p in packs:
+            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, EPS, h_out=h, y=y, mode=qmv.QMV_FAST, stream=stream)
+    return fn, copies, packed_bytes(N, K, 2, 32), (packs, x, r, g, h, y)
+
+
+def block_c2(qmv, dev, L=32):
+    """Config 2: the decode layer at d_ff 8192 (four dependent launches),
+    L distinct layers resident (673 MB > L2), one graph of all L."""
+    import torch
+    layers = [{name: make_pack(qmv, dev, f"L{li}.{name}", N, K, b, g) for name, N, K, b, g, _ in LAYER}
+              for li in range(L)]
+    f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
+    b = dict(x=dev_f16(dev, "bench.x", (1, D_MODEL)), r=dev_f16(dev, "bench.r", (1, D_MODEL)),
+             g1=dev_f16(dev, "bench.g1", (D_MODEL,), mean=1.0, std=0.1),
+             g2=dev_f16(dev, "bench.g2", (D_MODEL,), mean=1.0, std=0.1),
+             h=f16(D_MODEL), y_qkv=f16(2560), y_o=f16(D_MODEL), y_gu=f16(2 * LAYER_FF))
+    return layers, b
 
 
 def layer_ops(lay, b):
@@ -217,162 +355,106 @@ def layer_ops(lay, b):
     return [("fused", lay["qkv"], b["x"], b["r"], b["g1"], b["h"], b["y_qkv"]),
             ("gemv", lay["o"], b["y_qkv"][:, :D_MODEL], None, None, None, b["y_o"]),
             ("fused", lay["gateup"], b["y_o"], b["h"], b["g2"], b["r"], b["y_gu"]),
-            ("gemv", lay["down"], b["y_gu"][:, :D_FF], None, None, None, b["x"])]
+            ("gemv", lay["down"], b["y_gu"][:, :LAYER_FF], None, None, None, b["x"])]
 
 
 def run_layer(qmv, lay, b, stream):
-    """One decode layer: 4 launches on `stream`, fp16 outputs."""
     for kind, p, x, r, g, h, y in layer_ops(lay, b):
         if kind == "fused":
-            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, 1e-6, h_out=h, y=y, y_dtype=qmv.QMV_F16,
+            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, EPS, h_out=h, y=y, y_dtype=qmv.QMV_F16,
                                        mode=qmv.QMV_FAST, stream=stream)
         else:
             qmv.qmv_gemv(p, x, y=y, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
 
 
-def chain_layers(qmv, layers, b, n):
-    """The same n layers (rotating over the resident ones) as one persistent chain."""
-    ch = qmv.Chain(4 * n)
-    for i in range(n):
-        for kind, p, x, r, g, h, y in layer_ops(layers[i % len(layers)], b):
+def chain_layers(qmv, layers, b):
+    """The same layers as one persistent chain."""
+    ch = qmv.Chain(4 * len(layers))
+    for lay in layers:
+        for kind, p, x, r, g, h, y in layer_ops(lay, b):
             if kind == "fused":
-                ch.add_fused_rmsnorm_gemv(p, x, r, g, 1e-6, h, y, y_dtype=qmv.QMV_F16)
+                ch.add_fused_rmsnorm_gemv(p, x, r, g, EPS, h, y, y_dtype=qmv.QMV_F16)
             else:
                 ch.add_gemv(p, x, y, y_dtype=qmv.QMV_F16)
     return ch
 
 
-def _graph_time(stream, build, reps):
-    """Capture build() once as a CUDA graph, replay it reps times; ms per replay."""
-    import torch
-    with torch.cuda.stream(stream):
-        build()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        build()
-    with torch.cuda.stream(stream):
-        g.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    return reduce_max(e0.elapsed_time(e1)) / reps
-
-
-# Chunked-prefill sweep on the int2 FFN at d_model 4096: gate/up (two
+# Config 4: chunked prefill on the int2 FFN at d_model 4096: gate/up (two
 # 14336 x 4096 matrices as one pack) and down 4096 x 14336, group 32.
 FFN4 = [("gateup", 2 * 14336, 4096), ("down", 4096, 14336)]
 FFN4_MS = (1, 4, 8, 16, 64, 128)
+FFN4_BYTES = sum(packed_bytes(N, K, 2, 32) for _, N, K in FFN4)
 
 
-def prefill_sweep(qmv, dev, stream, copies=4, reps=8):
+def block_c4(qmv, dev, copies=4):
     """The FFN's two matrices as chunks of M tokens (qmv_chunk_gemm, fast
     mode, fp16 outputs), weights rotated over `copies` resident sets (> L2):
-    M <= 16 (and 32) run the K-order-fixed CUDA-core tiles, every column equal
-    to the M = 1 result; M >= 64 the tcgen05 tensor tiles.  Per M: us per FFN,
-    tokens/s, effective GB/s, TFLOP/s."""
+    M <= 16 run the K-order-fixed CUDA-core tiles, every column equal to the
+    M = 1 result; M >= 64 the tcgen05 tensor tiles.  {M: fn(stream)}."""
     import torch
-
-    import synth
-    sets = []
-    for c in range(copies):
-        st = {}
-        for name, N, K in FFN4:
-            codes = synth.codes(SEED, f"ffn4.{c}.{name}", N, K, 2, device=dev)
-            scales = synth.scales(SEED, f"ffn4.{c}.{name}", N, K // 32, device=dev)
-            st[name] = qmv.Pack(N, K, 2, 32).pack_weights(codes, scales)
-            del codes, scales
-        sets.append(st)
-    nbytes = sum(packed_bytes(N, K, 2, 32) for _, N, K in FFN4)
-    flop1 = 2.0 * sum(N * K for _, N, K in FFN4)
-    out = {}
+    sets = [{name: make_pack(qmv, dev, f"ffn4.{c}.{name}", N, K, 2, 32) for name, N, K in FFN4}
+            for c in range(copies)]
+    fns = {}
     for M in FFN4_MS:
-        xs = {K: torch.from_numpy(synth.normal_f16(SEED, f"bench.ffn4.{M}.{K}", (M, K))).to(dev)
-              for _, _, K in FFN4}
+        xs = {K: dev_f16(dev, f"bench.ffn4.{M}.{K}", (M, K)) for _, _, K in FFN4}
         ys = {name: torch.empty(M, N, dtype=torch.float16, device=dev) for name, N, _ in FFN4}
 
-        def build():
+        def fn(stream, xs=xs, ys=ys):
             for st in sets:
                 for name, N, K in FFN4:
                     qmv.qmv_chunk_gemm(st[name], xs[K], y=ys[name], y_dtype=qmv.QMV_F16,
                                        mode=qmv.QMV_FAST, stream=stream)
-
-        ms = _graph_time(stream, build, reps) / copies
-        out[f"M{M}"] = {"us_per_ffn": round(ms * 1e3, 2), "tok_per_s": round(M / (ms * 1e-3), 1),
-                        "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                        "tflops": round(M * flop1 / (ms * 1e-3) / 1e12, 2)}
-    del sets
-    return out, nbytes
+        fns[M] = (fn, (xs, ys))
+    return fns, copies, sets
 
 
-# One full decode token, M = 1: the per-layer-embedding projection (one int8
-# per-row-scaled 2048 x 2048 matvec per token), 30 layers shaped as the decode
-# layer with d_ff 16384, then the int2 lm_head 262144 x 2048.
-TOKEN_LAYERS = 30
-TOKEN_LAYER = [("qkv", 2560, D_MODEL, 4, 32, True), ("o", D_MODEL, D_MODEL, 4, 32, False),
-               ("gateup", 2 * 16384, D_MODEL, 2, 32, True), ("down", D_MODEL, 16384, 2, 32, False)]
-PLE = ("ple", D_MODEL, D_MODEL, 8, D_MODEL)
-LM_HEAD = ("lm_head", 262144, D_MODEL, 2, 32)
+# Config 5: large batched decode in mixed int4/int8 at d_model 5376, d_ff 21504:
+# q/k/v int8 per-row-scaled (8192 + 2048 + 2048 rows, one pack), gate/up int4
+# 43008 x 5376, down int4 5376 x 21504, lm_head int4 262144 x 5376 (group 32),
+# activations with 0.1 % outliers at +-50, the fused RMSNorm prologue before
+# q/k/v and gate/up.
+C5_D, C5_FF = 5376, 21504
+C5_SET = [("qkv", 8192 + 2048 + 2048, C5_D, 8, C5_D), ("gateup", 2 * C5_FF, C5_D, 4, 32),
+          ("down", C5_D, C5_FF, 4, 32), ("lm_head", 262144, C5_D, 4, 32)]
+C5_MS = (1, 8, 32)
+C5_BYTES = sum(packed_bytes(N, K, b, g) for _, N, K, b, g in C5_SET)
 
 
-def token_chain(qmv, dev, stream, reps=4):
-    """One decode token through the whole chain (the embedding projection, 4
-    matvecs a layer x 30, the lm_head), each matvec reading the previous one's
-    output, as one CUDA graph with programmatic dependent launch.  Returns (ms
-    per token, packed bytes per token)."""
+def block_c5(qmv, dev):
+    """One pass over the set per call: fused RMSNorm + q/k/v (x, r) -> fused
+    RMSNorm + gate/up (h, x) -> down (the gated activation is not on this
+    path: down reads a separate M x 21504 input at M > 1, the first 21504
+    gate/up outputs at M = 1) -> lm_head (down's output).  {M: fn}."""
     import torch
+    packs = {name: make_pack(qmv, dev, f"c5.{name}", N, K, b, g) for name, N, K, b, g in C5_SET}
+    g1 = dev_f16(dev, "c5.g1", (C5_D,), mean=1.0, std=0.1)
+    g2 = dev_f16(dev, "c5.g2", (C5_D,), mean=1.0, std=0.1)
+    fns = {}
+    for M in C5_MS:
+        x = dev_f16(dev, f"c5.{M}.x", (M, C5_D), outliers=True)
+        r = dev_f16(dev, f"c5.{M}.r", (M, C5_D), outliers=True)
+        act = dev_f16(dev, f"c5.{M}.act", (M, C5_FF), outliers=True)
+        h = torch.empty(M, C5_D, dtype=torch.float16, device=dev)
+        h2 = torch.empty(M, C5_D, dtype=torch.float16, device=dev)
+        yq = torch.empty(M, 12288, dtype=torch.float16, device=dev)
+        ygu = torch.empty(M, 2 * C5_FF, dtype=torch.float16, device=dev)
+        yd = torch.empty(M, C5_D, dtype=torch.float16, device=dev)
+        logits = torch.empty(M, 262144, dtype=torch.float16, device=dev)
 
-    import synth
-    layers = []
-    for li in range(TOKEN_LAYERS):
-        lay = {}
-        for name, N, K, bits, group, _ in TOKEN_LAYER:
-            codes = synth.codes(SEED, f"tok.L{li}.{name}", N, K, bits, device=dev)
-            scales = synth.scales(SEED, f"tok.L{li}.{name}", N, K // group, device=dev)
-            lay[name] = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
-            del codes, scales
-        layers.append(lay)
-    def one(spec, tag):
-        _, N, K, bits, group = spec
-        codes = synth.codes(SEED, tag, N, K, bits, device=dev)
-        scales = synth.scales(SEED, tag, N, K // group, device=dev)
-        return qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
-    ple = one(PLE, "tok.ple")
-    head = one(LM_HEAD, "tok.lm_head")
-    N = LM_HEAD[1]
-    nbytes = TOKEN_LAYERS * sum(packed_bytes(N_, K_, b, g) for _, N_, K_, b, g, _ in TOKEN_LAYER) + \
-        packed_bytes(*PLE[1:]) + packed_bytes(*LM_HEAD[1:])
-    f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
-    x = torch.from_numpy(synth.normal_f16(SEED, "tok.x", (1, D_MODEL))).to(dev)
-    r = torch.from_numpy(synth.normal_f16(SEED, "tok.r", (1, D_MODEL))).to(dev)
-    g1 = torch.from_numpy(synth.normal_f16(SEED, "tok.g1", (D_MODEL,), mean=1.0, std=0.1)).to(dev)
-    g2 = torch.from_numpy(synth.normal_f16(SEED, "tok.g2", (D_MODEL,), mean=1.0, std=0.1)).to(dev)
-    e = torch.from_numpy(synth.normal_f16(SEED, "tok.embed", (1, D_MODEL))).to(dev)
-    h, yq, yo, ygu = f16(D_MODEL), f16(2560), f16(D_MODEL), f16(2 * 16384)
-    logits = torch.empty(1, N, dtype=torch.float32, device=dev)
+        def fn(stream, M=M, x=x, r=r, act=act, h=h, h2=h2, yq=yq, ygu=ygu, yd=yd, logits=logits):
+            F16, FAST = qmv.QMV_F16, qmv.QMV_FAST
+            qmv.qmv_fused_rmsnorm_gemv(packs["qkv"], x, r, g1, EPS, h_out=h, y=yq, y_dtype=F16, mode=FAST,
+                                       stream=stream)
+            qmv.qmv_fused_rmsnorm_gemv(packs["gateup"], h, x, g2, EPS, h_out=h2, y=ygu, y_dtype=F16,
+                                       mode=FAST, stream=stream)
+            qmv.qmv_chunk_gemm(packs["down"], ygu[:, :C5_FF] if M == 1 else act, y=yd, y_dtype=F16,
+                               mode=FAST, stream=stream)
+            qmv.qmv_chunk_gemm(packs["lm_head"], yd, y=logits, y_dtype=F16, mode=FAST, stream=stream)
+        fns[M] = (fn, (x, r, act, h, h2, yq, ygu, yd, logits))
+    return fns, packs
 
-    def build():
-        qmv.qmv_gemv(ple, e, y=x, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
-        for lay in layers:
-            qmv.qmv_fused_rmsnorm_gemv(lay["qkv"], x, r, g1, 1e-6, h_out=h, y=yq, y_dtype=qmv.QMV_F16,
-                                       mode=qmv.QMV_FAST, stream=stream)
-            qmv.qmv_gemv(lay["o"], yq[:, :D_MODEL], y=yo, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
-            qmv.qmv_fused_rmsnorm_gemv(lay["gateup"], yo, h, g2, 1e-6, h_out=r, y=ygu, y_dtype=qmv.QMV_F16,
-                                       mode=qmv.QMV_FAST, stream=stream)
-            qmv.qmv_gemv(lay["down"], ygu[:, :16384], y=x, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST,
-                         stream=stream)
-        qmv.qmv_gemv(head, x, y=logits, mode=qmv.QMV_FAST, stream=stream)
 
-    ms = _graph_time(stream, build, reps)
-    del layers, head, ple
-    return ms, nbytes
-
+# ----------------------------------------------------------------- GPU arm --
 
 def gpu_arm(args, rank, world, local):
     import torch
@@ -381,72 +463,50 @@ def gpu_arm(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
-    L = args.layers
-    layers = build_layers(L, dev)
-    hin = host_inputs()
-    # x, r, g1, g2 side by side in one device buffer (views), so that an
-    # end-to-end step moves its inputs with one host->device copy and its two
-    # outputs (x, r) with one device->host copy
-    io = torch.empty(4 * D_MODEL, dtype=torch.float16, device=dev)
-    b = {k: io[i * D_MODEL:(i + 1) * D_MODEL].view(1, D_MODEL) if k in ("x", "r") else io[i * D_MODEL:(i + 1) * D_MODEL]
-         for i, k in enumerate(("x", "r", "g1", "g2"))}
-    for k in ("x", "r", "g1", "g2"):
-        b[k].copy_(torch.from_numpy(hin[k]).reshape(b[k].shape))
-    f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
-    b.update(h=f16(D_MODEL), y_qkv=f16(2560), y_o=f16(D_MODEL), y_gu=f16(2 * D_FF))
     K, W = args.steps, args.warmup
-
     # dependent matvecs overlap through programmatic dependent launch
     qmv.qmv_set_pdl(True)
-    # warm-up through the plain API (first calls set kernel attributes)
-    with torch.cuda.stream(stream):
-        for i in range(W):
-            run_layer(qmv, layers[i % L], b, stream)
-    torch.cuda.synchronize()
 
-    # CUDA graphs remove the per-launch host cost: one graph per layer (a
-    # step) and one graph of all L layers (L steps); the dominant kernel
-    # alone over the L layers is a third graph, timed on its own.
-    g_one = []
-    for li in range(L):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            run_layer(qmv, layers[li], b, stream)
-        g_one.append(g)
-    g_all = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_all, stream=stream):
-        for li in range(L):
-            run_layer(qmv, layers[li], b, stream)
-    g_dom = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dom, stream=stream):
-        for li in range(L):
-            kind, p, x, r, g, h, y = layer_ops(layers[li], b)[2]
-            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, 1e-6, h_out=h, y=y, y_dtype=qmv.QMV_F16,
-                                       mode=qmv.QMV_FAST, stream=stream)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            g_all.replay()
-            g_dom.replay()
+    tok = Token(qmv, dev)
     torch.cuda.synchronize()
-
-    # ---- timed region: exactly K steps, device time ----
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            tok.run(stream)
+    torch.cuda.synchronize()
+    g_tok = capture(stream, lambda: tok.run(stream))
+    g_dom = capture(stream, lambda: tok.run_dominant(stream))
+    # the clock sampler runs from here: the untimed warm-up replays (W, and at
+    # least 0.5 s of them) keep the GPU under the same load just before the
+    # timed steps, which take only milliseconds
     clocks = Clocks()
     clocks.start()
+    t_warm = time.perf_counter()
+    n_warm = 0
+    while n_warm < W or time.perf_counter() - t_warm < 0.5:
+        with torch.cuda.stream(stream):
+            for _ in range(10):
+                g_tok.replay()
+        torch.cuda.synchronize()
+        n_warm += 10
+
+    # ---- timed region: exactly K token replays, device time ----
     barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for _ in range(K // L):
-            g_all.replay()
-        for li in range(K % L):
-            g_one[li].replay()
+        for a, b in ev:
+            a.record(stream)
+            g_tok.replay()
+            b.record(stream)
         t1.record(stream)
-        # the dominant kernel's own launches, same rotation over L layers
+        # the dominant kernel's own launches: the 30 fused gate/up of the
+        # token, same weights and buffers, right after the timed steps
+        reps = max(3, K // 4)
         d0 = torch.cuda.Event(enable_timing=True)
         d1 = torch.cuda.Event(enable_timing=True)
-        reps = max(1, K // L)
         d0.record(stream)
         for _ in range(reps):
             g_dom.replay()
@@ -455,71 +515,33 @@ def gpu_arm(args, rank, world, local):
     barrier()
     ck = clocks.stop()
     ms = t0.elapsed_time(t1)
-    dom_ms = d0.elapsed_time(d1) / (reps * L)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dom_ms = d0.elapsed_time(d1) / (reps * TOKEN_LAYERS)
     ms_max = reduce_max(ms)
 
     # ---- end to end through the public API: pinned host -> device -> host ----
-    pin = torch.from_numpy(np.concatenate([hin[k].reshape(-1) for k in ("x", "r", "g1", "g2")])).pin_memory()
-    outs = torch.empty(2 * D_MODEL, dtype=torch.float16).pin_memory()   # x, r
+    pin = torch.from_numpy(tok.host_in).pin_memory()
+    logits_host = torch.empty(tok.logits.shape, dtype=torch.float32).pin_memory()
     h2d = pin.numel() * pin.element_size()
-    d2h = outs.numel() * outs.element_size()
+    d2h = logits_host.numel() * logits_host.element_size()
+
+    def e2e_step():
+        tok.io.copy_(pin, non_blocking=True)
+        tok.run(stream)
+        logits_host.copy_(tok.logits, non_blocking=True)
+
+    g_e2e = capture(stream, e2e_step)
     KE = max(3, K // 2)
-
-    def e2e_step(li):
-        io.copy_(pin, non_blocking=True)
-        run_layer(qmv, layers[li], b, stream)
-        outs.copy_(io[:2 * D_MODEL], non_blocking=True)
-
-    # one graph per layer: the copies are memcpy nodes, run again on every replay
-    g_e2e = []
-    for li in range(L):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            e2e_step(li)
-        g_e2e.append(g)
-    torch.cuda.synchronize()
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(KE):
-            g_e2e[i % L].replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1))
+    e2e_ms = reduce_max(sum(replay_timed(stream, g_e2e, KE)))
     barrier()
-
-    # ---- the same layers as one persistent chain launch (L layers) ----
-    ch = chain_layers(qmv, layers, b, L)
-    reps = max(1, K // L)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            ch.run(stream)
-    torch.cuda.synchronize()
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        c0.record(stream)
-        for _ in range(reps):
-            ch.run(stream)
-        c1.record(stream)
-    torch.cuda.synchronize()
-    chain_ms = reduce_max(c0.elapsed_time(c1)) / (reps * L)
-    chain_info = ch.info()
-    ch.close()
-
-    # ---- the other configurations, outside the timed region ----
-    tok_ms, tok_bytes = token_chain(qmv, dev, stream)
-    torch.cuda.empty_cache()
-    prefill, ffn_bytes = prefill_sweep(qmv, dev, stream)
-    torch.cuda.empty_cache()
+    del g_e2e
 
     peak, peak_kind = peaks()
-    gbs = world * LAYER_BYTES * K / (ms_max * 1e-3) / 1e9
-    dom_bytes = packed_bytes(2 * D_FF, D_MODEL, 2, 32)
+    gbs = world * TOKEN_BYTES * K / (ms_max * 1e-3) / 1e9
+    dom_bytes = packed_bytes(2 * TOKEN_FF, D_MODEL, 2, 32)
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
-    traffic = measured_traffic("gemv_m1_fused_int2_16384x2048")
+    st = stats(step_ms)
     out = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -533,94 +555,187 @@ def gpu_arm(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded SplitMix64 codes/scales, Box-Muller fp16 activations)",
-        "config": {"workload": "synthetic decode layer, M=1, d_model 2048, d_ff 8192: "
-                               "fused RMSNorm+qkv int4 2560x2048, o int4 2048x2048, "
-                               "fused RMSNorm+gate/up int2 16384x2048, down int2 2048x8192",
-                   "formats": FORMATS,
-                   "layer_bytes": LAYER_BYTES, "resident_layers": L,
-                   "resident_bytes": LAYER_BYTES * L,
-                   "l2": "inputs larger than L2 (distinct layer weights rotated per step)",
+        "config": {"workload": "full decode token, M=1 (30 layers, d_model 2048, d_ff 16384): int8 per-row "
+                               "per-layer-embedding projection 2048x2048; 30 x (fused RMSNorm+qkv int4 "
+                               "2560x2048, o int4 2048x2048, fused RMSNorm+gate/up int2 32768x2048, down "
+                               "int2 2048x16384); int2 lm_head 262144x2048",
+                   "formats": FORMATS, "bytes_per_token": TOKEN_BYTES,
+                   "launches_per_token": TOKEN_LAUNCHES,
+                   "l2": "inputs larger than L2 (1.27 GB of distinct weights per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": round(100.0 * gbs / world / peak, 1),
         "tok_per_s_equiv": round(world * K / (ms_max * 1e-3), 1),
-        "gpu_launches": 4 * K,
+        "step_ms": {k: (round(v, 5) if isinstance(v, float) else v) for k, v in st.items()},
+        "gpu_launches": TOKEN_LAUNCHES * K,
         "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "traffic": traffic,
-                     "kernel": "gemv_m1 fused RMSNorm + int2 gate/up 16384x2048",
-                     "algorithmic_bytes": dom_bytes, "peak_source": peak_kind},
-        "e2e": {"value": round(world * LAYER_BYTES * KE / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                     "traffic": measured_traffic("gemv_m1_fused_int2_32768x2048"),
+                     "kernel": "fused RMSNorm + int2 gate/up 32768x2048 (M=1 pipeline)",
+                     "algorithmic_bytes": dom_bytes, "us_per_launch": round(dom_ms * 1e3, 3),
+                     "peak_source": peak_kind},
+        "e2e": {"value": round(world * TOKEN_BYTES * KE / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "tok_per_s": round(world * KE / (e2e_ms * 1e-3), 1)},
         "clocks": ck,
-        "chain": {"value": round(world * LAYER_BYTES / (chain_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                  "ms_per_step": round(chain_ms, 5), "layers_per_launch": L,
-                  "grid_barriers": chain_info["barriers"],
-                  "note": "same dependent layers as one persistent cooperative launch (qmv_chain_run); "
-                          "the headline value uses CUDA graphs with programmatic dependent launch"},
-        "token": {"workload": "one decode token, M=1: int8 per-row per-layer-embedding projection "
-                              "2048x2048, 30 layers (fused RMSNorm+qkv int4 2560x2048, o int4 2048x2048, "
-                              "fused RMSNorm+gate/up int2 32768x2048, down int2 2048x16384), int2 lm_head "
-                              "262144x2048",
-                  "bytes_per_token": tok_bytes, "ms_per_token": round(tok_ms, 4),
-                  "tok_per_s": round(world * 1e3 / tok_ms, 1),
-                  "gbs": round(world * tok_bytes / (tok_ms * 1e-3) / 1e9, 1),
-                  "launches_per_token": 4 * TOKEN_LAYERS + 2},
-        "prefill": dict(prefill, workload="chunked prefill on the int2 FFN, d_model 4096: gate/up "
-                        "28672x4096 + down 4096x14336 (bytes per FFN %d), qmv_chunk_gemm fast mode; "
-                        "M<=16 on the K-order-fixed CUDA-core tiles (each column equal to M=1), M>=64 on "
-                        "tcgen05 tensor tiles; 4 weight sets rotated (> L2)" % ffn_bytes),
     }
+    del g_tok, g_dom, tok
+    torch.cuda.empty_cache()
+    if args.blocks != "none":
+        out.update(side_blocks(qmv, dev, stream, args, world))
+    return out
+
+
+def side_blocks(qmv, dev, stream, args, world):
+    """The other configurations, outside the timed region: medians, p10 and
+    p90 of interleaved repeats."""
+    import torch
+    want = set(args.blocks.split(",")) if args.blocks != "all" else {"c1", "c2", "c4", "c5", "chain"}
+    out = {}
+    rounds = args.rounds
+
+    def summ(ms_list, units, nbytes, extra=None):
+        s = stats(ms_list)
+        med = s["median"]
+        d = {"ms_median": round(med, 5), "ms_p10": round(s["p10"], 5), "ms_p90": round(s["p90"], 5),
+             "gbs": round(world * nbytes * units / (med * 1e-3) / 1e9, 1), "repeats": s["n"]}
+        if extra:
+            d.update(extra(med))
+        return d
+
+    if "c1" in want:
+        fn, n, b1, keep = block_c1(qmv, dev)
+        g = capture(stream, lambda: fn(stream))
+        r = interleaved(stream, {"c1": g}, rounds)["c1"]
+        out["c1"] = dict(summ(r, n, b1, lambda m: {"us_per_matvec": round(m * 1e3 / n, 3)}),
+                         workload="fused RMSNorm + int2 1024x1024 g32, M=1, fp32 out; 512 resident copies "
+                                  "(168 MB > L2) back to back", bytes_per_matvec=b1)
+        del g, keep
+        torch.cuda.empty_cache()
+
+    if "c2" in want or "chain" in want:
+        layers, b = block_c2(qmv, dev)
+        L = len(layers)
+        items = {}
+        if "c2" in want:
+            items["c2"] = capture(stream, lambda: [run_layer(qmv, lay, b, stream) for lay in layers])
+        ch = None
+        if "chain" in want:
+            ch = chain_layers(qmv, layers, b)
+            items["chain"] = capture(stream, lambda: ch.run(stream))
+        r = interleaved(stream, items, rounds)
+        if "c2" in r:
+            out["c2"] = dict(summ(r["c2"], L, LAYER_BYTES,
+                                  lambda m: {"us_per_layer": round(m * 1e3 / L, 3),
+                                             "layers_per_s": round(world * L / (m * 1e-3), 1)}),
+                             workload="decode layer, M=1, d_model 2048, d_ff 8192: fused RMSNorm+qkv int4 "
+                                      "2560x2048, o int4 2048x2048, fused RMSNorm+gate/up int2 16384x2048, "
+                                      "down int2 2048x8192; 32 resident layers (673 MB > L2), one graph",
+                             bytes_per_layer=LAYER_BYTES)
+        if "chain" in r:
+            out["chain"] = dict(summ(r["chain"], L, LAYER_BYTES,
+                                     lambda m: {"us_per_layer": round(m * 1e3 / L, 3)}),
+                                workload="the c2 layers as one persistent cooperative launch (qmv_chain_run)",
+                                grid_barriers=ch.info()["barriers"])
+            ch.close()
+        del items, layers, b
+        torch.cuda.empty_cache()
+
+    if "c4" in want:
+        fns, copies, sets = block_c4(qmv, dev)
+        items = {M: capture(stream, lambda f=f: f(stream)) for M, (f, _) in fns.items()}
+        r = interleaved(stream, items, rounds)
+        flop1 = 2.0 * sum(N * K for _, N, K in FFN4)
+        c4 = {}
+        for M, ms_list in r.items():
+            c4[f"M{M}"] = summ(ms_list, copies, FFN4_BYTES, lambda m, M=M: {
+                "us_per_ffn": round(m * 1e3 / copies, 2),
+                "tok_per_s": round(world * M * copies / (m * 1e-3), 1),
+                "tflops": round(world * M * flop1 * copies / (m * 1e-3) / 1e12, 2)})
+        c4["workload"] = ("chunked prefill on the int2 FFN, d_model 4096: gate/up 28672x4096 + down "
+                          "4096x14336 (%d bytes per FFN), qmv_chunk_gemm fast mode, fp16 out; M<=16 on the "
+                          "K-order-fixed CUDA-core tiles, M>=64 on tcgen05 tensor tiles; 4 weight sets "
+                          "rotated (> L2)" % FFN4_BYTES)
+        out["c4"] = c4
+        del items, fns, sets
+        torch.cuda.empty_cache()
+
+    if "c5" in want:
+        fns, packs = block_c5(qmv, dev)
+        items = {M: capture(stream, lambda f=f: f(stream)) for M, (f, _) in fns.items()}
+        r = interleaved(stream, items, rounds)
+        c5 = {}
+        for M, ms_list in r.items():
+            c5[f"M{M}"] = summ(ms_list, 1, C5_BYTES, lambda m, M=M: {
+                "us_per_set": round(m * 1e3, 2), "tok_per_s": round(world * M / (m * 1e-3), 1)})
+        c5["workload"] = ("mixed int4/int8 set, d_model 5376, d_ff 21504: fused RMSNorm+qkv int8 per-row "
+                          "12288x5376, fused RMSNorm+gate/up int4 43008x5376, down int4 5376x21504, lm_head "
+                          "int4 262144x5376 (%d bytes per set, > L2), activations with 0.1%% outliers at "
+                          "+-50, fast mode, fp16 out" % C5_BYTES)
+        out["c5"] = c5
+        del items, fns, packs
+        torch.cuda.empty_cache()
     return out
 
 
 # ------------------------------------------------------------- CPU oracle --
 
-def oracle_sample(frac_rows: int):
-    """Host inputs of one layer, restricted to every `frac_rows`-th row."""
+def oracle_token_sample(every: int):
+    """Host inputs of one decode token, each matrix restricted to every
+    `every`-th row (distinct rows of all 122 matrices)."""
     import synth
-    hin = host_inputs()
-    mats = {}
-    for name, N, K, bits, group, fused in LAYER:
-        rows = np.arange(0, N, frac_rows)
-        codes = synth.codes(SEED, f"L0.{name}", N, K, bits, rows=rows).numpy()
-        scales = synth.scales(SEED, f"L0.{name}", N, K // group, rows=rows).numpy()
-        mats[name] = (codes, scales, group, fused, packed_bytes(len(rows), K, bits, group))
-    return hin, mats
+    e = synth.normal_f16(SEED, "tok.embed", (1, D_MODEL))
+    r = synth.normal_f16(SEED, "tok.r", (1, D_MODEL))
+    g1 = synth.normal_f16(SEED, "tok.g1", (D_MODEL,), mean=1.0, std=0.1)
+    g2 = synth.normal_f16(SEED, "tok.g2", (D_MODEL,), mean=1.0, std=0.1)
+    yo = synth.normal_f16(SEED, "tok.cpu.yo", (1, D_MODEL))
+    act = synth.normal_f16(SEED, "tok.cpu.act", (1, TOKEN_FF))
+
+    def mat(tag, N, K, bits, group):
+        rows = np.arange(0, N, every)
+        c = synth.codes(SEED, tag, N, K, bits, rows=rows).numpy()
+        s = synth.scales(SEED, tag, N, K // group, rows=rows).numpy()
+        return c, s, group, packed_bytes(len(rows), K, bits, group)
+
+    mats = [("gemv", mat("tok.ple", *PLE[1:]))]
+    for li in range(TOKEN_LAYERS):
+        for name, N, K, b, g, fused in TOKEN_LAYER:
+            mats.append(("fused" if fused else "gemv", mat(f"tok.L{li}.{name}", N, K, b, g)))
+    mats.append(("gemv", mat("tok.lm_head", *LM_HEAD[1:])))
+    return dict(e=e, r=r, g1=g1, g2=g2, yo=yo, act=act), mats
 
 
-def oracle_layer(oracle, hin, mats):
-    """The layer's four matvecs on the CPU oracle, for timing: a row sample
-    cannot carry the layer's dependencies, so o_proj and down read static
-    stand-in inputs of their widths."""
-    x, r, g1, g2, attn, act = (hin[k] for k in ("x", "r", "g1", "g2", "attn", "act"))
-    c, s, g, _, _ = mats["qkv"]
-    h, _, _ = oracle.fused_rmsnorm_gemv(c, s, g, x, r, g1)
-    c, s, g, _, _ = mats["o"]
-    oracle.gemv(c, s, g, attn)
-    c, s, g, _, _ = mats["gateup"]
-    oracle.fused_rmsnorm_gemv(c, s, g, attn, h, g2)
-    c, s, g, _, _ = mats["down"]
-    oracle.gemv(c, s, g, act)
+def oracle_token(oracle, hin, mats):
+    """The token's 122 matvecs on the CPU oracle, for timing: a row sample
+    cannot carry the dependencies, so each matvec reads a stand-in input of
+    its width."""
+    ins = {D_MODEL: hin["e"], TOKEN_FF: hin["act"]}
+    for kind, (c, s, g, _) in mats:
+        K = c.shape[1]
+        if kind == "fused":
+            oracle.fused_rmsnorm_gemv(c, s, g, ins[K], hin["r"], hin["g1"])
+        else:
+            oracle.gemv(c, s, g, ins[K])
 
 
-def cpu_baseline(budget_s: float = 12.0, frac_rows: int = 4):
+def cpu_baseline(budget_s: float = 12.0, every: int = 64):
     """The oracle, as it stands, timed on one host core over a bounded sample
-    of the decode layer: passes over the row sample until budget_s seconds of
+    of the decode token: passes over the row sample until budget_s seconds of
     CPU work have run."""
     import oracle
     oracle.build()
-    hin, mats = oracle_sample(frac_rows)
-    sample_bytes = sum(m[4] for m in mats.values())
-    oracle_layer(oracle, hin, mats)          # warm
+    hin, mats = oracle_token_sample(every)
+    sample_bytes = sum(m[1][3] for m in mats)
+    oracle_token(oracle, hin, mats)          # warm
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle_layer(oracle, hin, mats)
+        oracle_token(oracle, hin, mats)
         n += 1
         dt = time.perf_counter() - t0
         if dt >= budget_s:
             break
     return {"value": round(sample_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"every {frac_rows}th row of each matrix of one decode layer "
+            "sample": f"every {every}th row of each of the decode token's 122 matrices "
                       f"({sample_bytes} packed bytes) x {n} passes, fused prologues included, "
                       f"single-threaded C"}
 
@@ -630,24 +745,24 @@ def reference_arm(args, rank, world):
         return None
     import oracle
     oracle.build()
-    frac = 16
-    hin, mats = oracle_sample(frac)
-    sample_bytes = sum(m[4] for m in mats.values())
+    every = 256
+    hin, mats = oracle_token_sample(every)
+    sample_bytes = sum(m[1][3] for m in mats)
     for _ in range(args.warmup):
-        oracle_layer(oracle, hin, mats)
+        oracle_token(oracle, hin, mats)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_layer(oracle, hin, mats)
+        oracle_token(oracle, hin, mats)
     dt = time.perf_counter() - t0
     v = round(sample_bytes * args.steps / dt / 1e9, 4)
-    sample = (f"every {frac}th row of each matrix of one decode layer ({sample_bytes} packed bytes) "
-              f"per step, fused prologues included, single-threaded C")
+    sample = (f"every {every}th row of each of the decode token's 122 matrices ({sample_bytes} packed "
+              f"bytes) per step, fused prologues included, single-threaded C")
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "synthetic decode layer, M=1, d_model 2048, d_ff 8192 (row sample)",
+        "config": {"workload": "full decode token, M=1 (30 layers, d_model 2048, d_ff 16384; row sample)",
                    "formats": FORMATS},
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -659,22 +774,18 @@ def probe(spec: str):
     spec = "N,K,bits,group,M[,fused]"."""
     import torch
 
-    import synth
     from bit_weight_only_packed_gb300 import qmv
     parts = spec.split(",")
     N, K, bits, group, M = (int(v) for v in parts[:5])
     fused = len(parts) > 5 and parts[5] == "fused"
     dev = torch.device("cuda")
-    codes = synth.codes(SEED, "probe", N, K, bits, device=dev)
-    scales = synth.scales(SEED, "probe", N, K // group, device=dev)
-    p = qmv.Pack(N, K, bits, group).pack_weights(codes, scales)
-    del codes, scales
-    x = torch.from_numpy(synth.normal_f16(SEED, "probe.x", (M, K))).to(dev)
-    r = torch.from_numpy(synth.normal_f16(SEED, "probe.r", (M, K))).to(dev)
-    g = torch.from_numpy(synth.normal_f16(SEED, "probe.g", (K,), mean=1.0, std=0.1)).to(dev)
+    p = make_pack(qmv, dev, "probe", N, K, bits, group)
+    x = dev_f16(dev, "probe.x", (M, K))
+    r = dev_f16(dev, "probe.r", (M, K))
+    g = dev_f16(dev, "probe.g", (K,), mean=1.0, std=0.1)
     for _ in range(3):
         if fused:
-            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, 1e-6)
+            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, EPS)
         else:
             qmv.qmv_chunk_gemm(p, x) if M > 1 else qmv.qmv_gemv(p, x)
     torch.cuda.synchronize()
@@ -686,9 +797,10 @@ def main():
     ap.add_argument("--probe", default=None,
                     help="run 3 launches of one shape N,K,bits,group,M[,fused] and exit")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--rounds", type=int, default=9, help="interleaved repeats of each side block")
+    ap.add_argument("--blocks", default="all", help="side blocks: all, none, or a list of c1,c2,c4,c5,chain")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
