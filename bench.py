@@ -221,6 +221,16 @@ def dev_f16(dev, tag, shape, mean=0.0, std=1.0, outliers=False):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
+def workspace_for(qmv, dev, calls, y_dtype=None, mode=None):
+    """One caller workspace big enough for every (pack, M, fused) call in
+    `calls` (fp16 output, fast mode), or None when none needs scratch."""
+    import torch
+    y_dtype = qmv.QMV_F16 if y_dtype is None else y_dtype
+    mode = qmv.QMV_FAST if mode is None else mode
+    n = max(qmv.qmv_workspace_bytes(p, M, y_dtype, mode, fused) for p, M, fused in calls)
+    return torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+
+
 def capture(stream, fn, warm=2):
     """Run fn() `warm` times (first calls set kernel attributes), then capture
     it once as a CUDA graph on `stream`."""
@@ -398,13 +408,15 @@ def block_c4(qmv, dev, copies=4):
     for M in FFN4_MS:
         xs = {K: dev_f16(dev, f"bench.ffn4.{M}.{K}", (M, K)) for _, _, K in FFN4}
         ys = {name: torch.empty(M, N, dtype=torch.float16, device=dev) for name, N, _ in FFN4}
+        # one caller workspace for the calls of this M (they run in turn on one stream)
+        ws = workspace_for(qmv, dev, [(sets[0][name], M, False) for name, _, _ in FFN4])
 
-        def fn(stream, xs=xs, ys=ys):
+        def fn(stream, xs=xs, ys=ys, ws=ws):
             for st in sets:
                 for name, N, K in FFN4:
                     qmv.qmv_chunk_gemm(st[name], xs[K], y=ys[name], y_dtype=qmv.QMV_F16,
-                                       mode=qmv.QMV_FAST, stream=stream)
-        fns[M] = (fn, (xs, ys))
+                                       mode=qmv.QMV_FAST, stream=stream, workspace=ws)
+        fns[M] = (fn, (xs, ys, ws))
     return fns, copies, sets
 
 
@@ -440,17 +452,20 @@ def block_c5(qmv, dev):
         ygu = torch.empty(M, 2 * C5_FF, dtype=torch.float16, device=dev)
         yd = torch.empty(M, C5_D, dtype=torch.float16, device=dev)
         logits = torch.empty(M, 262144, dtype=torch.float16, device=dev)
+        ws = workspace_for(qmv, dev, [(packs["qkv"], M, True), (packs["gateup"], M, True),
+                                      (packs["down"], M, False), (packs["lm_head"], M, False)])
 
-        def fn(stream, M=M, x=x, r=r, act=act, h=h, h2=h2, yq=yq, ygu=ygu, yd=yd, logits=logits):
+        def fn(stream, M=M, x=x, r=r, act=act, h=h, h2=h2, yq=yq, ygu=ygu, yd=yd, logits=logits, ws=ws):
             F16, FAST = qmv.QMV_F16, qmv.QMV_FAST
             qmv.qmv_fused_rmsnorm_gemv(packs["qkv"], x, r, g1, EPS, h_out=h, y=yq, y_dtype=F16, mode=FAST,
-                                       stream=stream)
+                                       stream=stream, workspace=ws)
             qmv.qmv_fused_rmsnorm_gemv(packs["gateup"], h, x, g2, EPS, h_out=h2, y=ygu, y_dtype=F16,
-                                       mode=FAST, stream=stream)
+                                       mode=FAST, stream=stream, workspace=ws)
             qmv.qmv_chunk_gemm(packs["down"], ygu[:, :C5_FF] if M == 1 else act, y=yd, y_dtype=F16,
-                               mode=FAST, stream=stream)
-            qmv.qmv_chunk_gemm(packs["lm_head"], yd, y=logits, y_dtype=F16, mode=FAST, stream=stream)
-        fns[M] = (fn, (x, r, act, h, h2, yq, ygu, yd, logits))
+                               mode=FAST, stream=stream, workspace=ws)
+            qmv.qmv_chunk_gemm(packs["lm_head"], yd, y=logits, y_dtype=F16, mode=FAST, stream=stream,
+                               workspace=ws)
+        fns[M] = (fn, (x, r, act, h, h2, yq, ygu, yd, logits, ws))
     return fns, packs
 
 

@@ -107,6 +107,27 @@ static int check_common(const qmv_pack* p, int M, const void* x, void* y, int y_
   return QMV_OK;
 }
 
+static size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// The scratch of a call, following run_cuda_core's dispatch: the fused
+// prologue of the pipelined M-column tiles (M >= 2, K % 256 == 0), or the
+// tensor tiles' split-K partials (M > 32, fast mode, int2, no prologue).
+static size_t workspace_need(const qmv_pack* p, int M, int y_dtype, int mode, int fused) {
+  if (M < 2 || M > 4096) return 0;
+  if (fused) return (p->K % 256 == 0) ? round256((size_t)M * (size_t)p->K * 2) : 0;
+  if (M > 32 && mode == QMV_FAST && p->bits == 2)
+    return round256(qmv::tc_workspace_bytes(M, p->N, p->K, y_dtype == QMV_F16));
+  return 0;
+}
+
+static int check_workspace(const qmv_pack* p, int M, int y_dtype, int mode, int fused, void* ws,
+                           size_t ws_bytes) {
+  if (ws && !aligned(ws, 256)) return QMV_ERR_ALIGNMENT;
+  const size_t need = workspace_need(p, M, y_dtype, mode, fused);
+  if (need && (!ws || ws_bytes < need)) return QMV_ERR_WORKSPACE;
+  return QMV_OK;
+}
+
 static qmv::GemvArgs base_args(const qmv_pack* p, int M, const void* x, void* y, int y_dtype) {
   qmv::GemvArgs a;
   memset(&a, 0, sizeof(a));
@@ -177,25 +198,43 @@ static int run_cuda_core(qmv::GemvArgs a, int bits, cudaStream_t s, int mode) {
   return QMV_OK;
 }
 
+size_t qmv_workspace_bytes(const qmv_pack* p, int M, int y_dtype, int mode, int fused) {
+  if (!pack_ok(p) || (y_dtype != QMV_F32 && y_dtype != QMV_F16) || (mode != QMV_FAST && mode != QMV_EXACT))
+    return 0;
+  return workspace_need(p, M, y_dtype, mode, fused != 0);
+}
+
 int qmv_gemv(const qmv_pack* p, int M, int N, int K, int bits, int group, const void* x, void* y,
-             int y_dtype, int mode, void* stream) {
+             int y_dtype, int mode, void* d_workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(p, M, x, y, y_dtype, mode);
   if (rc != QMV_OK) return rc;
   if (N != p->N || K != p->K || bits != p->bits || group != p->group) return QMV_ERR_SHAPE;
-  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream, mode);
+  rc = check_workspace(p, M, y_dtype, mode, 0, d_workspace, workspace_bytes);
+  if (rc != QMV_OK) return rc;
+  qmv::GemvArgs a = base_args(p, M, x, y, y_dtype);
+  a.ws = d_workspace;
+  a.ws_bytes = workspace_bytes;
+  return run_cuda_core(a, p->bits, (cudaStream_t)stream, mode);
 }
 
 int qmv_chunk_gemm(const qmv_pack* p, int M, const void* x, void* y, int y_dtype, int mode,
-                   void* stream) {
+                   void* d_workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(p, M, x, y, y_dtype, mode);
   if (rc != QMV_OK) return rc;
-  return run_cuda_core(base_args(p, M, x, y, y_dtype), p->bits, (cudaStream_t)stream, mode);
+  rc = check_workspace(p, M, y_dtype, mode, 0, d_workspace, workspace_bytes);
+  if (rc != QMV_OK) return rc;
+  qmv::GemvArgs a = base_args(p, M, x, y, y_dtype);
+  a.ws = d_workspace;
+  a.ws_bytes = workspace_bytes;
+  return run_cuda_core(a, p->bits, (cudaStream_t)stream, mode);
 }
 
 int qmv_fused_rmsnorm_gemv(const qmv_pack* p, int M, const void* x, const void* residual,
                            const void* gamma, float eps, void* h_out, void* y, int y_dtype,
-                           int mode, void* stream) {
+                           int mode, void* d_workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(p, M, x, y, y_dtype, mode);
+  if (rc != QMV_OK) return rc;
+  rc = check_workspace(p, M, y_dtype, mode, 1, d_workspace, workspace_bytes);
   if (rc != QMV_OK) return rc;
   if (!residual || !gamma) return QMV_ERR_INVALID_ARG;
   if (!(eps >= 0.0f)) return QMV_ERR_INVALID_ARG;
@@ -207,6 +246,8 @@ int qmv_fused_rmsnorm_gemv(const qmv_pack* p, int M, const void* x, const void* 
   a.gamma = (const __half*)gamma;
   a.eps = eps;
   a.h_out = (__half*)h_out;
+  a.ws = d_workspace;
+  a.ws_bytes = workspace_bytes;
   return run_cuda_core(a, p->bits, (cudaStream_t)stream, mode);
 }
 
@@ -292,6 +333,7 @@ const char* qmv_status_string(int status) {
     case QMV_ERR_SHAPE: return "shape does not match the pack or the layout rules";
     case QMV_ERR_CUDA: return "CUDA error (see qmv_last_cuda_error)";
     case QMV_ERR_TIMEOUT: return "device-side wait timed out";
+    case QMV_ERR_WORKSPACE: return "workspace missing or smaller than qmv_workspace_bytes()";
     default: return "unknown status";
   }
 }

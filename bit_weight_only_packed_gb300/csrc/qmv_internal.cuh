@@ -49,6 +49,11 @@ struct GemvArgs {
   // j*gather_rows ..) is expert gather_ids[j], j < gather_n
   const int* gather_ids;
   int gather_rows, gather_n, gather_E;
+  // the caller's device scratch (256-byte aligned, ws_bytes long, nullable):
+  // the tensor tiles' split-K partial tiles, or the fused prologue's
+  // normalised activations for M >= 2 (workspace_bytes says how much)
+  void* ws;
+  size_t ws_bytes;
 };
 
 struct DevInfo {
@@ -72,6 +77,9 @@ bool tma_fits(int K, int bits, bool perrow);
 // tcgen05 tensor-core tiles for 1..128 token columns, int2 weights (fast
 // mode); QMV_ERR_UNSUPPORTED for other widths or the fused prologue.
 int launch_tc_gemm(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
+// Scratch bytes launch_tc_gemm needs for up to 128 columns of M (split-K
+// partial tiles; 0 when it needs none).
+size_t tc_workspace_bytes(int M, int N, int K, bool y_f16);
 // Programmatic dependent launch of the M = 1 kernels (off by default).
 bool pdl_enabled();
 void set_pdl(bool on);

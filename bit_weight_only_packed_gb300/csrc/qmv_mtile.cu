@@ -657,11 +657,11 @@ int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) 
   if (a.M < 2 || a.K % 256 != 0 || a.gather_rows || a.amax_ws) return QMV_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(a.x) & 15u) != 0) return QMV_ERR_UNSUPPORTED;
   if (!a.fused) return launch_mtile_plain(a, bits, s, err);
-  // fused prologue: the normalised activations into a stream-ordered scratch
-  // (the device's default memory pool), then the plain tiles on them
-  __half* yn = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&yn), (size_t)a.M * a.K * sizeof(__half), s);
-  if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  // fused prologue: the normalised activations into the caller's workspace
+  // (checked by the ABI), then the plain tiles on them
+  if (!a.ws || a.ws_bytes < (size_t)a.M * a.K * sizeof(__half)) return QMV_ERR_WORKSPACE;
+  __half* yn = reinterpret_cast<__half*>(a.ws);
+  cudaError_t e = cudaSuccess;
   const size_t psm = (size_t)(a.K / 32) * sizeof(float);
   if (psm > 48 * 1024) {
     e = cudaFuncSetAttribute(rms_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
@@ -695,12 +695,9 @@ int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) 
     b.r = nullptr;
     b.gamma = nullptr;
     b.h_out = nullptr;
+    b.ws = nullptr;
+    b.ws_bytes = 0;
     rc = launch_mtile_plain(b, bits, s, err);
-  }
-  const cudaError_t ef = cudaFreeAsync(yn, s);
-  if (rc == QMV_OK && ef != cudaSuccess) {
-    *err = ef;
-    rc = QMV_ERR_CUDA;
   }
   return rc;
 }

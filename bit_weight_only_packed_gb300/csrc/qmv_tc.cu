@@ -143,6 +143,41 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 
 }  // namespace
 
+// Raw-ring depth (slabs a raw stage) of the two tile shapes.
+constexpr int TC_RS_M64 = 2, TC_RS_M128 = 2;
+
+// How K is split across CTAs: split K to balance the waves; the time is
+// about ceil(tiles * split / SMs) CTA-slots of 1/split of the work each; the
+// smallest such time wins (at least 8 slabs per split), the smaller split on
+// a tie.  A split that needs the scratch and the reduction kernel (fp16
+// output, or more than two splits) must save a third of the time: the
+// partial tiles' round trip costs about 15 us on a 28672 x 4096 M = 128 tile
+// set (two splits, fp16: 94 us against 79 us for fp32 atomics).  Each split
+// takes whole raw stages, so every box starts on a 16-byte boundary.  Two
+// splits with fp32 output add into the zeroed output with atomics.
+struct TcSplit {
+  int split, slabs_per_split;
+  bool atomics;
+};
+static TcSplit tc_split(int tiles, int K, bool y16, int RS) {
+  const int nslab = K / 64;
+  const int sms = dev_info().sms;
+  int split = 1;
+  double best = 1e30;
+  for (int sp = 1; sp <= 8 && nslab / sp >= 8; ++sp) {
+    double t = (double)((tiles * sp + sms - 1) / sms) / sp;
+    const bool scratch = sp > 1 && (sp > 2 || y16);
+    if (scratch) t *= 1.5;
+    if (t < best - 1e-9) {
+      best = t;
+      split = sp;
+    }
+  }
+  int sps = (((nslab + split - 1) / split) + RS - 1) / RS * RS;
+  while (split > 1 && (split - 1) * sps >= nslab) --split;
+  return TcSplit{split, sps, split == 2 && !y16};
+}
+
 struct TcArgs {
   const __half* scales;    // [N][G] (one scale per row when perrow)
   float* y;                // [M][N] fp32 output (or null)
@@ -486,59 +521,38 @@ static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s
              64, MT, CU_TENSOR_MAP_SWIZZLE_128B))
     return QMV_ERR_UNSUPPORTED;
   TcArgs a = a0;
-  const int nslab = a.K / 64;
-  const int sms = dev_info().sms;
-  // split K across CTAs to balance the waves: the time is about
-  // ceil(tiles * split / SMs) CTA-slots of 1/split of the work each; the
-  // smallest such time wins (at least 8 slabs per split), the smaller split
-  // on a tie.  A split that needs the scratch and the reduction kernel (fp16
-  // output, or more than two splits) must save a third of the time: the
-  // partial tiles' round trip costs about 15 us on a 28672 x 4096 M = 128
-  // tile set (two splits, fp16: 94 us against 79 us for fp32 atomics)
-  int split = 1;
-  {
-    double best = 1e30;
-    for (int sp = 1; sp <= 8 && nslab / sp >= 8; ++sp) {
-      double t = (double)((tiles * sp + sms - 1) / sms) / sp;
-      const bool scratch = sp > 1 && (sp > 2 || a.y16 != nullptr);
-      if (scratch) t *= 1.5;
-      if (t < best - 1e-9) {
-        best = t;
-        split = sp;
-      }
-    }
-  }
-  a.split = split;
-  // whole raw stages per split, so every box starts on a 16-byte boundary
-  a.slabs_per_split = (((nslab + split - 1) / split) + RS - 1) / RS * RS;
-  while (split > 1 && (split - 1) * a.slabs_per_split >= nslab) {
-    --split;
-    a.split = split;
-  }
+  const TcSplit sp = tc_split(tiles, a.K, a.y16 != nullptr, RS);
+  a.split = sp.split;
+  a.slabs_per_split = sp.slabs_per_split;
   a.part = nullptr;
   const int64_t total = (int64_t)a.M * a.N;
-  const bool atomics = split == 2 && a.y16 == nullptr;
-  if (atomics) {
+  if (sp.atomics) {
     e = cudaMemsetAsync(a.y, 0, (size_t)total * sizeof(float), s);
     if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
-  } else if (split > 1) {
-    // stream-ordered scratch for the partial tiles (from the device's
-    // default memory pool; freed on the stream after the reduction)
-    e = cudaMallocAsync(reinterpret_cast<void**>(&a.part), (size_t)split * total * sizeof(float), s);
-    if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
+  } else if (sp.split > 1) {
+    // the partial tiles go to the caller's workspace (checked by the ABI)
+    if (!g.ws || g.ws_bytes < (size_t)sp.split * total * sizeof(float)) return QMV_ERR_WORKSPACE;
+    a.part = reinterpret_cast<float*>(g.ws);
   }
-  kern<<<dim3(tiles, split), TC_THREADS, smem, s>>>(a, tmc, tms, tmx);
+  kern<<<dim3(tiles, sp.split), TC_THREADS, smem, s>>>(a, tmc, tms, tmx);
   e = cudaGetLastError();
-  if (a.part) {
-    if (e == cudaSuccess) {
-      tc_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a.part, split, total, a.y, a.y16);
-      e = cudaGetLastError();
-    }
-    const cudaError_t ef = cudaFreeAsync(a.part, s);
-    if (e == cudaSuccess) e = ef;
+  if (a.part && e == cudaSuccess) {
+    tc_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(a.part, sp.split, total, a.y, a.y16);
+    e = cudaGetLastError();
   }
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   return QMV_OK;
+}
+
+// Scratch of a launch of up to 128 columns: split-K partial tiles in fp32
+// when the chosen split needs the reduction kernel.
+size_t tc_workspace_bytes(int M, int N, int K, bool y_f16) {
+  if (M < 1 || K % 256 != 0) return 0;
+  const int m = M < 128 ? M : 128;
+  const int tiles = (N + 127) / 128;
+  const TcSplit sp = tc_split(tiles, K, y_f16, m <= 64 ? TC_RS_M64 : TC_RS_M128);
+  if (sp.split <= 1 || sp.atomics) return 0;
+  return (size_t)sp.split * (size_t)m * (size_t)N * sizeof(float);
 }
 
 // M in 1 .. 128 token columns, int2 weights; y fp32 or fp16.
@@ -563,8 +577,8 @@ int launch_tc_gemm(const GemvArgs& g, int bits, cudaStream_t s, cudaError_t* err
   // removed), so a stage carries four slabs for M <= 64 (two stages of
   // 96 KB) and two for M = 128 (three stages of 64 KB); a two-slab raw ring
   // keeps a code and scale copy in flight
-  if (g.M <= 64) return run_tc<64, 2, 2, 4>(a, g, tiles, s, err);
-  return run_tc<128, 3, 2, 2>(a, g, tiles, s, err);
+  if (g.M <= 64) return run_tc<64, 2, TC_RS_M64, 4>(a, g, tiles, s, err);
+  return run_tc<128, 3, TC_RS_M128, 2>(a, g, tiles, s, err);
 }
 
 }  // namespace qmv

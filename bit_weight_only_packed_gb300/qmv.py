@@ -22,6 +22,7 @@ QMV_ERR_ALIGNMENT = -3
 QMV_ERR_SHAPE = -4
 QMV_ERR_CUDA = -5
 QMV_ERR_TIMEOUT = -6
+QMV_ERR_WORKSPACE = -7
 QMV_F32, QMV_F16 = 0, 1
 QMV_FAST, QMV_EXACT = 0, 1
 
@@ -30,9 +31,10 @@ _P, _I, _F, _SZP = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.POINTER
 SIGNATURES = {
     "qmv_create_pack": (_I, [ctypes.POINTER(_P), _I, _I, _I, _I, _SZP, _SZP]),
     "qmv_pack_weights": (_I, [_P, _P, _P, _P, _P, _P]),
-    "qmv_gemv": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P]),
-    "qmv_fused_rmsnorm_gemv": (_I, [_P, _I, _P, _P, _P, _F, _P, _P, _I, _I, _P]),
-    "qmv_chunk_gemm": (_I, [_P, _I, _P, _P, _I, _I, _P]),
+    "qmv_workspace_bytes": (ctypes.c_size_t, [_P, _I, _I, _I, _I]),
+    "qmv_gemv": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _I, _I, _P, ctypes.c_size_t, _P]),
+    "qmv_fused_rmsnorm_gemv": (_I, [_P, _I, _P, _P, _P, _F, _P, _P, _I, _I, _P, ctypes.c_size_t, _P]),
+    "qmv_chunk_gemm": (_I, [_P, _I, _P, _P, _I, _I, _P, ctypes.c_size_t, _P]),
     "qmv_unpack_codes": (_I, [_P, _P, _P]),
     "qmv_pack_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
                            ctypes.POINTER(_I)]),
@@ -186,28 +188,53 @@ def _out(y, M, N, y_dtype, like):
     return y
 
 
-def qmv_gemv(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None, M=None):
+def qmv_workspace_bytes(p: Pack, M: int, y_dtype=QMV_F32, mode=QMV_FAST, fused=False) -> int:
+    """Device scratch bytes a call needs (0 for none)."""
+    return int(_lib.qmv_workspace_bytes(p.handle, M, y_dtype, mode, 1 if fused else 0))
+
+
+def workspace(p: Pack, M: int, y_dtype=QMV_F32, mode=QMV_FAST, fused=False, device=None):
+    """A workspace tensor for such calls (None when they need none)."""
+    n = qmv_workspace_bytes(p, M, y_dtype, mode, fused)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda") if n else None
+
+
+def _ws(p, M, y_dtype, mode, fused, ws, like):
+    """The caller's workspace, checked, or (when none is given) a fresh torch
+    allocation of the size the call needs: (pointer, bytes, tensor)."""
+    n = qmv_workspace_bytes(p, M, y_dtype, mode, fused)
+    if ws is None:
+        if n == 0:
+            return None, 0, None
+        ws = torch.empty(n, dtype=torch.uint8, device=like.device)
+    _need_bytes("workspace", ws, n)
+    return _dptr(ws), ws.numel() * ws.element_size(), ws
+
+
+def qmv_gemv(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None, M=None, workspace=None):
     M = x.shape[0] if (M is None and x.dim() == 2) else (M or 1)
     _need("x", x, torch.float16, M * p.K)
     _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
+    wp, wb, _keep = _ws(p, M, y_dtype, mode, False, workspace, x)
     _check("qmv_gemv", _lib.qmv_gemv(p.handle, M, p.N, p.K, p.bits, p.group, _dptr(x), _dptr(y),
-                                     y_dtype, mode, _stream(stream)))
+                                     y_dtype, mode, wp, wb, _stream(stream)))
     return y
 
 
-def qmv_chunk_gemm(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None):
+def qmv_chunk_gemm(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None, workspace=None):
     M = x.shape[0]
     _need("x", x, torch.float16, M * p.K)
     _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
+    wp, wb, _keep = _ws(p, M, y_dtype, mode, False, workspace, x)
     _check("qmv_chunk_gemm", _lib.qmv_chunk_gemm(p.handle, M, _dptr(x), _dptr(y), y_dtype, mode,
-                                                 _stream(stream)))
+                                                 wp, wb, _stream(stream)))
     return y
 
 
 def qmv_fused_rmsnorm_gemv(p: Pack, x, residual, gamma, eps=1e-6, h_out=None, y=None,
-                           y_dtype=QMV_F32, mode=QMV_FAST, stream=None):
+                           y_dtype=QMV_F32, mode=QMV_FAST, stream=None, workspace=None):
     M = x.shape[0] if x.dim() == 2 else 1
     _need("x", x, torch.float16, M * p.K)
     _need("residual", residual, torch.float16, M * p.K)
@@ -215,9 +242,10 @@ def qmv_fused_rmsnorm_gemv(p: Pack, x, residual, gamma, eps=1e-6, h_out=None, y=
     _need("h_out", h_out, torch.float16, M * p.K)
     _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
+    wp, wb, _keep = _ws(p, M, y_dtype, mode, True, workspace, x)
     _check("qmv_fused_rmsnorm_gemv", _lib.qmv_fused_rmsnorm_gemv(
         p.handle, M, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out), _dptr(y),
-        y_dtype, mode, _stream(stream)))
+        y_dtype, mode, wp, wb, _stream(stream)))
     return y
 
 

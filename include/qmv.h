@@ -17,14 +17,10 @@
  *
  * Conventions (all entry points):
  *   - Every pointer named d_* or described as "device" is a CUDA device
- *     pointer owned by the caller.  The library allocates no device memory of
- *     its own, with two stream-ordered exceptions: the tensor-core tiles' split-K
- *     partial tiles (M > 32 in QMV_FAST with int2 weights, when the K split
- *     needs more than two splits or fp16 output) and the fused prologue's
- *     normalised activations for M >= 2 (M x K fp16).  Both come from the
- *     device's default memory pool with cudaMallocAsync on the call's stream
- *     and go back with cudaFreeAsync on the same stream after use; an
- *     allocation failure returns QMV_ERR_CUDA.
+ *     pointer owned by the caller.  The library allocates no device memory:
+ *     the scratch some calls need (the tensor-core tiles' split-K partial
+ *     tiles, the fused prologue's normalised activations for M >= 2) is a
+ *     caller-provided workspace whose size qmv_workspace_bytes() gives.
  *   - fp16 values are IEEE binary16 bit patterns (uint16_t / __half).
  *   - Matrices are row-major with no padding.  Activations are M x K (row m is
  *     column m of the matvec, i.e. token m); outputs are M x N.
@@ -88,7 +84,8 @@ typedef enum {
     QMV_ERR_ALIGNMENT = -3,     /* a pointer is not aligned as documented */
     QMV_ERR_SHAPE = -4,         /* N/K/bits/group disagree with the pack or layout rules */
     QMV_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
-    QMV_ERR_TIMEOUT = -6        /* a bounded device-side wait ran out */
+    QMV_ERR_TIMEOUT = -6,       /* a bounded device-side wait ran out */
+    QMV_ERR_WORKSPACE = -7      /* the call needs a larger workspace (qmv_workspace_bytes) */
 } qmv_status;
 
 typedef enum { QMV_F32 = 0, QMV_F16 = 1 } qmv_dtype;      /* output element type */
@@ -126,6 +123,19 @@ QMV_API int qmv_pack_weights(qmv_pack *p, const int8_t *d_codes_in, const uint16
                      void *d_codes, void *d_scales, void *stream);
 
 /*
+ * qmv_workspace_bytes -- device scratch bytes that a call of qmv_gemv /
+ * qmv_chunk_gemm (fused = 0) or qmv_fused_rmsnorm_gemv (fused = 1) with this
+ * pack, M, y_dtype and mode needs in its d_workspace: fp32 split-K partial
+ * tiles of the tensor-core tiles (M > 32, QMV_FAST, int2) when the chosen
+ * split needs more than the output itself, or the fused prologue's
+ * normalised activations (M x K fp16) for M >= 2; 0 when the call needs none
+ * (always for M = 1).  The size depends only on these arguments and the
+ * device's SM count, so one workspace serves every later call with them.
+ * Host only; 0 for invalid arguments.
+ */
+QMV_API size_t qmv_workspace_bytes(const qmv_pack *p, int M, int y_dtype, int mode, int fused);
+
+/*
  * qmv_gemv -- y = x . W^T for M columns: y[m][n] = sum_g (sum_{k in g}
  * x[m][k] * v[n][k]) * s[n][g] in the order stated at the top of this file.
  * [A19] int2 item (exact products, fp32 in code order); [PLAY] K-order-fixed
@@ -142,10 +152,15 @@ QMV_API int qmv_pack_weights(qmv_pack *p, const int8_t *d_codes_in, const uint16
  *   y            device [M][N] of y_dtype (fp32, or fp16 = RNE of the fp32
  *                result), 4-byte aligned.
  *   mode         QMV_FAST or QMV_EXACT.
- * Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, CUDA.
+ *   d_workspace, workspace_bytes  caller scratch, 256-byte aligned, at least
+ *                qmv_workspace_bytes(p, M, y_dtype, mode, 0) bytes (may be
+ *                NULL, 0 when that is 0).  Its contents on entry do not
+ *                matter; calls that share a workspace must not overlap.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED, WORKSPACE, CUDA.
  */
 QMV_API int qmv_gemv(const qmv_pack *p, int M, int N, int K, int bits, int group,
-             const void *x, void *y, int y_dtype, int mode, void *stream);
+             const void *x, void *y, int y_dtype, int mode, void *d_workspace,
+             size_t workspace_bytes, void *stream);
 
 /*
  * qmv_fused_rmsnorm_gemv -- residual add + RMSNorm folded into the matvec
@@ -158,11 +173,14 @@ QMV_API int qmv_gemv(const qmv_pack *p, int M, int N, int K, int bits, int group
  *   M            1 .. 4096; every column runs the CUDA-core kernels (the
  *                fused prologue never takes the tensor-core tiles), each
  *                column equal to the M = 1 result.
+ *   d_workspace, workspace_bytes  as qmv_gemv, sized by
+ *                qmv_workspace_bytes(p, M, y_dtype, mode, 1).
  * Errors: as qmv_gemv.
  */
 QMV_API int qmv_fused_rmsnorm_gemv(const qmv_pack *p, int M, const void *x, const void *residual,
                            const void *gamma, float eps, void *h_out, void *y,
-                           int y_dtype, int mode, void *stream);
+                           int y_dtype, int mode, void *d_workspace, size_t workspace_bytes,
+                           void *stream);
 
 /*
  * qmv_chunk_gemm -- a prefill chunk of M tokens against one pack ([PLAY]
@@ -170,10 +188,10 @@ QMV_API int qmv_fused_rmsnorm_gemv(const qmv_pack *p, int M, const void *x, cons
  * own N, K, bits and group.  M = 4, 8, 16 (and any M <= 32, or any M in
  * QMV_EXACT, or int4/int8) use the K-order-fixed CUDA-core tiles; M = 64,
  * 128 (any M > 32) in QMV_FAST with int2 weights use tcgen05 tensor-core
- * tiles.
+ * tiles.  d_workspace, workspace_bytes as qmv_gemv.
  */
 QMV_API int qmv_chunk_gemm(const qmv_pack *p, int M, const void *x, void *y, int y_dtype,
-                   int mode, void *stream);
+                   int mode, void *d_workspace, size_t workspace_bytes, void *stream);
 
 /*
  * qmv_gemv_argmax -- the lm_head matvec with the greedy-token step fused into

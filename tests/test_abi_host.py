@@ -68,23 +68,45 @@ def test_calls_on_unbound_pack_fail_on_host(q):
     p = q.Pack(64, 128, 2, 32)
     lib = q.lib()
     # not packed yet -> invalid argument, before any CUDA call
-    assert lib.qmv_gemv(p.handle, 1, 64, 128, 2, 32, 16, 32, 0, 0, None) == -1
-    assert lib.qmv_chunk_gemm(p.handle, 4, 16, 32, 0, 0, None) == -1
-    assert lib.qmv_fused_rmsnorm_gemv(p.handle, 1, 16, 16, 16, 1e-6, None, 32, 0, 0, None) == -1
+    assert lib.qmv_gemv(p.handle, 1, 64, 128, 2, 32, 16, 32, 0, 0, None, 0, None) == -1
+    assert lib.qmv_chunk_gemm(p.handle, 4, 16, 32, 0, 0, None, 0, None) == -1
+    assert lib.qmv_fused_rmsnorm_gemv(p.handle, 1, 16, 16, 16, 1e-6, None, 32, 0, 0, None, 0, None) == -1
     assert lib.qmv_unpack_codes(p.handle, 16, None) == -1
     # null and misaligned pointers are rejected on the host
     assert lib.qmv_pack_weights(p.handle, None, 16, 16, 16, None) == -1
     assert lib.qmv_pack_weights(p.handle, 8, 16, 16, 16, None) == -3
     assert lib.qmv_pack_weights(p.handle, 16, 16, 16, 24, None) == -3
-    assert lib.qmv_gemv(None, 1, 64, 128, 2, 32, 16, 32, 0, 0, None) == -1
+    assert lib.qmv_gemv(None, 1, 64, 128, 2, 32, 16, 32, 0, 0, None, 0, None) == -1
     assert lib.qmv_destroy_pack(None) == -1
 
 
 def test_status_strings(q):
-    for s in range(-6, 1):
+    for s in range(-7, 1):
         assert q.qmv_status_string(s) and q.qmv_status_string(s) != "unknown status"
     assert q.qmv_status_string(-99) == "unknown status"
     assert q.qmv_last_cuda_error() == 0
+
+
+def test_workspace_sizes_follow_the_dispatch(q):
+    # qmv_workspace_bytes, host only: nothing for M = 1 or for calls that need
+    # no scratch; M x K fp16 (256-byte multiple) for the fused prologue at
+    # M >= 2; split-K partial tiles only for the int2 tensor tiles (M > 32,
+    # fast mode), never more than a split of 8 over 128 columns
+    p2 = q.Pack(28672, 4096, 2, 32)
+    p4 = q.Pack(4096, 4096, 4, 32)
+    assert q.qmv_workspace_bytes(p2, 1, q.QMV_F32, q.QMV_FAST, fused=True) == 0
+    assert q.qmv_workspace_bytes(p2, 16, q.QMV_F32, q.QMV_FAST, fused=True) == 16 * 4096 * 2
+    assert q.qmv_workspace_bytes(p2, 3, q.QMV_F16, q.QMV_EXACT, fused=True) == (3 * 4096 * 2 + 255) // 256 * 256
+    assert q.qmv_workspace_bytes(p2, 16, q.QMV_F32, q.QMV_FAST) == 0
+    assert q.qmv_workspace_bytes(p2, 128, q.QMV_F32, q.QMV_EXACT) == 0
+    assert q.qmv_workspace_bytes(p4, 128, q.QMV_F16, q.QMV_FAST) == 0
+    for M in (33, 64, 128, 200):
+        for dt in (q.QMV_F32, q.QMV_F16):
+            n = q.qmv_workspace_bytes(p2, M, dt, q.QMV_FAST)
+            assert n % 256 == 0 and n <= 8 * 128 * 28672 * 4, (M, dt, n)
+    # the down projection's shape splits K with fp16 output: it needs scratch
+    pd = q.Pack(4096, 14336, 2, 32)
+    assert q.qmv_workspace_bytes(pd, 128, q.QMV_F16, q.QMV_FAST) > 0
 
 
 def test_binding_checks_tensors_before_any_call(q):
@@ -146,7 +168,10 @@ int main(void) {
     if (cb != 48 * 256 / 2 || sb != 48 * 8 * 2) return 2;
     if (qmv_pack_info(p, &N, &K, &bits, &group) != QMV_OK) return 3;
     if (N != 48 || K != 256 || bits != 4 || group != 32) return 4;
-    if (qmv_gemv(p, 1, 48, 256, 4, 32, NULL, NULL, QMV_F32, QMV_FAST, NULL) != QMV_ERR_INVALID_ARG) return 5;
+    if (qmv_gemv(p, 1, 48, 256, 4, 32, NULL, NULL, QMV_F32, QMV_FAST, NULL, 0, NULL) != QMV_ERR_INVALID_ARG) return 5;
+    if (qmv_workspace_bytes(p, 1, QMV_F32, QMV_FAST, 1) != 0) return 7;
+    if (qmv_workspace_bytes(p, 16, QMV_F32, QMV_EXACT, 1) != 16 * 256 * 2) return 8;
+    if (qmv_workspace_bytes(p, 64, QMV_F16, QMV_FAST, 0) != 0) return 9;
     if (qmv_destroy_pack(p) != QMV_OK) return 6;
     printf("%s\n", qmv_status_string(QMV_ERR_SHAPE));
     return 0;

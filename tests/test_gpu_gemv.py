@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import Mat, acts, bits_equal, first_diff, max_rel_err, to_dev, within_tol, qmv
+from gpu_util import Mat, acts, bits_equal, first_diff, max_rel_err, to_dev, within_tol, qmv, qmv_guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -30,7 +30,7 @@ SHAPES = [
 
 @pytest.mark.parametrize("N,K,bits,group", SHAPES)
 def test_gemv_m1_bit_exact(N, K, bits, group):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"g{N}x{K}b{bits}g{group}", N, K, bits, group)
     x, _, _ = acts(f"g{N}x{K}", 1, K)
     y = q.qmv_gemv(m.pack, to_dev(x), mode=q.QMV_EXACT)
@@ -45,7 +45,7 @@ def test_gemv_m1_bit_exact(N, K, bits, group):
 
 @pytest.mark.parametrize("N,K,bits,group", SHAPES)
 def test_gemv_m1_fast_within_tolerance(N, K, bits, group):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"g{N}x{K}b{bits}g{group}", N, K, bits, group)
     x, _, _ = acts(f"g{N}x{K}", 1, K)
     y = q.qmv_gemv(m.pack, to_dev(x), mode=q.QMV_FAST)
@@ -64,7 +64,7 @@ def test_gemv_m1_fast_within_tolerance(N, K, bits, group):
                                             (65, 256, 8, 32), (33, 2048, 2, 2048)])
 @pytest.mark.parametrize("M", [2, 5, 8, 16, 17, 32])
 def test_fast_tile_columns_equal_fast_m1(N, K, bits, group, M):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"f{N}x{K}b{bits}g{group}", N, K, bits, group)
     x, _, _ = acts(f"f{N}x{K}m{M}", M, K)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_FAST)
@@ -83,7 +83,7 @@ def test_fast_tile_columns_equal_fast_m1(N, K, bits, group, M):
                                             (37, 5376, 8, 5376), (33, 128, 2, 32)])
 @pytest.mark.parametrize("M", [2, 3, 4, 5, 8, 16, 17, 32, 33, 40])
 def test_chunk_columns_bit_exact(N, K, bits, group, M):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"c{N}x{K}b{bits}g{group}", N, K, bits, group)
     x, _, _ = acts(f"c{N}x{K}m{M}", M, K)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_EXACT)
@@ -100,7 +100,7 @@ def test_chunk_columns_bit_exact(N, K, bits, group, M):
 
 
 def test_output_fp16_rne_small_tile():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("f16tile", 300, 2048, 2, 32)
     x, _, _ = acts("f16tile", 8, 2048)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), y_dtype=q.QMV_F16, mode=q.QMV_EXACT)
@@ -111,7 +111,7 @@ def test_output_fp16_rne_small_tile():
 
 
 def test_zero_codes_give_zero():
-    q = qmv()
+    q = qmv_guarded()
     N, K = 64, 256
     p = q.Pack(N, K, 2, 32).pack_weights(torch.zeros(N, K, dtype=torch.int8, device="cuda"),
                                          torch.full((N, K // 32), 0.01, dtype=torch.float16,
@@ -125,7 +125,7 @@ def test_zero_codes_give_zero():
 
 
 def test_repeated_calls_identical():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("repeat", 4096, 2048, 2, 32)
     x, _, _ = acts("repeat", 1, 2048)
     xd = to_dev(x)
@@ -136,21 +136,21 @@ def test_repeated_calls_identical():
 
 
 def test_shape_mismatch_rejected():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("mismatch", 64, 128, 2, 32)
     x = torch.zeros(1, 128, dtype=torch.float16, device="cuda")
     y = torch.zeros(1, 64, dtype=torch.float32, device="cuda")
     lib = q.lib()
     s = torch.cuda.current_stream().cuda_stream
-    assert lib.qmv_gemv(m.pack.handle, 1, 65, 128, 2, 32, x.data_ptr(), y.data_ptr(), 0, 0, s) == -4
-    assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 4, 32, x.data_ptr(), y.data_ptr(), 0, 0, s) == -4
-    assert lib.qmv_gemv(m.pack.handle, 0, 64, 128, 2, 32, x.data_ptr(), y.data_ptr(), 0, 0, s) == -1
-    assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 2, 32, x.data_ptr() + 2, y.data_ptr(), 0, 0, s) == -3
-    assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 2, 32, x.data_ptr(), y.data_ptr(), 7, 0, s) == -1
+    assert lib.qmv_gemv(m.pack.handle, 1, 65, 128, 2, 32, x.data_ptr(), y.data_ptr(), 0, 0, None, 0, s) == -4
+    assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 4, 32, x.data_ptr(), y.data_ptr(), 0, 0, None, 0, s) == -4
+    assert lib.qmv_gemv(m.pack.handle, 0, 64, 128, 2, 32, x.data_ptr(), y.data_ptr(), 0, 0, None, 0, s) == -1
+    assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 2, 32, x.data_ptr() + 2, y.data_ptr(), 0, 0, None, 0, s) == -3
+    assert lib.qmv_gemv(m.pack.handle, 1, 64, 128, 2, 32, x.data_ptr(), y.data_ptr(), 7, 0, None, 0, s) == -1
 
 
 def test_device_error_word_clear_after_runs():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("errword", 8192, 2048, 2, 32)
     x, _, _ = acts("errword", 1, 2048)
     for _ in range(3):
