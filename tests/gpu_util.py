@@ -101,3 +101,142 @@ def max_rel_err(y, ref):
     y = np.asarray(y, np.float64)
     ref = np.asarray(ref, np.float64)
     return float(np.max(np.abs(y - ref) / (1.0 + np.abs(ref))))
+
+
+# ------------------------------------------------------------ guard bands --
+# compute-sanitizer is not available, so out-of-bounds stores are caught by
+# guard bands: every output (and workspace) of a guarded call sits between
+# two 4 KiB bands of 0xA5 that must be intact after the call.
+
+GUARD = 4096
+CANARY = 0xA5
+
+
+class GuardBuf:
+    """nbytes of device memory between two GUARD-byte bands of CANARY (the
+    payload itself filled with `fill`); the payload is 256-byte aligned."""
+
+    def __init__(self, nbytes, fill=CANARY):
+        self.nbytes = int(nbytes)
+        self.raw = torch.full((2 * GUARD + self.nbytes,), CANARY, dtype=torch.uint8, device="cuda")
+        if fill != CANARY:
+            self.raw[GUARD:GUARD + self.nbytes].fill_(fill)
+
+    def view(self, dtype, shape):
+        return self.raw[GUARD:GUARD + self.nbytes].view(dtype).view(shape)
+
+    def check(self, what):
+        lo = torch.nonzero(self.raw[:GUARD] != CANARY)
+        hi = torch.nonzero(self.raw[GUARD + self.nbytes:] != CANARY)
+        assert lo.numel() == 0, f"{what}: {lo.numel()} bytes written before the buffer (first at -{GUARD - int(lo[0])})"
+        assert hi.numel() == 0, f"{what}: {hi.numel()} bytes written past the buffer (first at +{int(hi[0])})"
+
+
+def _esize(dtype):
+    return torch.tensor([], dtype=dtype).element_size()
+
+
+def guarded_like(t):
+    """A guarded buffer shaped and typed like tensor t (payload 0xA5)."""
+    g = GuardBuf(t.numel() * _esize(t.dtype))
+    return g, g.view(t.dtype, t.shape)
+
+
+class _GuardedQmv:
+    """The binding with guard bands around every output, h_out and workspace
+    of the matvec calls (the workspace payload is filled with 0x5A: its
+    contents on entry must not matter); each call synchronises, checks the
+    bands, and returns (or fills) the caller's outputs as the binding does."""
+
+    def __init__(self, q):
+        self._q = q
+
+    def __getattr__(self, name):
+        return getattr(self._q, name)
+
+    def _ydt(self, y_dtype):
+        return torch.float16 if y_dtype == self._q.QMV_F16 else torch.float32
+
+    def _ws(self, p, M, y_dtype, mode, fused):
+        n = self._q.qmv_workspace_bytes(p, M, y_dtype, mode, fused)
+        if n == 0:
+            return None, None
+        g = GuardBuf(n, fill=0x5A)
+        return g, g.view(torch.uint8, (n,))
+
+    def _finish(self, bufs, outs):
+        torch.cuda.synchronize()
+        for name, g in bufs:
+            if g is not None:
+                g.check(name)
+        for dst, src in outs:
+            if dst is not None:
+                dst.copy_(src)
+
+    def _call(self, fn, p, M, N, y, y_dtype, mode, fused, h_out, **kw):
+        gy = GuardBuf(M * N * _esize(self._ydt(y_dtype)))
+        yv = gy.view(self._ydt(y_dtype), (M, N))
+        gh, hv = (None, None) if h_out is None else guarded_like(h_out)
+        gw, wv = self._ws(p, M, y_dtype, mode, fused)
+        if fused:
+            kw["h_out"] = hv
+        fn(y=yv, y_dtype=y_dtype, mode=mode, workspace=wv, **kw)
+        self._finish([("y", gy), ("h_out", gh), ("workspace", gw)], [(h_out, hv)])
+        if y is not None:
+            y.copy_(yv.view_as(y))
+            return y
+        return yv.clone()
+
+    def qmv_gemv(self, p, x, y=None, y_dtype=0, mode=0, stream=None, M=None, workspace=None):
+        M = x.shape[0] if (M is None and x.dim() == 2) else (M or 1)
+        return self._call(lambda **kw: self._q.qmv_gemv(p, x, stream=stream, M=M, **kw),
+                          p, M, p.N, y, y_dtype, mode, False, None)
+
+    def qmv_chunk_gemm(self, p, x, y=None, y_dtype=0, mode=0, stream=None, workspace=None):
+        return self._call(lambda **kw: self._q.qmv_chunk_gemm(p, x, stream=stream, **kw),
+                          p, x.shape[0], p.N, y, y_dtype, mode, False, None)
+
+    def qmv_fused_rmsnorm_gemv(self, p, x, residual, gamma, eps=1e-6, h_out=None, y=None, y_dtype=0,
+                               mode=0, stream=None, workspace=None):
+        M = x.shape[0] if x.dim() == 2 else 1
+        return self._call(lambda **kw: self._q.qmv_fused_rmsnorm_gemv(p, x, residual, gamma, eps,
+                                                                      stream=stream, **kw),
+                          p, M, p.N, y, y_dtype, mode, True, h_out)
+
+    def qmv_gemv_gather(self, p, rows_per_expert, expert_ids, x, y=None, y_dtype=0, mode=0, stream=None):
+        n = expert_ids.numel() * rows_per_expert
+        gy = GuardBuf(n * _esize(self._ydt(y_dtype)))
+        yv = gy.view(self._ydt(y_dtype), (1, n))
+        self._q.qmv_gemv_gather(p, rows_per_expert, expert_ids, x, y=yv, y_dtype=y_dtype, mode=mode,
+                                stream=stream)
+        self._finish([("y", gy)], [])
+        if y is not None:
+            y.copy_(yv.view_as(y))
+            return y
+        return yv.clone()
+
+    def qmv_gemv_argmax(self, p, x, workspace, residual=None, gamma=None, eps=1e-6, h_out=None, y=None,
+                        y_dtype=0, mode=0, stream=None, index=None, value=None):
+        gi = GuardBuf(4)
+        gv = GuardBuf(4)
+        iv, vv = gi.view(torch.int32, (1,)), gv.view(torch.float32, (1,))
+        gy, yv = (None, None) if y is None else guarded_like(y)
+        gh, hv = (None, None) if h_out is None else guarded_like(h_out)
+        gw = GuardBuf(workspace.numel() * workspace.element_size(), fill=0)
+        wv = gw.view(torch.uint8, (gw.nbytes,))
+        wv.copy_(workspace.view(torch.uint8).view(-1))
+        self._q.qmv_gemv_argmax(p, x, wv, residual=residual, gamma=gamma, eps=eps, h_out=hv, y=yv,
+                                y_dtype=y_dtype, mode=mode, stream=stream, index=iv, value=vv)
+        self._finish([("index", gi), ("value", gv), ("y", gy), ("h_out", gh), ("workspace", gw)],
+                     [(y, yv), (h_out, hv)])
+        workspace.view(torch.uint8).view(-1).copy_(wv)
+        if index is not None:
+            index.copy_(iv)
+        if value is not None:
+            value.copy_(vv)
+        return (index if index is not None else iv.clone()), (value if value is not None else vv.clone())
+
+
+def qmv_guarded():
+    """The binding with guard-band checks around every matvec output."""
+    return _GuardedQmv(qmv())

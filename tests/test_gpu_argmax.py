@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import EPS, TOL, Mat, acts, bits_equal, to_dev, qmv
+from gpu_util import EPS, TOL, Mat, acts, bits_equal, to_dev, qmv, qmv_guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +23,7 @@ def _ws():
                                             (4099, 2048, 8, 2048), (300, 256, 2, 32)])
 @pytest.mark.parametrize("fused", [False, True])
 def test_argmax_exact_equals_oracle(N, K, bits, group, fused):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"am{N}x{K}b{bits}", N, K, bits, group)
     x, r, g = acts(f"am{N}x{K}", 1, K, outliers=(K == 5376))
     ws = _ws()
@@ -48,7 +48,7 @@ def test_argmax_exact_equals_oracle(N, K, bits, group, fused):
 
 @pytest.mark.parametrize("N,K,bits,group", [(32768, 2048, 2, 32), (20000, 5376, 4, 32)])
 def test_argmax_fast_is_a_true_maximum(N, K, bits, group):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"amf{N}x{K}b{bits}", N, K, bits, group)
     x, _, _ = acts(f"amf{N}x{K}", 1, K)
     y = torch.zeros(1, N, dtype=torch.float32, device="cuda")
@@ -67,7 +67,7 @@ def test_argmax_fast_is_a_true_maximum(N, K, bits, group):
 @pytest.mark.parametrize("mode", ["fast", "exact"])
 def test_argmax_ties_take_the_first(mode):
     """three identical maximal rows planted among random ones: the lowest wins"""
-    q = qmv()
+    q = qmv_guarded()
     N, K = 40000, 2048
     codes = synth.codes(7, "amtie", N, K, 2)
     scales = synth.scales(7, "amtie", N, K // 32)
@@ -93,7 +93,7 @@ def test_argmax_full_size_lm_head_int2():
     """262144 x 2048 int2 (the decode token's lm_head), exact mode: the index is
     the first maximum of the stored logits and the oracle computes that row's
     value bit for bit"""
-    q = qmv()
+    q = qmv_guarded()
     head = Mat("full.head2", 262144, 2048, 2, 32)
     x, _, _ = acts("full.head2.am", 1, 2048)
     y = torch.zeros(1, 262144, dtype=torch.float32, device="cuda")

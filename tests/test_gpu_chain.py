@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import EPS, Mat, acts, bits_equal, first_diff, to_dev, qmv
+from gpu_util import EPS, GuardBuf, Mat, acts, bits_equal, first_diff, to_dev, qmv
 
 pytestmark = pytest.mark.gpu
 
@@ -37,9 +37,17 @@ def _bufs(tag):
     return d
 
 
-def _outs():
-    f = lambda n: torch.zeros(1, n, dtype=torch.float32, device="cuda")
-    h = lambda n: torch.zeros(1, n, dtype=torch.float16, device="cuda")
+def _outs(guards=None):
+    """the layer's outputs; with a guards list, each sits between guard
+    bands (appended to the list, to be checked after the chain runs)"""
+    def mk(n, dt):
+        if guards is None:
+            return torch.zeros(1, n, dtype=dt, device="cuda")
+        g = GuardBuf(n * (2 if dt == torch.float16 else 4))
+        guards.append(g)
+        return g.view(dt, (1, n))
+    f = lambda n: mk(n, torch.float32)
+    h = lambda n: mk(n, torch.float16)
     return {"h": h(2048), "h2": h(2048), "y_qkv": f(2560), "y_o": f(2048), "y_gu": f(16384),
             "y_down": f(2048)}
 
@@ -80,7 +88,8 @@ def test_decode_layers_chain_equals_calls(layers, mode):
     q = qmv()
     md = q.QMV_FAST if mode == "fast" else q.QMV_EXACT
     b = _bufs("L")
-    ref_o, got_o = _outs(), _outs()
+    guards = []
+    ref_o, got_o = _outs(), _outs(guards)
     # reference: the calls one by one, outputs snapshotted after each op
     ref = []
     for lay in layers:
@@ -96,6 +105,8 @@ def test_decode_layers_chain_equals_calls(layers, mode):
     ch.run()
     torch.cuda.synchronize()
     assert q.qmv_device_error(clear=True) == 0
+    for i, g in enumerate(guards):
+        g.check(f"chain output {i}")
     # the last layer's outputs equal the last calls' outputs
     for op, r in zip(ops[4:], ref[4:]):
         outs = list(op[5:]) if op[0] == "fused" else [op[3]]

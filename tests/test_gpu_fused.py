@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import EPS, Mat, acts, bits_equal, first_diff, to_dev, within_tol, qmv
+from gpu_util import EPS, Mat, acts, bits_equal, first_diff, to_dev, within_tol, qmv, qmv_guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
     (33, 64, 2, 32, 1, False),
 ])
 def test_fused_bit_exact(N, K, bits, group, M, outliers):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"fu{N}x{K}b{bits}", N, K, bits, group)
     x, r, g = acts(f"fu{N}x{K}m{M}", M, K, outliers)
     h = torch.empty(M, K, dtype=torch.float16, device="cuda")
@@ -41,7 +41,7 @@ def test_fused_bit_exact(N, K, bits, group, M, outliers):
 
 
 def test_fused_without_h_out():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("fu_noh", 512, 2048, 2, 32)
     x, r, g = acts("fu_noh", 1, 2048)
     y = q.qmv_fused_rmsnorm_gemv(m.pack, to_dev(x), to_dev(r), to_dev(g), EPS, mode=q.QMV_EXACT)
@@ -54,7 +54,7 @@ def test_fused_without_h_out():
 
 
 def test_fused_zero_input():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("fu_zero", 128, 1024, 2, 32)
     z = np.zeros((1, 1024), np.float16)
     _, _, g = acts("fu_zero", 1, 1024)

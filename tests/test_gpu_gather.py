@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import Mat, acts, bits_equal, first_diff, max_rel_err, to_dev, within_tol, qmv
+from gpu_util import Mat, acts, bits_equal, first_diff, max_rel_err, to_dev, within_tol, qmv, qmv_guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
                                                  (8, 700, 5376, 8, 5376), (32, 96, 256, 2, 32)])
 @pytest.mark.parametrize("mode", ["fast", "exact"])
 def test_gather_equals_gathered_rows(E, rows, K, bits, group, mode):
-    q = qmv()
+    q = qmv_guarded()
     md = q.QMV_FAST if mode == "fast" else q.QMV_EXACT
     m = Mat(f"ga{E}x{rows}x{K}b{bits}", E * rows, K, bits, group)
     x, _, _ = acts(f"ga{E}x{rows}", 1, K)
@@ -43,7 +43,7 @@ def test_gather_equals_gathered_rows(E, rows, K, bits, group, mode):
 def test_gather_ids_from_the_previous_kernel_with_pdl():
     """ids computed on the device right before the call (programmatic launch
     on): the kernel reads them only after that kernel completes"""
-    q = qmv()
+    q = qmv_guarded()
     E, rows, K = 128, 512, 2048
     m = Mat("gapdl", E * rows, K, 2, 32)
     x = to_dev(acts("gapdl", 1, K)[0])
@@ -65,7 +65,7 @@ def test_gather_ids_from_the_previous_kernel_with_pdl():
 
 
 def test_gather_invalid_id_gives_zeros_and_error_word():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("gabad", 4 * 256, 256, 2, 32)
     x = to_dev(acts("gabad", 1, 256)[0])
     q.qmv_device_error(clear=True)

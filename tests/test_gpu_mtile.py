@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from gpu_util import (EPS, Mat, acts, bits_equal, first_diff, max_rel_err, sample_rows, to_dev,
-                      within_tol, qmv)
+                      within_tol, qmv, qmv_guarded)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +32,7 @@ MS = [2, 3, 4, 7, 9, 16, 24, 33, 70]
 @pytest.mark.parametrize("N,K,bits,group", SHAPES)
 @pytest.mark.parametrize("M", MS)
 def test_mtile_exact_equals_oracle(N, K, bits, group, M):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"mt{N}x{K}b{bits}g{group}", N, K, bits, group)
     x, _, _ = acts(f"mt{N}x{K}m{M}", M, K)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_EXACT)
@@ -47,7 +47,7 @@ def test_mtile_exact_equals_oracle(N, K, bits, group, M):
 @pytest.mark.parametrize("N,K,bits,group", SHAPES)
 @pytest.mark.parametrize("M", [2, 5, 8, 13, 32, 40])
 def test_mtile_fast_columns_equal_m1(N, K, bits, group, M):
-    q = qmv()
+    q = qmv_guarded()
     if bits == 2 and M > 32:
         pytest.skip("int2 at M > 32 in fast mode runs the tensor tiles (hardware order)")
     m = Mat(f"mf{N}x{K}b{bits}g{group}", N, K, bits, group)
@@ -67,7 +67,7 @@ def test_mtile_fast_columns_equal_m1(N, K, bits, group, M):
 
 @pytest.mark.parametrize("mode", ["exact", "fast"])
 def test_mtile_fp16_output_is_rne_of_fp32(mode):
-    q = qmv()
+    q = qmv_guarded()
     md = q.QMV_EXACT if mode == "exact" else q.QMV_FAST
     m = Mat("mt16out", 700, 2304, 2, 32)
     x, _, _ = acts("mt16out", 11, 2304)
@@ -78,7 +78,7 @@ def test_mtile_fp16_output_is_rne_of_fp32(mode):
 
 
 def test_mtile_repeated_calls_identical():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("mtrep", 2000, 2048, 2, 32)
     x, _, _ = acts("mtrep", 16, 2048)
     xd = to_dev(x)
@@ -92,7 +92,7 @@ def test_mtile_repeated_calls_identical():
 def test_mtile_full_size_sampled(name, N, K, M):
     """the full projections at prefill chunk sizes: exact mode on sampled rows
     equals the oracle; fast mode equals the fast M = 1 results"""
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"mtfull.{name}", N, K, 2, 32)
     x, _, _ = acts(f"mtfull.{name}", M, K)
     xd = to_dev(x)
@@ -119,7 +119,7 @@ def test_mtile_fused_prologue(N, K, bits, group, M):
     """fused residual-add + RMSNorm before the tiles: h bit-exact, the exact
     mode bit-exact against the oracle, and every fast-mode column equal to the
     fused fast M = 1 result for that column"""
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"mfu{N}x{K}b{bits}g{group}", N, K, bits, group)
     x, r, g = acts(f"mfu{N}x{K}m{M}", M, K, outliers=(K == 5376))
     xd, rd, gd = to_dev(x), to_dev(r), to_dev(g)
@@ -146,7 +146,7 @@ def test_fused_above_32_columns(N, K, bits, group):
     """the fused prologue at M = 40: the pipelined tiles (K % 256 == 0) and the
     plain tiles in 32-column launches (K % 256 != 0) -- h and y bit-exact
     against the oracle in exact mode, fast columns equal to fused fast M = 1"""
-    q = qmv()
+    q = qmv_guarded()
     M = 40
     m = Mat(f"fu40.{N}x{K}b{bits}", N, K, bits, group)
     x, r, g = acts(f"fu40.{N}x{K}", M, K)
@@ -170,7 +170,7 @@ def test_fused_above_32_columns(N, K, bits, group):
 def test_mtile_max_columns():
     """M = 4096 (the largest chunk the ABI takes) on a small matrix: 1024 column
     chunks of one row tile each; exact mode bit-exact against the oracle"""
-    q = qmv()
+    q = qmv_guarded()
     N, K, M = 100, 256, 4096
     m = Mat("mtmax", N, K, 2, 32)
     x, _, _ = acts("mtmax", M, K)

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import Mat, acts, bits_equal, first_diff, max_rel_err, to_dev, within_tol, qmv
+from gpu_util import Mat, acts, bits_equal, first_diff, max_rel_err, to_dev, within_tol, qmv, qmv_guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
                                        (64, 64, 32), (2048, 4096, 32)])
 @pytest.mark.parametrize("M", [33, 64, 65, 100, 128, 200])
 def test_tensor_tiles_within_tolerance(N, K, group, M):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"tc{N}x{K}g{group}", N, K, 2, group)
     x, _, _ = acts(f"tc{N}x{K}m{M}", M, K)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_FAST)
@@ -30,7 +30,7 @@ def test_tensor_tiles_within_tolerance(N, K, group, M):
 
 
 def test_tensor_tiles_fp16_output():
-    q = qmv()
+    q = qmv_guarded()
     m = Mat("tc_f16", 512, 2048, 2, 32)
     x, _, _ = acts("tc_f16", 64, 2048)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), y_dtype=q.QMV_F16, mode=q.QMV_FAST)
@@ -44,7 +44,7 @@ def test_tensor_tiles_fp16_output():
 def test_tensor_tiles_repeatable(N, K):
     """split-K partials are added in split order by a second kernel: the same
     call gives the same bits every time (16 to 224 row tiles, splits 1 to 8)"""
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"tc_rep{N}x{K}", N, K, 2, 32)
     x, _, _ = acts(f"tc_rep{N}", 128, K)
     xd = to_dev(x)
@@ -59,7 +59,7 @@ def test_tensor_tiles_repeatable(N, K):
 def test_tensor_tiles_split_fp16_is_rne_of_fp32(M):
     """down-projection shape (16 row tiles, split K): the fp16 output is the RNE
     of the fp32 output, and both are within tolerance of the oracle"""
-    q = qmv()
+    q = qmv_guarded()
     N, K = 2048, 8192
     m = Mat("tc_split16", N, K, 2, 32)
     x, _, _ = acts(f"tc_split16m{M}", M, K)
@@ -77,7 +77,7 @@ def test_tensor_tiles_split_fp16_is_rne_of_fp32(M):
 
 @pytest.mark.parametrize("bits,M", [(4, 64), (8, 40), (2, 48)])
 def test_exact_above_32_columns_bit_exact(bits, M):
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"ex{bits}", 200, 1024, bits, 32)
     x, _, _ = acts(f"ex{bits}m{M}", M, 1024)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_EXACT)
@@ -91,7 +91,7 @@ def test_exact_above_32_columns_bit_exact(bits, M):
 def test_fast_wide_codes_above_32_columns(bits, M):
     """int4/int8 above 32 columns run the CUDA-core tiles in 32-column chunks:
     within tolerance, and every column equal to the fast M = 1 result."""
-    q = qmv()
+    q = qmv_guarded()
     m = Mat(f"ex{bits}", 200, 1024, bits, 32)
     x, _, _ = acts(f"ex{bits}m{M}", M, 1024)
     y = q.qmv_chunk_gemm(m.pack, to_dev(x), mode=q.QMV_FAST)
