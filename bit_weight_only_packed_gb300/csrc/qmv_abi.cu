@@ -109,15 +109,16 @@ static int check_common(const qmv_pack* p, int M, const void* x, void* y, int y_
 
 static size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-// The scratch of a call, following run_cuda_core's dispatch: the fused
-// prologue of the pipelined M-column tiles (M >= 2, K % 256 == 0), or the
-// tensor tiles' split-K partials (M > 32, fast mode, int2, no prologue).
+// The scratch of a call, following run_cuda_core's dispatch: the tensor
+// tiles' split-K partials (M > 32, fast mode, int2, no prologue), else the
+// pipelined M-column tiles' segment tables and the fused prologue's
+// activations (M >= 2, K % 256 == 0); nothing for M = 1 or for the 32-column
+// tiles that take K not a multiple of 256.
 static size_t workspace_need(const qmv_pack* p, int M, int y_dtype, int mode, int fused) {
-  if (M < 2 || M > 4096) return 0;
-  if (fused) return (p->K % 256 == 0) ? round256((size_t)M * (size_t)p->K * 2) : 0;
-  if (M > 32 && mode == QMV_FAST && p->bits == 2)
+  if (M < 2 || M > 4096 || p->K % 256 != 0) return 0;
+  if (!fused && M > 32 && mode == QMV_FAST && p->bits == 2)
     return round256(qmv::tc_workspace_bytes(M, p->N, p->K, y_dtype == QMV_F16));
-  return 0;
+  return qmv::mt_workspace_bytes(M, p->K, fused != 0);
 }
 
 static int check_workspace(const qmv_pack* p, int M, int y_dtype, int mode, int fused, void* ws,

@@ -80,6 +80,11 @@ int launch_tc_gemm(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err
 // Scratch bytes launch_tc_gemm needs for up to 128 columns of M (split-K
 // partial tiles; 0 when it needs none).
 size_t tc_workspace_bytes(int M, int N, int K, bool y_f16);
+// Scratch bytes launch_mtile needs: the segment tables of the M columns
+// (8960 bytes per 4 columns and 512 codes), after the fused prologue's
+// normalised activations (M x K fp16, 256-byte rounded); 0 where it does not
+// run (M < 2, K not a multiple of 256).
+size_t mt_workspace_bytes(int M, int K, bool fused);
 // Programmatic dependent launch of the M = 1 kernels (off by default).
 bool pdl_enabled();
 void set_pdl(bool on);
@@ -91,8 +96,9 @@ int record_cuda_error(cudaError_t e);
 // QMV_ERR_UNSUPPORTED when the shape does not fit them.
 int launch_tile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
 // M-column tiles on the bulk-copy pipeline (any M >= 2, K a multiple of 256,
-// no fused prologue), every column equal to the M = 1 result;
-// QMV_ERR_UNSUPPORTED when the shape does not fit them.
+// with or without the fused prologue), every column equal to the M = 1
+// result, on a.ws of at least mt_workspace_bytes (QMV_ERR_WORKSPACE
+// otherwise); QMV_ERR_UNSUPPORTED when the shape does not fit them.
 int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
 
 

@@ -9,31 +9,32 @@
 // the same per-block chains, block finish and serial fold over the blocks.
 //
 // Layout of the work:
+//   * a segment's activation table depends on the activations only, not on
+//     the weight rows, so a small kernel first builds every (column chunk,
+//     512-code segment) table once per call, with its block sums, into the
+//     caller's workspace (8960 bytes each; a few hundred KB that stay in L2);
 //   * a tile is R = 32*U weight rows x MC = 4 token columns over the whole K;
 //     a persistent CTA (one per SM) walks its tiles, each in segments of 512
 //     codes;
 //   * the copy warp brings, per segment, the tile's packed codes (one or more
 //     128-byte-swizzled boxes of R rows x 128 bytes), its group-32 scales and
-//     the MC x 512 fp16 activations into a ring of stages;
-//   * four table warps turn the activations into the segment's table (the
-//     M = 1 pipeline's scaled fp32 pairs, the MC columns side by side) and
-//     block sums, into one of two table buffers; one segment behind, they
-//     also fold: each thread owns one row's (row, column) accumulators and
-//     adds the previous segment's block results in block order, and stores
-//     the tile after its last segment;
+//     the segment's prebuilt table into a ring of stages;
 //   * compute warp w takes 64-code item w of the segment for all R rows: lane
 //     l holds rows l + 32u, decodes each code once and runs the paired-FMA
 //     chains of the MC columns (one 16-byte shared-memory broadcast serves two
 //     columns of U rows); the block results go to one of two fold buffers
-//     (one 16-byte store per row), so the compute warps only decode and FMA.
+//     (one 16-byte store per row), so the compute warps only decode and FMA;
+//   * four fold warps, one segment behind, add the block results in block
+//     order: each thread owns one row's (row, column) accumulators, and
+//     stores the tile after its last segment.
 // With the fused residual-add + RMSNorm prologue, a small kernel first forms
 // each column's h = fp16(x + r) (stored to h_out), its sum of squares in the
 // oracle's order and the normalised fp16 activations y = fp16((h*inv)*gamma)
-// into a stream-ordered scratch, once per column instead of once per row
-// tile; the tiles then run on that y, which is what the fused definition
+// into the workspace, once per column instead of once per row tile; the
+// tables are then built from that y, which is what the fused definition
 // feeds the matvec.
-// The roles meet only on mbarriers (stage full/empty, table full/empty, fold
-// buffer full/empty), so a slow warp delays the others by its lag, not by a
+// The roles meet only on mbarriers (stage full/empty, fold buffer
+// full/empty), so a slow warp delays the others by its lag, not by a
 // CTA-wide barrier per segment.  Every wait is bounded; a wait that runs out
 // records an error code in this file's device error word and the CTA winds
 // down.
@@ -56,11 +57,23 @@ constexpr int MT_ITEMS = MT_KS / 64;         // 64-code items per segment (one p
 constexpr int MT_BLOCKS = MT_KS / 32;        // 32-code blocks per segment
 constexpr int MT_MC = 4;                     // token columns per tile
 constexpr int MT_CW = MT_ITEMS;              // compute warps
-constexpr int MT_TW = 4;                     // table warps (fold and store too)
+constexpr int MT_TW = 4;                     // fold warps (fold and store)
 constexpr int MT_CT = 32 * MT_CW;            // compute threads
 constexpr int MT_THREADS = 32 * (MT_CW + MT_TW + 1);   // + the copy warp
 constexpr int MT_HDR = 1024;                 // barriers, flags
 constexpr int ERR_MT_TIMEOUT = 32;
+
+// One segment's table record, as the table kernel writes it to the workspace
+// and the copy warp brings it into a stage: per item 4 octets of 8 steps, a
+// step MC fp32 pairs (the columns side by side), each octet padded by 16
+// bytes, then the block sums [block][MC] (fast mode).
+constexpr int MT_OCT = 8 * MT_MC + 2;                    // u64 per octet
+constexpr int MT_TITEM = 4 * MT_OCT;                     // u64 per item
+constexpr int MT_TAB = MT_ITEMS * MT_TITEM * 8;          // table bytes
+constexpr int MT_YSUM = MT_BLOCKS * MT_MC * 4;           // block-sum bytes
+constexpr int MT_TBLK = MT_TAB + MT_YSUM;                // 8960 bytes a record
+constexpr int MT_TB_THREADS = 128;                       // threads of the table kernel
+static_assert(MT_TBLK % 256 == 0, "records start 256-byte aligned in the workspace; bulk copies move 16-byte multiples");
 
 // Shared-memory layout of one kernel variant (offsets from a 1024-byte
 // aligned base; the copies with 128-byte swizzle need 1024-byte aligned
@@ -72,43 +85,143 @@ struct MtLayout {
   static constexpr int NBOX = BITS / 2;                    // 128-byte code boxes per row per segment
   static constexpr int BOX = R * 128;
   static constexpr int SC_OFF = NBOX * BOX;                // scales: [R][16] fp16
-  static constexpr int X_OFF = SC_OFF + R * 32;            // activations: [2][MC][256] fp16
-  static constexpr int STAGE = (X_OFF + MC * 1024 + 1023) / 1024 * 1024;
+  static constexpr int TBL_OFF = SC_OFF + R * 32;          // the segment's table record
+  static constexpr int STAGE = (TBL_OFF + MT_TBLK + 1023) / 1024 * 1024;
   static constexpr int STAGES_OFF = MT_HDR;
-  // one table: per item 4 octets of 8 steps, a step MC fp32 pairs (the
-  // columns side by side), each octet padded by 16 bytes so that the table
-  // warps' stores of steps 8 apart fall in different banks
-  static constexpr int OCT = 8 * MC + 2;                   // u64 per octet
-  static constexpr int TITEM = 4 * OCT;                    // u64 per item
-  static constexpr int TAB = MT_ITEMS * TITEM * 8;
-  static constexpr int TAB_OFF = STAGES_OFF + MT_NS * STAGE;
-  static constexpr int YSUM = MT_BLOCKS * MC * 4;          // one set of block sums: [block][MC]
-  static constexpr int YSUM_OFF = TAB_OFF + 2 * TAB;
   static constexpr int TB = MT_BLOCKS * R * MC * 4;        // one fold buffer: [block][R][MC]
-  static constexpr int TB_OFF = YSUM_OFF + 2 * YSUM;
+  static constexpr int TB_OFF = STAGES_OFF + MT_NS * STAGE;
   static constexpr int BYTES = TB_OFF + 2 * TB;
   static constexpr int SMEM = BYTES + 1024;                // slack to align the base
-  static constexpr int FC = R * MC / (32 * MT_TW);        // columns folded per table-warp thread (one row)
+  static constexpr int FC = R * MC / (32 * MT_TW);        // columns folded per fold-warp thread (one row)
 };
 
 struct MtPlan {
   int tiles;     // row tiles x column chunks
   int CC;        // column chunks (of MC columns)
   int NSEG;      // segments per row (ceil(K / 512))
+  const unsigned char* tabs;   // table records [CC][NSEG] in the workspace
 };
 
-// mbarriers in the header: stage full/empty, table full/empty, fold buffer
-// full/empty
+// mbarriers in the header: stage full/empty, fold buffer full/empty
 struct MtBars {
   uint64_t full[MT_NS], empty[MT_NS];
-  uint64_t tfull[2], tempty[2];
   uint64_t bfull[2], bempty[2];
 };
+
+// Untiled bulk copy global -> shared (16-byte aligned ends, a multiple of 16
+// bytes), completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   sa(dst)),
+               "l"(src), "r"(bytes), "r"(sa(bar))
+               : "memory");
+}
+
+// The table of segment blockIdx.x for the column chunk blockIdx.y: the M = 1
+// pipeline's scaled fp32 pairs of each column, side by side, and (fast mode)
+// the block sums, in the record layout above.  Activations past M or K read
+// as zero.  Exact form: step k of an item holds (code k of block 0, code k of
+// block 1) * 2^-o(k); folded form: step 16*blk + CPW*p + j holds (code j of
+// word 2p, of word 2p + 1) * 2^(FOLD_E - o(j)).  The block sums add the
+// block's activations in the order of the dots (even and odd words serially,
+// then together) and scale by 2^(b-1).
+template <int BITS, bool FOLD>
+__global__ void __launch_bounds__(MT_TB_THREADS) mt_table_kernel(const __half* x, int M, int K, int NSEG,
+                                                                 unsigned char* tabs) {
+  constexpr int MC = MT_MC, CPW = 32 / BITS, HALF = CPW / 2;
+  __shared__ __align__(16) __half xs[2 * MC * 256];       // [half][m][256]
+  __shared__ __align__(16) u64 rec[MT_TBLK / 8];
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // x comes from the previous kernel, and it may still read the workspace
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int s = blockIdx.x, m0 = blockIdx.y * MC, tt = threadIdx.x;
+  for (int i = tt; i < MT_TBLK / 8; i += MT_TB_THREADS) rec[i] = 0ull;
+  for (int i = tt; i < MC * MT_KS / 8; i += MT_TB_THREADS) {
+    const int m = i / (MT_KS / 8), k = 8 * (i % (MT_KS / 8)), kk = s * MT_KS + k;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m0 + m < M && kk < K) v = *reinterpret_cast<const uint4*>(x + (int64_t)(m0 + m) * K + kk);
+    *reinterpret_cast<uint4*>(xs + (k >> 8) * (MC * 256) + m * 256 + (k & 255)) = v;
+  }
+  __syncthreads();
+  const int items = min(MT_ITEMS, (K - s * MT_KS) / 64);
+  // 8 fp16 activations of column m from element k (a multiple of 8)
+  auto chunk = [&](int m, int k, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xs + (k >> 8) * (MC * 256) + m * 256 + (k & 255));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __half2 h2 = u32_as_h2(w[e]);
+      f[2 * e] = __low2float(h2);
+      f[2 * e + 1] = __high2float(h2);
+    }
+  };
+  // task (m, item, quarter): 8 steps of one item for one column, from two
+  // 16-byte chunks of activations
+  for (int task = tt; task < MC * items * 4; task += MT_TB_THREADS) {
+    const int m = task / (items * 4), iq = task % (items * 4), item = iq >> 2, q = iq & 3;
+    const int hq = q & 1, blk = q >> 1;
+    float A[8], Bv[8];
+    if (!FOLD) {
+      chunk(m, 64 * item + 8 * q, A);          // block 0, codes 8q ..
+      chunk(m, 64 * item + 32 + 8 * q, Bv);    // block 1, codes 8q ..
+    } else {
+      const int a0 = 64 * item + 32 * blk + (BITS == 2 ? 8 : 16) * hq;
+      chunk(m, a0, A);
+      chunk(m, a0 + (BITS == 2 ? 16 : 8), Bv);
+    }
+    u64* dst = rec + (size_t)item * MT_TITEM + q * MT_OCT + m;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float v0, v1, sc;
+      if (!FOLD) {
+        sc = pow2f(-BITS * (((8 * q + i) % CPW) % HALF));
+        v0 = A[i];
+        v1 = Bv[i];
+      } else {
+        const int j = (8 * hq + i) % CPW;
+        sc = pow2f(FOLD_E - BITS * (j % HALF));
+        if (BITS == 8) {
+          v0 = (i < 4) ? A[i] : Bv[i - 4];
+          v1 = (i < 4) ? A[i + 4] : Bv[i];
+        } else {
+          v0 = A[i];
+          v1 = Bv[i];
+        }
+      }
+      dst[i * MC] = pk(__fmul_rn(v0, sc), __fmul_rn(v1, sc));
+    }
+  }
+  if (FOLD) {
+    float* ysum = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(rec) + MT_TAB);
+    for (int task = tt; task < MC * 2 * items; task += MT_TB_THREADS) {
+      const int m = task / (2 * items), bl = task % (2 * items);
+      float y[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float f[8];
+        chunk(m, 32 * bl + 8 * c, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[8 * c + e] = f[e];
+      }
+      float S0 = 0.0f, S1 = 0.0f;
+#pragma unroll
+      for (int t16 = 0; t16 < 16; ++t16) {
+        const int k0 = 2 * CPW * (t16 / CPW) + t16 % CPW;
+        S0 = __fadd_rn(S0, y[k0]);
+        S1 = __fadd_rn(S1, y[k0 + CPW]);
+      }
+      ysum[bl * MC + m] = __fmul_rn(__fadd_rn(S0, S1), (float)(1 << (BITS - 1)));
+    }
+  }
+  __syncthreads();
+  uint4* out = reinterpret_cast<uint4*>(tabs + ((size_t)blockIdx.y * NSEG + s) * MT_TBLK);
+  for (int i = tt; i < MT_TBLK / 16; i += MT_TB_THREADS) out[i] = reinterpret_cast<const uint4*>(rec)[i];
+}
 
 template <int BITS, bool FOLD, int U>
 __global__ void __launch_bounds__(MT_THREADS, 1)
     gemm_mt_kernel(GemvArgs a, MtPlan P, const __grid_constant__ CUtensorMap tm_codes,
-                   const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_x) {
+                   const __grid_constant__ CUtensorMap tm_scales) {
   using L = MtLayout<BITS, U>;
   constexpr int R = L::R, MC = L::MC;
   constexpr int CPW = 32 / BITS, HALF = CPW / 2, WPB = 32 / CPW, NP = 16 / CPW;
@@ -131,11 +244,9 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < MT_NS; ++s) {
       mbar_init(&B->full[s], 1);
-      mbar_init(&B->empty[s], MT_CW + MT_TW);
+      mbar_init(&B->empty[s], MT_CW);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&B->tfull[b], MT_TW);
-      mbar_init(&B->tempty[b], MT_CW);
       mbar_init(&B->bfull[b], MT_CW);
       mbar_init(&B->bempty[b], MT_TW);
     }
@@ -143,17 +254,19 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // activations come from the previous kernel, and it may still read y
+  // the tables come from the table kernel, and the previous kernel may still
+  // read y
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ------------------------------------------------------------ copies --
   if (warp == MT_CW + MT_TW) {
     if (lane == 0) {
-      const uint32_t tx = (uint32_t)(L::NBOX * L::BOX + (perrow ? 0 : R * 32) + MC * 1024);
+      const uint32_t tx = (uint32_t)(L::NBOX * L::BOX + (perrow ? 0 : R * 32) + MT_TBLK);
       int g = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < P.tiles && !stop; t += gridDim.x) {
-        const int r0 = (t / P.CC) * R, m0 = (t % P.CC) * MC;
+        const int r0 = (t / P.CC) * R, c = t % P.CC;
+        const unsigned char* trec = P.tabs + (size_t)c * P.NSEG * MT_TBLK;
         for (int s = 0; s < P.NSEG; ++s, ++g) {
           const int slot = g % MT_NS;
           if (g >= MT_NS &&
@@ -170,8 +283,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
 #pragma unroll
           for (int b = 0; b < L::NBOX; ++b) tma_2d(st + b * L::BOX, &tm_codes, s * 8 * BITS + 16 * b, r0, &B->full[slot]);
           if (!perrow) tma_2d(st + L::SC_OFF, &tm_scales, s * 16, r0, &B->full[slot]);
-          tma_2d(st + L::X_OFF, &tm_x, s * MT_KS, m0, &B->full[slot]);
-          tma_2d(st + L::X_OFF + MC * 512, &tm_x, s * MT_KS + 256, m0, &B->full[slot]);
+          bulk_g2s(st + L::TBL_OFF, trec + (size_t)s * MT_TBLK, MT_TBLK, &B->full[slot]);
         }
       }
       // let every copy issued land before the CTA can exit
@@ -180,164 +292,68 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
     return;
   }
 
-  // -------------------------------------------------------- table warps --
+  // --------------------------------------------------------- fold warps --
   if (warp >= MT_CW) {
+    // Thread tt owns FC columns of one row of the tile and adds each
+    // segment's block results in block order; after a tile's last segment it
+    // stores the tile.
     const int tt = tid - MT_CT;   // 0 .. 32*MT_TW - 1
-    // The fold, one segment behind the tables: thread tt owns FC columns of
-    // one row of the tile and adds the previous segment's block results in
-    // block order; after a tile's last segment it stores the tile.
     const int frow = tt % R, fc0 = (tt / R) * L::FC;
     float acc[L::FC];
 #pragma unroll
     for (int c = 0; c < L::FC; ++c) acc[c] = 0.0f;
-    int p_items = 0, p_r0 = 0, p_m0 = 0;
-    bool p_last = false;
-    auto fold_prev = [&](int gg) -> bool {
-      const int bb = gg & 1;
-      if (!mbar_wait_fast(&B->bfull[bb], (gg >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) return false;
-      const float* tb = reinterpret_cast<const float*>(sm + L::TB_OFF + bb * L::TB) + frow * MC + fc0;
-      float v[MT_BLOCKS][L::FC];
-#pragma unroll
-      for (int bl = 0; bl < MT_BLOCKS; ++bl)
-        if (bl < 2 * p_items) {
-          if constexpr (L::FC == 4) {
-            const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
-            v[bl][0] = f.x;
-            v[bl][1] = f.y;
-            v[bl][2] = f.z;
-            v[bl][3] = f.w;
-          } else if constexpr (L::FC == 2) {
-            const float2 f = *reinterpret_cast<const float2*>(tb + bl * R * MC);
-            v[bl][0] = f.x;
-            v[bl][1] = f.y;
-          } else {
-            v[bl][0] = tb[bl * R * MC];
-          }
-        }
-#pragma unroll
-      for (int bl = 0; bl < MT_BLOCKS; ++bl)
-        if (bl < 2 * p_items)
-#pragma unroll
-          for (int c = 0; c < L::FC; ++c) acc[c] = __fadd_rn(acc[c], v[bl][c]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B->bempty[bb]);
-      if (p_last) {
-        const int64_t n = (int64_t)p_r0 + frow;
-#pragma unroll
-        for (int c = 0; c < L::FC; ++c) {
-          const int col = p_m0 + fc0 + c;
-          if (n < a.N && col < a.M) {
-            float out = acc[c];
-            if (perrow) out = __fadd_rn(0.0f, __fmul_rn(out, __half2float(a.scales[n])));
-            const int64_t o = (int64_t)col * a.N + n;
-            if (a.y_f16)
-              reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(out);
-            else
-              reinterpret_cast<float*>(a.y)[o] = out;
-          }
-          acc[c] = 0.0f;
-        }
-      }
-      return true;
-    };
     int g = 0;
     for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
       const int r0 = (t / P.CC) * R, m0 = (t % P.CC) * MC;
       for (int s = 0; s < P.NSEG; ++s, ++g) {
-        const int slot = g % MT_NS, b = g & 1;
-        if (!mbar_wait_fast(&B->full[slot], (g / MT_NS) & 1, abort_f, ERR_MT_TIMEOUT, err)) return;
-        if (g >= 2 && !mbar_wait_fast(&B->tempty[b], ((g >> 1) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) return;
-        const unsigned char* st = sm + L::STAGES_OFF + slot * L::STAGE;
-        const __half* xs = reinterpret_cast<const __half*>(st + L::X_OFF);
-        u64* tab = reinterpret_cast<u64*>(sm + L::TAB_OFF + b * L::TAB);
-        float* ysum = reinterpret_cast<float*>(sm + L::YSUM_OFF + b * L::YSUM);
+        const int bb = g & 1;
         const int items = min(MT_ITEMS, (a.K - s * MT_KS) / 64);
-        // 8 fp16 activations of column m from element k (a multiple of 8)
-        auto chunk = [&](int m, int k, float (&f)[8]) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xs + (k >> 8) * (MC * 256) + m * 256 + (k & 255));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        if (!mbar_wait_fast(&B->bfull[bb], (g >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) return;
+        const float* tb = reinterpret_cast<const float*>(sm + L::TB_OFF + bb * L::TB) + frow * MC + fc0;
+        float v[MT_BLOCKS][L::FC];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 h2 = u32_as_h2(w[e]);
-            f[2 * e] = __low2float(h2);
-            f[2 * e + 1] = __high2float(h2);
-          }
-        };
-        // task (m, item, quarter): 8 steps of one item for one column, from
-        // two 16-byte chunks of activations; the lanes of a warp walk
-        // (item, quarter) within a column
-        for (int task = tt; task < MC * items * 4; task += 32 * MT_TW) {
-          const int m = task / (items * 4), iq = task % (items * 4), item = iq >> 2, q = iq & 3;
-          const int hq = q & 1, blk = q >> 1;
-          float A[8], Bv[8];
-          if (!FOLD) {
-            chunk(m, 64 * item + 8 * q, A);          // block 0, codes 8q ..
-            chunk(m, 64 * item + 32 + 8 * q, Bv);    // block 1, codes 8q ..
-          } else {
-            const int a0 = 64 * item + 32 * blk + (BITS == 2 ? 8 : 16) * hq;
-            chunk(m, a0, A);
-            chunk(m, a0 + (BITS == 2 ? 16 : 8), Bv);
-          }
-          u64* dst = tab + (size_t)item * L::TITEM + q * L::OCT + m;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float v0, v1, sc;
-            if (!FOLD) {
-              // step k = 8q + i: (code k of block 0, code k of block 1) * 2^-o(k)
-              sc = pow2f(-BITS * (((8 * q + i) % CPW) % HALF));
-              v0 = A[i];
-              v1 = Bv[i];
+        for (int bl = 0; bl < MT_BLOCKS; ++bl)
+          if (bl < 2 * items) {
+            if constexpr (L::FC == 4) {
+              const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
+              v[bl][0] = f.x;
+              v[bl][1] = f.y;
+              v[bl][2] = f.z;
+              v[bl][3] = f.w;
+            } else if constexpr (L::FC == 2) {
+              const float2 f = *reinterpret_cast<const float2*>(tb + bl * R * MC);
+              v[bl][0] = f.x;
+              v[bl][1] = f.y;
             } else {
-              // step 16*blk + CPW*p + j: (code j of word 2p, of word 2p+1)
-              const int j = (8 * hq + i) % CPW;
-              sc = pow2f(FOLD_E - BITS * (j % HALF));
-              if (BITS == 8) {
-                v0 = (i < 4) ? A[i] : Bv[i - 4];
-                v1 = (i < 4) ? A[i + 4] : Bv[i];
-              } else {
-                v0 = A[i];
-                v1 = Bv[i];
-              }
+              v[bl][0] = tb[bl * R * MC];
             }
-            dst[i * MC] = pk(__fmul_rn(v0, sc), __fmul_rn(v1, sc));
           }
-        }
-        if (FOLD) {
-          // per block, the activation sum in the order of the dots (even and
-          // odd words serially, then added), times 2^(b-1)
-          for (int task = tt; task < MC * 2 * items; task += 32 * MT_TW) {
-            const int m = task / (2 * items), bl = task % (2 * items);
-            float y[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float f[8];
-              chunk(m, 32 * bl + 8 * c, f);
+        for (int bl = 0; bl < MT_BLOCKS; ++bl)
+          if (bl < 2 * items)
 #pragma unroll
-              for (int e = 0; e < 8; ++e) y[8 * c + e] = f[e];
-            }
-            float S0 = 0.0f, S1 = 0.0f;
-#pragma unroll
-            for (int t16 = 0; t16 < 16; ++t16) {
-              const int k0 = 2 * CPW * (t16 / CPW) + t16 % CPW;
-              S0 = __fadd_rn(S0, y[k0]);
-              S1 = __fadd_rn(S1, y[k0 + CPW]);
-            }
-            ysum[bl * MC + m] = __fmul_rn(__fadd_rn(S0, S1), (float)(1 << (BITS - 1)));
-          }
-        }
+            for (int c = 0; c < L::FC; ++c) acc[c] = __fadd_rn(acc[c], v[bl][c]);
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&B->tfull[b]);
-          mbar_arrive(&B->empty[slot]);
+        if (lane == 0) mbar_arrive(&B->bempty[bb]);
+        if (s == P.NSEG - 1) {
+          const int64_t n = (int64_t)r0 + frow;
+#pragma unroll
+          for (int c = 0; c < L::FC; ++c) {
+            const int col = m0 + fc0 + c;
+            if (n < a.N && col < a.M) {
+              float out = acc[c];
+              if (perrow) out = __fadd_rn(0.0f, __fmul_rn(out, __half2float(a.scales[n])));
+              const int64_t o = (int64_t)col * a.N + n;
+              if (a.y_f16)
+                reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(out);
+              else
+                reinterpret_cast<float*>(a.y)[o] = out;
+            }
+            acc[c] = 0.0f;
+          }
         }
-        if (g >= 1 && !fold_prev(g - 1)) return;
-        p_items = items;
-        p_r0 = r0;
-        p_m0 = m0;
-        p_last = (s == P.NSEG - 1);
       }
     }
-    if (g >= 1) fold_prev(g - 1);
     return;
   }
 
@@ -349,14 +365,13 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
       const int slot = g % MT_NS, b = g & 1;
       const int items = min(MT_ITEMS, (a.K - s * MT_KS) / 64);
       if (ok) ok = mbar_wait_fast(&B->full[slot], (g / MT_NS) & 1, abort_f, ERR_MT_TIMEOUT, err);
-      if (ok) ok = mbar_wait_fast(&B->tfull[b], (g >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
       if (ok && g >= 2) ok = mbar_wait_fast(&B->bempty[b], ((g >> 1) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
 
       // item `warp` of the segment for all R rows (lane: rows lane + 32u)
       if (ok && warp < items) {
         const unsigned char* st = sm + L::STAGES_OFF + slot * L::STAGE;
-        const u64* tabi = reinterpret_cast<const u64*>(sm + L::TAB_OFF + b * L::TAB) + (size_t)warp * L::TITEM;
-        const float* ysum = reinterpret_cast<const float*>(sm + L::YSUM_OFF + b * L::YSUM);
+        const u64* tabi = reinterpret_cast<const u64*>(st + L::TBL_OFF) + (size_t)warp * MT_TITEM;
+        const float* ysum = reinterpret_cast<const float*>(st + L::TBL_OFF + MT_TAB);
         float* tb = reinterpret_cast<float*>(sm + L::TB_OFF + b * L::TB);
         const int item = warp;
         const unsigned char* cbox = st + (item / IPB) * L::BOX;
@@ -400,7 +415,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
 #pragma unroll
                 for (int u = 0; u < U; ++u) v[u] = ((j < HALF) ? lo[u] : hi[u]) & mm64;
                 const int tq = CPW * p + j;   // step 16*blk + tq
-                const u64* yk = tabi + (2 * blk + (tq >> 3)) * L::OCT + (tq & 7) * MC;
+                const u64* yk = tabi + (2 * blk + (tq >> 3)) * MT_OCT + (tq & 7) * MC;
 #pragma unroll
                 for (int mm = 0; mm < MC; mm += 2) {
                   const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
@@ -464,7 +479,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
                 v[u] = decode2(wa, wb, MASK << o, pk(offf, offf));
               }
               const int tk = wi * CPW + j;   // step
-              const u64* yk = tabi + (tk >> 3) * L::OCT + (tk & 7) * MC;
+              const u64* yk = tabi + (tk >> 3) * MT_OCT + (tk & 7) * MC;
 #pragma unroll
               for (int mm = 0; mm < MC; mm += 2) {
                 const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
@@ -494,11 +509,10 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
           }
         }
       }
-      // the stage, the table and this warp's share of the fold buffer are done
+      // the stage and this warp's share of the fold buffer are done
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&B->empty[slot]);
-        mbar_arrive(&B->tempty[b]);
         mbar_arrive(&B->bfull[b]);
       }
     }
@@ -564,6 +578,36 @@ int read_mt_error(int clear, int* out) {
 
 namespace {
 
+// Launch on s, as a programmatic dependent of the previous kernel when PDL is
+// on (every kernel here waits for its predecessor with griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+cudaError_t mt_launch(void (*kern)(KArgs...), dim3 grid, int threads, size_t smem, cudaStream_t s,
+                      Args... args) {
+  if (pdl_enabled()) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+  }
+  kern<<<grid, threads, smem, s>>>(args...);
+  return cudaGetLastError();
+}
+
+size_t mt_table_bytes(int M, int K) {
+  const size_t CC = (size_t)(M + MT_MC - 1) / MT_MC, NSEG = (size_t)(K + MT_KS - 1) / MT_KS;
+  return CC * NSEG * MT_TBLK;
+}
+
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// The table kernel, then the tiles on its records (a.ws: the records).
 template <int BITS, bool FOLD, int U>
 int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   using L = MtLayout<BITS, U>;
@@ -572,15 +616,15 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   static thread_local KernCache cache;
   const DevInfo& d = dev_info();
   if ((size_t)L::SMEM > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
+  if (!a.ws || a.ws_bytes < mt_table_bytes(a.M, a.K)) return QMV_ERR_WORKSPACE;
   int occ = 0;
   cudaError_t e = prep_kernel(kern, cache, MT_THREADS, L::SMEM, &occ);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   if (occ < 1) return QMV_ERR_UNSUPPORTED;
   // codes as UINT64 [N][row_bytes/8] (box 16 x R, 128-byte swizzle), scales
-  // as UINT16 [N][K/32] (box 16 x R), activations as FP16 [M][K] (box 256 x
-  // MC); rows past N or M and columns past K are zero-filled
+  // as UINT16 [N][K/32] (box 16 x R); rows past N are zero-filled
   const uint64_t row_bytes = (uint64_t)a.K * BITS / 8;
-  CUtensorMap tmc, tms, tmx;
+  CUtensorMap tmc, tms;
   if (!enc2d(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT64, a.codes, row_bytes / 8, (uint64_t)a.N, row_bytes, 16, R,
              CU_TENSOR_MAP_SWIZZLE_128B))
     return QMV_ERR_UNSUPPORTED;
@@ -589,29 +633,16 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   else if (!enc2d(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.scales, (uint64_t)a.G, (uint64_t)a.N,
                   (uint64_t)a.G * 2, 16, R, CU_TENSOR_MAP_SWIZZLE_NONE))
     return QMV_ERR_UNSUPPORTED;
-  if (!enc2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 256, MC,
-             CU_TENSOR_MAP_SWIZZLE_NONE))
-    return QMV_ERR_UNSUPPORTED;
   MtPlan P;
   P.CC = (a.M + MC - 1) / MC;
   P.tiles = (int)(((int64_t)a.N + R - 1) / R) * P.CC;
   P.NSEG = (a.K + MT_KS - 1) / MT_KS;
-  const int grid = P.tiles < d.sms ? P.tiles : d.sms;
-  if (pdl_enabled()) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(MT_THREADS);
-    cfg.dynamicSmemBytes = L::SMEM;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, a, P, tmc, tms, tmx);
-  } else {
-    kern<<<grid, MT_THREADS, L::SMEM, s>>>(a, P, tmc, tms, tmx);
-    e = cudaGetLastError();
+  P.tabs = reinterpret_cast<const unsigned char*>(a.ws);
+  e = mt_launch(mt_table_kernel<BITS, FOLD>, dim3(P.NSEG, P.CC), MT_TB_THREADS, 0, s, a.x, a.M, a.K, P.NSEG,
+                reinterpret_cast<unsigned char*>(a.ws));
+  if (e == cudaSuccess) {
+    const int grid = P.tiles < d.sms ? P.tiles : d.sms;
+    e = mt_launch(kern, dim3(grid), MT_THREADS, L::SMEM, s, a, P, tmc, tms);
   }
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   return QMV_OK;
@@ -653,53 +684,39 @@ int mt_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
 
 static int launch_mtile_plain(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
 
+size_t mt_workspace_bytes(int M, int K, bool fused) {
+  if (M < 2 || K % 256 != 0) return 0;
+  return (fused ? round256((size_t)M * K * sizeof(__half)) : 0) + mt_table_bytes(M, K);
+}
+
 int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
   if (a.M < 2 || a.K % 256 != 0 || a.gather_rows || a.amax_ws) return QMV_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(a.x) & 15u) != 0) return QMV_ERR_UNSUPPORTED;
+  if (!a.ws || a.ws_bytes < mt_workspace_bytes(a.M, a.K, a.fused != 0)) return QMV_ERR_WORKSPACE;
   if (!a.fused) return launch_mtile_plain(a, bits, s, err);
-  // fused prologue: the normalised activations into the caller's workspace
-  // (checked by the ABI), then the plain tiles on them
-  if (!a.ws || a.ws_bytes < (size_t)a.M * a.K * sizeof(__half)) return QMV_ERR_WORKSPACE;
+  // fused prologue: the normalised activations into the front of the
+  // caller's workspace, then the tables and tiles on them
+  const size_t ysz = round256((size_t)a.M * a.K * sizeof(__half));
   __half* yn = reinterpret_cast<__half*>(a.ws);
   cudaError_t e = cudaSuccess;
   const size_t psm = (size_t)(a.K / 32) * sizeof(float);
   if (psm > 48 * 1024) {
     e = cudaFuncSetAttribute(rms_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
   }
-  if (e == cudaSuccess) {
-    if (pdl_enabled()) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cfg.gridDim = dim3(a.M);
-      cfg.blockDim = dim3(256);
-      cfg.dynamicSmemBytes = psm;
-      cfg.stream = s;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      e = cudaLaunchKernelEx(&cfg, rms_prologue_kernel, a, yn);
-    } else {
-      rms_prologue_kernel<<<a.M, 256, psm, s>>>(a, yn);
-      e = cudaGetLastError();
-    }
-  }
-  int rc = QMV_OK;
+  if (e == cudaSuccess) e = mt_launch(rms_prologue_kernel, dim3(a.M), 256, psm, s, a, yn);
   if (e != cudaSuccess) {
     *err = e;
-    rc = QMV_ERR_CUDA;
-  } else {
-    GemvArgs b = a;
-    b.x = yn;
-    b.fused = 0;
-    b.r = nullptr;
-    b.gamma = nullptr;
-    b.h_out = nullptr;
-    b.ws = nullptr;
-    b.ws_bytes = 0;
-    rc = launch_mtile_plain(b, bits, s, err);
+    return QMV_ERR_CUDA;
   }
-  return rc;
+  GemvArgs b = a;
+  b.x = yn;
+  b.fused = 0;
+  b.r = nullptr;
+  b.gamma = nullptr;
+  b.h_out = nullptr;
+  b.ws = reinterpret_cast<unsigned char*>(a.ws) + ysz;
+  b.ws_bytes = a.ws_bytes - ysz;
+  return launch_mtile_plain(b, bits, s, err);
 }
 
 static int launch_mtile_plain(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {

@@ -199,14 +199,22 @@ def workspace(p: Pack, M: int, y_dtype=QMV_F32, mode=QMV_FAST, fused=False, devi
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda") if n else None
 
 
-def _ws(p, M, y_dtype, mode, fused, ws, like):
+def _ws(p, M, y_dtype, mode, fused, ws, like, stream=None):
     """The caller's workspace, checked, or (when none is given) a fresh torch
-    allocation of the size the call needs: (pointer, bytes, tensor)."""
+    allocation of the size the call needs: (pointer, bytes, tensor).  A fresh
+    one used on another stream than torch's current one is recorded on that
+    stream, so the allocator does not hand it out again before the call ends."""
     n = qmv_workspace_bytes(p, M, y_dtype, mode, fused)
     if ws is None:
         if n == 0:
             return None, 0, None
         ws = torch.empty(n, dtype=torch.uint8, device=like.device)
+        if stream is not None:
+            cur = torch.cuda.current_stream(like.device)
+            if _stream(stream) != cur.cuda_stream:
+                ts = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(
+                    int(stream), device=like.device)
+                ws.record_stream(ts)
     _need_bytes("workspace", ws, n)
     return _dptr(ws), ws.numel() * ws.element_size(), ws
 
@@ -216,7 +224,7 @@ def qmv_gemv(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=None, M=
     _need("x", x, torch.float16, M * p.K)
     _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
-    wp, wb, _keep = _ws(p, M, y_dtype, mode, False, workspace, x)
+    wp, wb, _keep = _ws(p, M, y_dtype, mode, False, workspace, x, stream)
     _check("qmv_gemv", _lib.qmv_gemv(p.handle, M, p.N, p.K, p.bits, p.group, _dptr(x), _dptr(y),
                                      y_dtype, mode, wp, wb, _stream(stream)))
     return y
@@ -227,7 +235,7 @@ def qmv_chunk_gemm(p: Pack, x, y=None, y_dtype=QMV_F32, mode=QMV_FAST, stream=No
     _need("x", x, torch.float16, M * p.K)
     _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
-    wp, wb, _keep = _ws(p, M, y_dtype, mode, False, workspace, x)
+    wp, wb, _keep = _ws(p, M, y_dtype, mode, False, workspace, x, stream)
     _check("qmv_chunk_gemm", _lib.qmv_chunk_gemm(p.handle, M, _dptr(x), _dptr(y), y_dtype, mode,
                                                  wp, wb, _stream(stream)))
     return y
@@ -242,7 +250,7 @@ def qmv_fused_rmsnorm_gemv(p: Pack, x, residual, gamma, eps=1e-6, h_out=None, y=
     _need("h_out", h_out, torch.float16, M * p.K)
     _need("y", y, _YDT.get(y_dtype), M * p.N)
     y = _out(y, M, p.N, y_dtype, x)
-    wp, wb, _keep = _ws(p, M, y_dtype, mode, True, workspace, x)
+    wp, wb, _keep = _ws(p, M, y_dtype, mode, True, workspace, x, stream)
     _check("qmv_fused_rmsnorm_gemv", _lib.qmv_fused_rmsnorm_gemv(
         p.handle, M, _dptr(x), _dptr(residual), _dptr(gamma), float(eps), _dptr(h_out), _dptr(y),
         y_dtype, mode, wp, wb, _stream(stream)))

@@ -125,13 +125,18 @@ QMV_API int qmv_pack_weights(qmv_pack *p, const int8_t *d_codes_in, const uint16
 /*
  * qmv_workspace_bytes -- device scratch bytes that a call of qmv_gemv /
  * qmv_chunk_gemm (fused = 0) or qmv_fused_rmsnorm_gemv (fused = 1) with this
- * pack, M, y_dtype and mode needs in its d_workspace: fp32 split-K partial
- * tiles of the tensor-core tiles (M > 32, QMV_FAST, int2) when the chosen
- * split needs more than the output itself, or the fused prologue's
- * normalised activations (M x K fp16) for M >= 2; 0 when the call needs none
- * (always for M = 1).  The size depends only on these arguments and the
- * device's SM count, so one workspace serves every later call with them.
- * Host only; 0 for invalid arguments.
+ * pack, M, y_dtype and mode needs in its d_workspace:
+ *   - M = 1, or K not a multiple of 256: 0.
+ *   - M > 32, QMV_FAST, int2, fused = 0 (the tensor-core tiles): fp32
+ *     split-K partial tiles when the chosen split needs more than the output
+ *     itself, else 0.
+ *   - every other M >= 2 (the CUDA-core M-column tiles): the activation
+ *     tables, built once per call, ceil(M/4) * ceil(K/512) * 8960 bytes,
+ *     after (fused = 1) the prologue's normalised activations, M x K fp16
+ *     rounded up to 256 bytes.
+ * The size depends only on these arguments and the device's SM count, so one
+ * workspace serves every later call with them.  Host only; 0 for invalid
+ * arguments.
  */
 QMV_API size_t qmv_workspace_bytes(const qmv_pack *p, int M, int y_dtype, int mode, int fused);
 

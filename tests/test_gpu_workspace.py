@@ -1,9 +1,10 @@
-"""Calls that need scratch take it from the caller's workspace: the fused
-prologue's normalised activations (M >= 2) and the tensor tiles' split-K
-partial tiles.  On an explicit workspace whose contents are garbage, results
-equal the oracle (exact mode bit for bit; tensor tiles within tolerance) and
-the binding's own path; a missing or short workspace is refused before any
-launch, and the workspace's guard bands stay intact."""
+"""Calls that need scratch take it from the caller's workspace: the M-column
+tiles' segment tables, the fused prologue's normalised activations (M >= 2)
+and the tensor tiles' split-K partial tiles.  On an explicit workspace whose
+contents are garbage, results equal the oracle (exact mode bit for bit;
+tensor tiles within tolerance) and the binding's own path; a missing or short
+workspace is refused before any launch, and the workspace's guard bands stay
+intact."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +18,12 @@ pytestmark = pytest.mark.gpu
 
 def _bits(t):
     return t.view(torch.int16) if t.dtype == torch.float16 else t.view(torch.int32)
+
+
+def _tables(M, K):
+    """Bytes of the M-column tiles' table records: 8960 per 4 columns and 512
+    codes."""
+    return -(-M // 4) * -(-K // 512) * 8960
 
 
 def _ws(q, p, M, y_dtype, mode, fused):
@@ -35,7 +42,7 @@ def test_fused_m16_on_caller_workspace(mode):
     x, r, g = acts("ws.fused", M, K)
     xd, rd, gd = to_dev(x), to_dev(r), to_dev(g)
     gw, ws = _ws(q, m.pack, M, q.QMV_F32, md, True)
-    assert gw.nbytes == M * K * 2
+    assert gw.nbytes == M * K * 2 + _tables(M, K)
     h = torch.empty(M, K, dtype=torch.float16, device="cuda")
     y = q.qmv_fused_rmsnorm_gemv(m.pack, xd, rd, gd, EPS, h_out=h, mode=md, workspace=ws)
     y_auto = q.qmv_fused_rmsnorm_gemv(m.pack, xd, rd, gd, EPS, mode=md)
@@ -99,4 +106,85 @@ def test_missing_or_short_workspace_is_refused():
     # a call that needs none accepts none
     assert q.qmv_workspace_bytes(m.pack, 1, q.QMV_F16, q.QMV_FAST, False) == 0
     assert lib.qmv_gemv(m.pack.handle, 1, N, K, 2, 32, xd.data_ptr(), y.data_ptr(), 1, 0, None, 0, s) == 0
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("mode", ["exact", "fast"])
+@pytest.mark.parametrize("M", [2, 7, 16])
+def test_mtile_tables_on_caller_workspace(mode, M):
+    # the tables are built into a garbage-filled workspace, which then serves a
+    # second call; every column equals the M = 1 result bit for bit
+    q = qmv()
+    md = q.QMV_EXACT if mode == "exact" else q.QMV_FAST
+    N, K = 700, 4352          # a ragged row tile and a half last segment
+    m = Mat("ws.mt", N, K, 4, 32)
+    x, _, _ = acts("ws.mt", M, K)
+    xd = to_dev(x)
+    gw, ws = _ws(q, m.pack, M, q.QMV_F32, md, False)
+    assert gw.nbytes == _tables(M, K)
+    y = q.qmv_chunk_gemm(m.pack, xd, mode=md, workspace=ws)
+    ws.fill_(0xC3)
+    y2 = q.qmv_chunk_gemm(m.pack, xd, mode=md, workspace=ws)
+    y1 = [q.qmv_gemv(m.pack, xd[i:i + 1], mode=md) for i in range(M)]
+    torch.cuda.synchronize()
+    gw.check("workspace")
+    assert torch.equal(_bits(y), _bits(y2))
+    for i in range(M):
+        assert torch.equal(_bits(y[i]), _bits(y1[i][0])), i
+    if mode == "exact":
+        codes, scales = m.host()
+        ref = oracle.gemv(codes, scales, 32, x)
+        got = y.cpu().numpy()
+        assert bits_equal(got, ref), first_diff(got, ref)
+    assert q.qmv_device_error(clear=True) == 0
+
+
+def test_calls_in_turn_share_one_workspace_under_pdl():
+    # gate/up-like then down-like then gate/up-like again on one workspace,
+    # with programmatic dependent launch: a call's table kernel must not
+    # overwrite the records while the previous call's tiles still read them
+    q = qmv()
+    A = Mat("ws.pdlA", 2048, 4096, 2, 32)
+    B = Mat("ws.pdlB", 1024, 8192, 4, 32)
+    M = 16
+    xa, _, _ = acts("ws.pdlA", M, 4096)
+    xb, _, _ = acts("ws.pdlB", M, 8192)
+    xad, xbd = to_dev(xa), to_dev(xb)
+    ref = [q.qmv_chunk_gemm(A.pack, xad), q.qmv_chunk_gemm(B.pack, xbd)]
+    n = max(q.qmv_workspace_bytes(A.pack, M), q.qmv_workspace_bytes(B.pack, M))
+    gw = GuardBuf(n, fill=0x5A)
+    ws = gw.view(torch.uint8, (n,))
+    torch.cuda.synchronize()
+    q.qmv_set_pdl(True)
+    try:
+        outs = []
+        for _ in range(3):
+            outs.append(q.qmv_chunk_gemm(A.pack, xad, workspace=ws))
+            outs.append(q.qmv_chunk_gemm(B.pack, xbd, workspace=ws))
+        torch.cuda.synchronize()
+    finally:
+        q.qmv_set_pdl(False)
+    gw.check("workspace")
+    for i, o in enumerate(outs):
+        assert torch.equal(_bits(o), _bits(ref[i % 2])), i
+    assert q.qmv_device_error(clear=True) == 0
+
+
+def test_mtile_missing_workspace_is_refused():
+    q = qmv()
+    N, K, M = 256, 1024, 8
+    m = Mat("ws.mtshort", N, K, 2, 32)
+    xd = torch.zeros(M, K, dtype=torch.float16, device="cuda")
+    y = torch.zeros(M, N, dtype=torch.float32, device="cuda")
+    n = q.qmv_workspace_bytes(m.pack, M, q.QMV_F32, q.QMV_EXACT, False)
+    assert n == _tables(M, K)
+    lib, s = q.lib(), torch.cuda.current_stream().cuda_stream
+    for mode in (0, 1):
+        assert lib.qmv_chunk_gemm(m.pack.handle, M, xd.data_ptr(), y.data_ptr(), 0, mode, None, 0,
+                                  s) == q.QMV_ERR_WORKSPACE
+        assert lib.qmv_gemv(m.pack.handle, M, N, K, 2, 32, xd.data_ptr(), y.data_ptr(), 0, mode, None, 0,
+                            s) == q.QMV_ERR_WORKSPACE
+    short = torch.empty(n, dtype=torch.uint8, device="cuda")
+    assert lib.qmv_chunk_gemm(m.pack.handle, M, xd.data_ptr(), y.data_ptr(), 0, 1, short.data_ptr(), n - 16,
+                              s) == q.QMV_ERR_WORKSPACE
     torch.cuda.synchronize()
