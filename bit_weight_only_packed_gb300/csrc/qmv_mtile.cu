@@ -19,14 +19,16 @@
 //   * the copy warp brings, per segment, the tile's packed codes (one or more
 //     128-byte-swizzled boxes of R rows x 128 bytes), its group-32 scales and
 //     the segment's prebuilt table into a ring of stages;
-//   * compute warp w takes 64-code item w of the segment for all R rows: lane
-//     l holds rows l + 32u, decodes each code once and runs the paired-FMA
-//     chains of the MC columns (one 16-byte shared-memory broadcast serves two
-//     columns of U rows); the block results go to one of two fold buffers
-//     (one 16-byte store per row), so the compute warps only decode and FMA;
-//   * four fold warps, one segment behind, add the block results in block
-//     order: each thread owns one row's (row, column) accumulators, and
-//     stores the tile after its last segment.
+//   * each 64-code item of the segment goes to one compute warp (two for
+//     128-row tiles, each taking half the rows): lane l holds rows l + 32u,
+//     decodes each code once and runs the paired-FMA chains of the MC columns
+//     (one 16-byte shared-memory broadcast serves two columns of its rows);
+//     the block results go to one of two fold buffers (one 16-byte store per
+//     row), so the compute warps only decode and FMA;
+//   * the fold warps (four, or two beside sixteen compute warps), one segment
+//     behind, add the block results in block order: each thread owns some
+//     rows' (row, column) accumulators, and stores them after the tile's last
+//     segment.
 // With the fused residual-add + RMSNorm prologue, a small kernel first forms
 // each column's h = fp16(x + r) (stored to h_out), its sum of squares in the
 // oracle's order and the normalised fp16 activations y = fp16((h*inv)*gamma)
@@ -56,10 +58,6 @@ constexpr int MT_KS = 512;                   // codes per segment
 constexpr int MT_ITEMS = MT_KS / 64;         // 64-code items per segment (one per compute warp)
 constexpr int MT_BLOCKS = MT_KS / 32;        // 32-code blocks per segment
 constexpr int MT_MC = 4;                     // token columns per tile
-constexpr int MT_CW = MT_ITEMS;              // compute warps
-constexpr int MT_TW = 4;                     // fold warps (fold and store)
-constexpr int MT_CT = 32 * MT_CW;            // compute threads
-constexpr int MT_THREADS = 32 * (MT_CW + MT_TW + 1);   // + the copy warp
 constexpr int MT_HDR = 1024;                 // barriers, flags
 constexpr int ERR_MT_TIMEOUT = 32;
 
@@ -82,6 +80,14 @@ template <int BITS, int U>
 struct MtLayout {
   static constexpr int MC = MT_MC;
   static constexpr int R = 32 * U;                         // rows per tile
+  // 128-row tiles split each item's rows over two compute warps (four per
+  // scheduler: more warps to hide the paired FMAs' and loads' latencies);
+  // smaller tiles keep one warp per item (two rows or one a lane)
+  static constexpr int CWI = (U >= 4) ? 2 : 1;             // compute warps per item (row halves)
+  static constexpr int UW = U / CWI;                       // rows per lane of a compute warp
+  static constexpr int CW = MT_ITEMS * CWI;                // compute warps
+  static constexpr int TW = (CWI == 2) ? 2 : 4;            // fold warps (within the register file)
+  static constexpr int THREADS = 32 * (CW + TW + 1);       // + fold warps + the copy warp
   static constexpr int NBOX = BITS / 2;                    // 128-byte code boxes per row per segment
   static constexpr int BOX = R * 128;
   static constexpr int SC_OFF = NBOX * BOX;                // scales: [R][16] fp16
@@ -92,7 +98,11 @@ struct MtLayout {
   static constexpr int TB_OFF = STAGES_OFF + MT_NS * STAGE;
   static constexpr int BYTES = TB_OFF + 2 * TB;
   static constexpr int SMEM = BYTES + 1024;                // slack to align the base
-  static constexpr int FC = R * MC / (32 * MT_TW);        // columns folded per fold-warp thread (one row)
+  // the fold: each of the 32*TW fold threads owns FC columns of FRW rows
+  static constexpr int FPT = R * MC / (32 * TW);           // (row, column) pairs per fold thread
+  static constexpr int FC = FPT < MC ? FPT : MC;           // columns per fold thread
+  static constexpr int FRW = FPT / FC;                     // rows per fold thread
+  static constexpr int TPG = 32 * TW / (MC / FC);          // fold threads per column group
 };
 
 struct MtPlan {
@@ -219,16 +229,17 @@ __global__ void __launch_bounds__(MT_TB_THREADS) mt_table_kernel(const __half* x
 }
 
 template <int BITS, bool FOLD, int U>
-__global__ void __launch_bounds__(MT_THREADS, 1)
+__global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
     gemm_mt_kernel(GemvArgs a, MtPlan P, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales) {
   using L = MtLayout<BITS, U>;
-  constexpr int R = L::R, MC = L::MC;
+  constexpr int R = L::R, MC = L::MC, CW = L::CW, UW = L::UW;
   constexpr int CPW = 32 / BITS, HALF = CPW / 2, WPB = 32 / CPW, NP = 16 / CPW;
   constexpr uint32_t MASK = (1u << BITS) - 1u;
   constexpr int CPI = BITS / 2;          // 16-byte chunks per item and row
   constexpr int IPB = 8 / CPI;           // items per 128-byte box
-  static_assert(MC == 4 && (L::FC == 4 || L::FC == 2 || L::FC == 1) && R * MC == 32 * MT_TW * L::FC,
+  static_assert(MC == 4 && (L::FC == 4 || L::FC == 2 || L::FC == 1) &&
+                    R * MC == 32 * L::TW * L::FC * L::FRW && L::TPG * L::FRW == R,
                 "tile shape");
 
   extern __shared__ unsigned char sm_raw[];
@@ -244,11 +255,11 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < MT_NS; ++s) {
       mbar_init(&B->full[s], 1);
-      mbar_init(&B->empty[s], MT_CW);
+      mbar_init(&B->empty[s], CW);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&B->bfull[b], MT_CW);
-      mbar_init(&B->bempty[b], MT_TW);
+      mbar_init(&B->bfull[b], CW);
+      mbar_init(&B->bempty[b], L::TW);
     }
     *abort_f = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ------------------------------------------------------------ copies --
-  if (warp == MT_CW + MT_TW) {
+  if (warp == CW + L::TW) {
     if (lane == 0) {
       const uint32_t tx = (uint32_t)(L::NBOX * L::BOX + (perrow ? 0 : R * 32) + MT_TBLK);
       int g = 0;
@@ -293,15 +304,18 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
   }
 
   // --------------------------------------------------------- fold warps --
-  if (warp >= MT_CW) {
-    // Thread tt owns FC columns of one row of the tile and adds each
-    // segment's block results in block order; after a tile's last segment it
-    // stores the tile.
-    const int tt = tid - MT_CT;   // 0 .. 32*MT_TW - 1
-    const int frow = tt % R, fc0 = (tt / R) * L::FC;
-    float acc[L::FC];
+  if (warp >= CW) {
+    // Thread tt owns FC columns of FRW rows of the tile (rows ri + TPG*k) and
+    // adds each segment's block results in block order; after a tile's last
+    // segment it stores the tile.
+    constexpr int FC = L::FC, FRW = L::FRW, TPG = L::TPG;
+    const int tt = tid - 32 * CW;   // 0 .. 32*L::TW - 1
+    const int ri = tt % TPG, fc0 = (tt / TPG) * FC;
+    float acc[FRW][FC];
 #pragma unroll
-    for (int c = 0; c < L::FC; ++c) acc[c] = 0.0f;
+    for (int k = 0; k < FRW; ++k)
+#pragma unroll
+      for (int c = 0; c < FC; ++c) acc[k][c] = 0.0f;
     int g = 0;
     for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
       const int r0 = (t / P.CC) * R, m0 = (t % P.CC) * MC;
@@ -309,47 +323,47 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
         const int bb = g & 1;
         const int items = min(MT_ITEMS, (a.K - s * MT_KS) / 64);
         if (!mbar_wait_fast(&B->bfull[bb], (g >> 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) return;
-        const float* tb = reinterpret_cast<const float*>(sm + L::TB_OFF + bb * L::TB) + frow * MC + fc0;
-        float v[MT_BLOCKS][L::FC];
 #pragma unroll
-        for (int bl = 0; bl < MT_BLOCKS; ++bl)
-          if (bl < 2 * items) {
-            if constexpr (L::FC == 4) {
-              const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
-              v[bl][0] = f.x;
-              v[bl][1] = f.y;
-              v[bl][2] = f.z;
-              v[bl][3] = f.w;
-            } else if constexpr (L::FC == 2) {
-              const float2 f = *reinterpret_cast<const float2*>(tb + bl * R * MC);
-              v[bl][0] = f.x;
-              v[bl][1] = f.y;
-            } else {
-              v[bl][0] = tb[bl * R * MC];
+        for (int k = 0; k < FRW; ++k) {
+          const float* tb = reinterpret_cast<const float*>(sm + L::TB_OFF + bb * L::TB) + (ri + TPG * k) * MC + fc0;
+#pragma unroll
+          for (int bl = 0; bl < MT_BLOCKS; ++bl)
+            if (bl < 2 * items) {
+              if constexpr (FC == 4) {
+                const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
+                acc[k][0] = __fadd_rn(acc[k][0], f.x);
+                acc[k][1] = __fadd_rn(acc[k][1], f.y);
+                acc[k][2] = __fadd_rn(acc[k][2], f.z);
+                acc[k][3] = __fadd_rn(acc[k][3], f.w);
+              } else if constexpr (FC == 2) {
+                const float2 f = *reinterpret_cast<const float2*>(tb + bl * R * MC);
+                acc[k][0] = __fadd_rn(acc[k][0], f.x);
+                acc[k][1] = __fadd_rn(acc[k][1], f.y);
+              } else {
+                acc[k][0] = __fadd_rn(acc[k][0], tb[bl * R * MC]);
+              }
             }
-          }
-#pragma unroll
-        for (int bl = 0; bl < MT_BLOCKS; ++bl)
-          if (bl < 2 * items)
-#pragma unroll
-            for (int c = 0; c < L::FC; ++c) acc[c] = __fadd_rn(acc[c], v[bl][c]);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&B->bempty[bb]);
         if (s == P.NSEG - 1) {
-          const int64_t n = (int64_t)r0 + frow;
 #pragma unroll
-          for (int c = 0; c < L::FC; ++c) {
-            const int col = m0 + fc0 + c;
-            if (n < a.N && col < a.M) {
-              float out = acc[c];
-              if (perrow) out = __fadd_rn(0.0f, __fmul_rn(out, __half2float(a.scales[n])));
-              const int64_t o = (int64_t)col * a.N + n;
-              if (a.y_f16)
-                reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(out);
-              else
-                reinterpret_cast<float*>(a.y)[o] = out;
+          for (int k = 0; k < FRW; ++k) {
+            const int64_t n = (int64_t)r0 + ri + TPG * k;
+#pragma unroll
+            for (int c = 0; c < FC; ++c) {
+              const int col = m0 + fc0 + c;
+              if (n < a.N && col < a.M) {
+                float out = acc[k][c];
+                if (perrow) out = __fadd_rn(0.0f, __fmul_rn(out, __half2float(a.scales[n])));
+                const int64_t o = (int64_t)col * a.N + n;
+                if (a.y_f16)
+                  reinterpret_cast<__half*>(a.y)[o] = __float2half_rn(out);
+                else
+                  reinterpret_cast<float*>(a.y)[o] = out;
+              }
+              acc[k][c] = 0.0f;
             }
-            acc[c] = 0.0f;
           }
         }
       }
@@ -367,20 +381,21 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
       if (ok) ok = mbar_wait_fast(&B->full[slot], (g / MT_NS) & 1, abort_f, ERR_MT_TIMEOUT, err);
       if (ok && g >= 2) ok = mbar_wait_fast(&B->bempty[b], ((g >> 1) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
 
-      // item `warp` of the segment for all R rows (lane: rows lane + 32u)
-      if (ok && warp < items) {
+      // item `warp / CWI` of the segment for rows half `warp % CWI` of the
+      // tile (lane: rows lane + 32 * (half * UW + u))
+      const int item = warp / L::CWI, rh = (warp % L::CWI) * UW;
+      if (ok && item < items) {
         const unsigned char* st = sm + L::STAGES_OFF + slot * L::STAGE;
-        const u64* tabi = reinterpret_cast<const u64*>(st + L::TBL_OFF) + (size_t)warp * MT_TITEM;
+        const u64* tabi = reinterpret_cast<const u64*>(st + L::TBL_OFF) + (size_t)item * MT_TITEM;
         const float* ysum = reinterpret_cast<const float*>(st + L::TBL_OFF + MT_TAB);
         float* tb = reinterpret_cast<float*>(sm + L::TB_OFF + b * L::TB);
-        const int item = warp;
         const unsigned char* cbox = st + (item / IPB) * L::BOX;
         const int ch0 = (item % IPB) * CPI;
-        u64 wp[U][BITS];   // the item's words as 64-bit pairs (2q, 2q + 1)
-        uint32_t scw[U];
+        u64 wp[UW][BITS];   // the item's words as 64-bit pairs (2q, 2q + 1)
+        uint32_t scw[UW];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int r = lane + 32 * u;
+        for (int u = 0; u < UW; ++u) {
+          const int r = lane + 32 * (rh + u);
 #pragma unroll
           for (int c = 0; c < CPI; ++c) {
             // 128-byte swizzle: chunk c of row r sits at chunk c ^ (r % 8)
@@ -394,16 +409,16 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
         if (FOLD) {
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {
-            u64 acc2[U][MC];
+            u64 acc2[UW][MC];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+            for (int u = 0; u < UW; ++u)
 #pragma unroll
               for (int mm = 0; mm < MC; ++mm) acc2[u][mm] = 0ull;
 #pragma unroll
             for (int p = 0; p < NP; ++p) {
-              u64 lo[U], hi[U];
+              u64 lo[UW], hi[UW];
 #pragma unroll
-              for (int u = 0; u < U; ++u) {
+              for (int u = 0; u < UW; ++u) {
                 lo[u] = wp[u][blk * NP + p];
                 hi[u] = lo[u] >> 16;
               }
@@ -411,16 +426,16 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
               for (int j = 0; j < CPW; ++j) {
                 const uint32_t m32 = MASK << (BITS * (j % HALF));
                 const u64 mm64 = ((u64)m32 << 32) | m32;
-                u64 v[U];
+                u64 v[UW];
 #pragma unroll
-                for (int u = 0; u < U; ++u) v[u] = ((j < HALF) ? lo[u] : hi[u]) & mm64;
+                for (int u = 0; u < UW; ++u) v[u] = ((j < HALF) ? lo[u] : hi[u]) & mm64;
                 const int tq = CPW * p + j;   // step 16*blk + tq
                 const u64* yk = tabi + (2 * blk + (tq >> 3)) * MT_OCT + (tq & 7) * MC;
 #pragma unroll
                 for (int mm = 0; mm < MC; mm += 2) {
                   const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
 #pragma unroll
-                  for (int u = 0; u < U; ++u) {
+                  for (int u = 0; u < UW; ++u) {
                     acc2[u][mm] = ffma2(y2.x, v[u], acc2[u][mm]);
                     acc2[u][mm + 1] = ffma2(y2.y, v[u], acc2[u][mm + 1]);
                   }
@@ -431,7 +446,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
             const float4 bS = *reinterpret_cast<const float4*>(ysum + bl * MC);
             const float bs[4] = {bS.x, bS.y, bS.z, bS.w};
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < UW; ++u) {
               const float sc = __half2float(__ushort_as_half((uint16_t)(blk ? (scw[u] >> 16) : (scw[u] & 0xFFFFu))));
               float o[MC];
 #pragma unroll
@@ -442,28 +457,28 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
                 if (!perrow) pb = __fmul_rn(pb, sc);
                 o[mm] = pb;
               }
-              *reinterpret_cast<float4*>(tb + (bl * R + lane + 32 * u) * MC) = make_float4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<float4*>(tb + (bl * R + lane + 32 * (rh + u)) * MC) = make_float4(o[0], o[1], o[2], o[3]);
             }
           }
         } else {
-          uint32_t w[U][2 * WPB];
+          uint32_t w[UW][2 * WPB];
 #pragma unroll
-          for (int u = 0; u < U; ++u)
+          for (int u = 0; u < UW; ++u)
 #pragma unroll
             for (int q = 0; q < BITS; ++q) {
               w[u][2 * q] = (uint32_t)wp[u][q];
               w[u][2 * q + 1] = (uint32_t)(wp[u][q] >> 32);
             }
-          u64 acc2[U][MC];
+          u64 acc2[UW][MC];
 #pragma unroll
-          for (int u = 0; u < U; ++u)
+          for (int u = 0; u < UW; ++u)
 #pragma unroll
             for (int mm = 0; mm < MC; ++mm) acc2[u][mm] = 0ull;
 #pragma unroll
           for (int wi = 0; wi < WPB; ++wi) {
-            uint32_t h0[U], h1[U];
+            uint32_t h0[UW], h1[UW];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < UW; ++u) {
               h0[u] = w[u][wi] >> 16;
               h1[u] = w[u][WPB + wi] >> 16;
             }
@@ -471,9 +486,9 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
             for (int j = 0; j < CPW; ++j) {
               const int o = BITS * (j % HALF);
               const float offf = pow2f(23) + (float)(1 << (BITS - 1 + o));
-              u64 v[U];
+              u64 v[UW];
 #pragma unroll
-              for (int u = 0; u < U; ++u) {
+              for (int u = 0; u < UW; ++u) {
                 const uint32_t wa = (j < HALF) ? w[u][wi] : h0[u];
                 const uint32_t wb = (j < HALF) ? w[u][WPB + wi] : h1[u];
                 v[u] = decode2(wa, wb, MASK << o, pk(offf, offf));
@@ -484,7 +499,7 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
               for (int mm = 0; mm < MC; mm += 2) {
                 const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
+                for (int u = 0; u < UW; ++u) {
                   acc2[u][mm] = ffma2(y2.x, v[u], acc2[u][mm]);
                   acc2[u][mm + 1] = ffma2(y2.y, v[u], acc2[u][mm + 1]);
                 }
@@ -492,10 +507,10 @@ __global__ void __launch_bounds__(MT_THREADS, 1)
             }
           }
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
+          for (int u = 0; u < UW; ++u) {
             const float s_lo = __half2float(__ushort_as_half((uint16_t)(scw[u] & 0xFFFFu)));
             const float s_hi = __half2float(__ushort_as_half((uint16_t)(scw[u] >> 16)));
-            const int r = lane + 32 * u;
+            const int r = lane + 32 * (rh + u);
             float o0[MC], o1[MC];
 #pragma unroll
             for (int mm = 0; mm < MC; ++mm) {
@@ -618,7 +633,7 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   if ((size_t)L::SMEM > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
   if (!a.ws || a.ws_bytes < mt_table_bytes(a.M, a.K)) return QMV_ERR_WORKSPACE;
   int occ = 0;
-  cudaError_t e = prep_kernel(kern, cache, MT_THREADS, L::SMEM, &occ);
+  cudaError_t e = prep_kernel(kern, cache, L::THREADS, L::SMEM, &occ);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   if (occ < 1) return QMV_ERR_UNSUPPORTED;
   // codes as UINT64 [N][row_bytes/8] (box 16 x R, 128-byte swizzle), scales
@@ -642,7 +657,7 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
                 reinterpret_cast<unsigned char*>(a.ws));
   if (e == cudaSuccess) {
     const int grid = P.tiles < d.sms ? P.tiles : d.sms;
-    e = mt_launch(kern, dim3(grid), MT_THREADS, L::SMEM, s, a, P, tmc, tms);
+    e = mt_launch(kern, dim3(grid), L::THREADS, L::SMEM, s, a, P, tmc, tms);
   }
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
   return QMV_OK;
