@@ -378,12 +378,15 @@ __device__ __forceinline__ void build_table(const GemvArgs& a, float* y2f, float
     // registers when every thread has at most one block; its gamma is
     // prefetched into L1 for pass 2)
     const bool one = NB <= nt;
-    uint32_t h0[16];
+    uint32_t h0[16], g0[16];
     for (int b = tt; b < NB; b += nt) {
       uint32_t x[16], r[16];
       load_blk(a.x + 32 * b, x);
       load_blk(a.r + 32 * b, r);
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(a.gamma + 32 * b));
+      if (one)
+        load_blk(a.gamma + 32 * b, g0);
+      else
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(a.gamma + 32 * b));
       bsum[b] = residual_blk(x, r, h0);
       if (h_out) {
 #pragma unroll
@@ -414,8 +417,8 @@ __device__ __forceinline__ void build_table(const GemvArgs& a, float* y2f, float
         load_blk(a.r + 32 * b, r);
         residual_blk(x, r, h0);
       }
-      uint32_t g0[16], y[16];
-      load_blk(a.gamma + 32 * b, g0);
+      uint32_t y[16];
+      if (!one) load_blk(a.gamma + 32 * b, g0);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const __half2 hh = u32_as_h2(h0[e]), gg = u32_as_h2(g0[e]);
