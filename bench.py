@@ -377,6 +377,55 @@ def run_layer(qmv, lay, b, stream):
             qmv.qmv_gemv(p, x, y=y, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
 
 
+def wall_us(fn, reps):
+    """Median wall-clock microseconds of fn() between two device synchronises
+    (host issue included: the eager, uncaptured use)."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        fn()
+        torch.cuda.synchronize()
+        ts.append(time.perf_counter() - t0)
+    return float(np.median(ts)) * 1e6
+
+
+def chain_eager(qmv, dev, stream, layers, b, ch, reps):
+    """Where the chain wins: calls issued eagerly from the host (no graph),
+    for the dependent c2 layers and for 64 independent fused RMSNorm + int2
+    1024 x 1024 matvecs with their own outputs (no grid barrier in the
+    chain).  Microseconds per layer / per matvec, wall clock."""
+    import torch
+    L = len(layers)
+    sep = wall_us(lambda: [run_layer(qmv, lay, b, stream) for lay in layers], reps) / L
+    chn = wall_us(lambda: ch.run(stream), reps) / L
+    n = 64
+    packs = [make_pack(qmv, dev, f"ce.{i}", 1024, 1024, 2, 32) for i in range(n)]
+    x = dev_f16(dev, "ce.x", (1, 1024))
+    r = dev_f16(dev, "ce.r", (1, 1024))
+    g = dev_f16(dev, "ce.g", (1024,), mean=1.0, std=0.1)
+    ys = [torch.empty(1, 1024, dtype=torch.float16, device=dev) for _ in range(n)]
+    ch2 = qmv.Chain(n)
+    for p, y in zip(packs, ys):
+        ch2.add_fused_rmsnorm_gemv(p, x, r, g, EPS, None, y, y_dtype=qmv.QMV_F16)
+
+    def each():
+        for p, y in zip(packs, ys):
+            qmv.qmv_fused_rmsnorm_gemv(p, x, r, g, EPS, y=y, y_dtype=qmv.QMV_F16, mode=qmv.QMV_FAST, stream=stream)
+    each()
+    ch2.run(stream)
+    ind_sep = wall_us(each, reps) / n
+    ind_chn = wall_us(lambda: ch2.run(stream), reps) / n
+    barriers = ch2.info()["barriers"]
+    ch2.close()
+    return {"layers_us_per_layer": {"separate": round(sep, 2), "chain": round(chn, 2)},
+            "independent_us_per_matvec": {"separate": round(ind_sep, 2), "chain": round(ind_chn, 2),
+                                          "chain_grid_barriers": barriers},
+            "workload": "eager host-issued calls, no graph, wall clock between synchronises: the 32 c2 "
+                        "layers, and 64 independent fused RMSNorm + int2 1024x1024 matvecs"}
+
+
 def chain_layers(qmv, layers, b):
     """The same layers as one persistent chain."""
     ch = qmv.Chain(4 * len(layers))
@@ -651,6 +700,7 @@ def side_blocks(qmv, dev, stream, args, world):
                                      lambda m: {"us_per_layer": round(m * 1e3 / L, 3)}),
                                 workload="the c2 layers as one persistent cooperative launch (qmv_chain_run)",
                                 grid_barriers=ch.info()["barriers"])
+            out["chain_eager"] = chain_eager(qmv, dev, stream, layers, b, ch, rounds)
             ch.close()
         del items, layers, b
         torch.cuda.empty_cache()
