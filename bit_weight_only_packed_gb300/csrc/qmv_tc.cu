@@ -18,20 +18,20 @@
 // on CTA timing).  A pipeline stage carries KSUB 64-code slabs (4 for MT =
 // 64, 2 for MT = 128): one hand-off between the roles per 64*KSUB codes.
 // Roles:
-//   warp 8 (one thread): TMA of the packed codes and scales of the tile, 4
+//   warp 16 (one thread): TMA of the packed codes and scales of the tile, 4
 //     K-slabs (256 codes) at a time, into a ring of raw stages.
-//   warp 10 (one thread): TMA of the activation sub-tiles of each stage's
+//   warp 18 (one thread): TMA of the activation sub-tiles of each stage's
 //     slabs straight into the MMA operand stage, with a 128-byte-swizzle
 //     tensor map (the K-major layout the MMA reads).
-//   warps 0..7: decode.  Threads r and 128 + r turn the two 32-code blocks of
-//     row r of each slab into fp16 weights w = v*s (half2 magic decode,
-//     re-paired into natural k order) and write them into the stage's
-//     128-byte-swizzled K-major A sub-tiles.  At the end they are the
-//     epilogue: tcgen05.ld of their TMEM lane quarter, half of the tile's
-//     columns each.
-//   warp 9 (one thread): allocates the accumulator in tensor memory and issues
-//     tcgen05.mma (M=128, N=MT, K=16; four per slab), releasing each stage with
-//     tcgen05.commit on its mbarrier.
+//   warps 0..15: decode.  Thread t takes row t % 128, 32-code block
+//     (t / 128) % 2 and every second slab of the stage from t / 256: it turns
+//     the block into fp16 weights w = v*s (half2 magic decode, re-paired into
+//     natural k order) and writes them into the stage's 128-byte-swizzled
+//     K-major A sub-tile.  At the end they are the epilogue: tcgen05.ld of
+//     their TMEM lane quarter, a quarter of the tile's columns each.
+//   warp 17 (one thread): allocates the accumulator in tensor memory and
+//     issues tcgen05.mma (M=128, N=MT, K=16; four per slab), releasing each
+//     stage with tcgen05.commit on its mbarrier.
 // Every wait is bounded; a wait that runs out records an error code in this
 // file's device error word and the CTA winds down.
 #include <cuda.h>
@@ -48,7 +48,8 @@ namespace {
 constexpr uint32_t TC_SPIN = 1u << 22;
 constexpr int ERR_TC_TIMEOUT = 16;
 constexpr int RS = 4;          // K slabs per raw stage (256 codes)
-constexpr int NDEC = 8;        // decode (and epilogue) warps
+constexpr int NDEC = 16;       // decode (and epilogue) warps
+constexpr int NSET = NDEC * 32 / 256;   // slabs of a stage decoded side by side
 constexpr int W_RAW = NDEC, W_MMA = NDEC + 1, W_B = NDEC + 2;   // role warps
 constexpr int TC_THREADS = 32 * (NDEC + 3);
 constexpr int RAW_CODES = 128 * RS * 16;   // bytes of codes per raw stage
@@ -320,9 +321,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           : "memory");
     }
   } else {
-    // ------------------------------- decode (NDEC warps, 2 per weight row) --
-    const int row = threadIdx.x & 127;      // weight row of the tile
-    const int blk = threadIdx.x >> 7;       // which 32-code block of the slab
+    // ---------------------------- decode (NDEC warps: row, block and slab) --
+    static_assert(KSUB % NSET == 0, "a stage's slabs split evenly over the decode sets");
+    const int row = threadIdx.x & 127;        // weight row of the tile
+    const int blk = (threadIdx.x >> 7) & 1;   // which 32-code block of the slab
+    const int uset = threadIdx.x >> 8;        // which of the stage's slabs (every NSET-th)
+    int waited = -1;                          // the last raw stage this thread waited for
     const uint32_t prs = a.perrow && n0 + row < a.N
                              ? (uint32_t)__half_as_ushort(__ldg(a.scales + n0 + row))
                              : 0u;
@@ -331,12 +335,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f)) break;
       bool ok = true;
 #pragma unroll 1
-      for (int u = 0; u < KSUB; ++u) {
+      for (int u = uset; u < KSUB; u += NSET) {
         const int sl = i * KSUB + u;   // slab
         const int j = sl / RS, rr = j % NRAW, sub = sl % RS;
-        if (sub == 0 && !tc_wait(&raw_full[rr], (j / NRAW) & 1, abort_f)) {
-          ok = false;
-          break;
+        if (j != waited) {
+          if (!tc_wait(&raw_full[rr], (j / NRAW) & 1, abort_f)) {
+            ok = false;
+            break;
+          }
+          waited = j;
         }
         const unsigned char* rb = rawbuf + rr * RAW_BYTES;
         const uint2 cw = *reinterpret_cast<const uint2*>(rb + row * (RS * 16) + sub * 16 + blk * 8);
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int q4 = warp & 3;
       const int r = 32 * q4 + lane;
       const int64_t n = (int64_t)n0 + r;
-      const int cbeg = (warp >> 2) * (MT / 2), cend = cbeg + MT / 2;
+      const int cbeg = (warp >> 2) * (MT / (NDEC / 4)), cend = cbeg + MT / (NDEC / 4);
 #pragma unroll 1
       for (int c0 = cbeg; c0 < cend; c0 += 16) {
         uint32_t v[16];
