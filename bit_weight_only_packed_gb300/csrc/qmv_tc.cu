@@ -557,7 +557,7 @@ size_t tc_workspace_bytes(int M, int N, int K, bool y_f16) {
   if (M < 1 || K % 256 != 0) return 0;
   const int m = M < 128 ? M : 128;
   const int tiles = (N + 127) / 128;
-  const TcSplit sp = tc_split(tiles, K, y_f16, m <= 64 ? TC_RS_M64 : TC_RS_M128);
+  const TcSplit sp = tc_split(tiles, K, y_f16, RS);
   if (sp.split <= 1 || sp.atomics) return 0;
   return (size_t)sp.split * (size_t)m * (size_t)N * sizeof(float);
 }
