@@ -118,7 +118,7 @@ static size_t workspace_need(const qmv_pack* p, int M, int y_dtype, int mode, in
   if (M < 2 || M > 4096 || p->K % 256 != 0) return 0;
   if (!fused && M > 32 && mode == QMV_FAST && p->bits == 2)
     return round256(qmv::tc_workspace_bytes(M, p->N, p->K, y_dtype == QMV_F16));
-  return qmv::mt_workspace_bytes(M, p->K, fused != 0);
+  return qmv::mt_workspace_bytes(M, p->N, p->K, p->bits, fused != 0);
 }
 
 static int check_workspace(const qmv_pack* p, int M, int y_dtype, int mode, int fused, void* ws,

@@ -81,10 +81,10 @@ int launch_tc_gemm(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err
 // partial tiles; 0 when it needs none).
 size_t tc_workspace_bytes(int M, int N, int K, bool y_f16);
 // Scratch bytes launch_mtile needs: the segment tables of the M columns
-// (8960 bytes per 4 columns and 512 codes), after the fused prologue's
-// normalised activations (M x K fp16, 256-byte rounded); 0 where it does not
-// run (M < 2, K not a multiple of 256).
-size_t mt_workspace_bytes(int M, int K, bool fused);
+// (per 512 codes, 8960 bytes per 4 columns or 17408 per 8, as the tile shape
+// chosen for N, M, K and bits has them), with or without the fused prologue;
+// 0 where it does not run (M < 2, K not a multiple of 256).
+size_t mt_workspace_bytes(int M, int N, int K, int bits, bool fused);
 // Programmatic dependent launch of the M = 1 kernels (off by default).
 bool pdl_enabled();
 void set_pdl(bool on);

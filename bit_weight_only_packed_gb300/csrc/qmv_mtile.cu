@@ -12,15 +12,18 @@
 //   * a segment's activation table depends on the activations only, not on
 //     the weight rows, so a small kernel first builds every (column chunk,
 //     512-code segment) table once per call, with its block sums, into the
-//     caller's workspace (8960 bytes each; a few hundred KB that stay in L2);
-//   * a tile is R = 32*U weight rows x MC = 4 token columns over the whole K;
-//     a persistent CTA (one per SM) walks its tiles, each in segments of 512
-//     codes;
+//     caller's workspace (8960 bytes each for 4 columns, 17408 for 8; a few
+//     hundred KB that stay in L2);
+//   * a tile is R = 32*U weight rows x MC = 4 or 8 token columns over the
+//     whole K (a cost model picks U and MC; with 8 columns each code's mask
+//     serves twice the paired FMAs, and two ring stages fit); a persistent
+//     CTA (one per SM) walks its tiles, each in segments of 512 codes;
 //   * the copy warp brings, per segment, the tile's packed codes (one or more
 //     128-byte-swizzled boxes of R rows x 128 bytes), its group-32 scales and
 //     the segment's prebuilt table into a ring of stages;
 //   * each 64-code item of the segment goes to one compute warp (two for
-//     128-row tiles, each taking half the rows): lane l holds rows l + 32u,
+//     128-row, 4-column tiles, each taking half the rows): lane l holds rows
+//     l + 32u,
 //     decodes each code once and runs the paired-FMA chains of the MC columns
 //     (one 16-byte shared-memory broadcast serves two columns of its rows);
 //     the block results go to one of two fold buffers (one 16-byte store per
@@ -29,12 +32,12 @@
 //     behind, add the block results in block order: each thread owns some
 //     rows' (row, column) accumulators, and stores them after the tile's last
 //     segment.
-// With the fused residual-add + RMSNorm prologue, a small kernel first forms
-// each column's h = fp16(x + r) (stored to h_out), its sum of squares in the
-// oracle's order and the normalised fp16 activations y = fp16((h*inv)*gamma)
-// into the workspace, once per column instead of once per row tile; the
-// tables are then built from that y, which is what the fused definition
-// feeds the matvec.
+// With the fused residual-add + RMSNorm prologue, the table kernel forms
+// each of its columns' h = fp16(x + r), the sum of squares in the oracle's
+// order and inv, then the normalised fp16 activations y = fp16((h*inv)*gamma)
+// of its segment, from which it builds the table, and stores that segment of
+// h to h_out: once per column and segment instead of once per row tile, and
+// y is what the fused definition feeds the matvec.
 // The roles meet only on mbarriers (stage full/empty, fold buffer
 // full/empty), so a slow warp delays the others by its lag, not by a
 // CTA-wide barrier per segment.  Every wait is bounded; a wait that runs out
@@ -53,37 +56,42 @@ namespace {
 
 using namespace pipe;
 
-constexpr int MT_NS = 3;                     // ring stages
+constexpr int MT_NSMAX = 3;                  // ring stages (at most)
 constexpr int MT_KS = 512;                   // codes per segment
 constexpr int MT_ITEMS = MT_KS / 64;         // 64-code items per segment (one per compute warp)
 constexpr int MT_BLOCKS = MT_KS / 32;        // 32-code blocks per segment
-constexpr int MT_MC = 4;                     // token columns per tile
 constexpr int MT_HDR = 1024;                 // barriers, flags
 constexpr int ERR_MT_TIMEOUT = 32;
 
-// One segment's table record, as the table kernel writes it to the workspace
-// and the copy warp brings it into a stage: per item 4 octets of 8 steps, a
-// step MC fp32 pairs (the columns side by side), each octet padded by 16
-// bytes, then the block sums [block][MC] (fast mode).
-constexpr int MT_OCT = 8 * MT_MC + 2;                    // u64 per octet
-constexpr int MT_TITEM = 4 * MT_OCT;                     // u64 per item
-constexpr int MT_TAB = MT_ITEMS * MT_TITEM * 8;          // table bytes
-constexpr int MT_YSUM = MT_BLOCKS * MT_MC * 4;           // block-sum bytes
-constexpr int MT_TBLK = MT_TAB + MT_YSUM;                // 8960 bytes a record
-constexpr int MT_TB_THREADS = 128;                       // threads of the table kernel
-static_assert(MT_TBLK % 256 == 0, "records start 256-byte aligned in the workspace; bulk copies move 16-byte multiples");
+// One segment's table record for MC token columns, as the table kernel
+// writes it to the workspace and the copy warp brings it into a stage: per
+// item 4 octets of 8 steps, a step MC fp32 pairs (the columns side by side),
+// each octet padded by 16 bytes, then the block sums [block][MC] (fast mode).
+template <int MC>
+struct MtRec {
+  static constexpr int OCT = 8 * MC + 2;                 // u64 per octet
+  static constexpr int TITEM = 4 * OCT;                  // u64 per item
+  static constexpr int TAB = MT_ITEMS * TITEM * 8;       // table bytes
+  static constexpr int YSUM = MT_BLOCKS * MC * 4;        // block-sum bytes
+  static constexpr int TBLK = TAB + YSUM;                // 8960 (MC 4) or 17408 (MC 8) bytes
+  static_assert(TBLK % 256 == 0, "records start 256-byte aligned in the workspace; bulk copies move 16-byte multiples");
+};
+constexpr int MT_TB_THREADS = 32;                        // threads of the table kernel per column
 
 // Shared-memory layout of one kernel variant (offsets from a 1024-byte
 // aligned base; the copies with 128-byte swizzle need 1024-byte aligned
 // boxes).
-template <int BITS, int U>
+template <int BITS, int U, int MC_>
 struct MtLayout {
-  static constexpr int MC = MT_MC;
+  static constexpr int MC = MC_;                           // token columns per tile (4 or 8)
   static constexpr int R = 32 * U;                         // rows per tile
-  // 128-row tiles split each item's rows over two compute warps (four per
-  // scheduler: more warps to hide the paired FMAs' and loads' latencies);
-  // smaller tiles keep one warp per item (two rows or one a lane)
-  static constexpr int CWI = (U >= 4) ? 2 : 1;             // compute warps per item (row halves)
+  static constexpr int NS = (MC == 8) ? 2 : 3;             // ring stages (what fits)
+  static constexpr int TBLK = MtRec<MC>::TBLK;
+  // 128-row tiles of 4 columns split each item's rows over two compute warps
+  // (four per scheduler: more warps to hide the paired FMAs' and loads'
+  // latencies); other tiles keep one warp per item (their FMA chains are
+  // long enough, or their rows are few)
+  static constexpr int CWI = (U >= 4 && MC == 4) ? 2 : 1;  // compute warps per item (row halves)
   static constexpr int UW = U / CWI;                       // rows per lane of a compute warp
   static constexpr int CW = MT_ITEMS * CWI;                // compute warps
   static constexpr int TW = (CWI == 2) ? 2 : 4;            // fold warps (within the register file)
@@ -92,10 +100,10 @@ struct MtLayout {
   static constexpr int BOX = R * 128;
   static constexpr int SC_OFF = NBOX * BOX;                // scales: [R][16] fp16
   static constexpr int TBL_OFF = SC_OFF + R * 32;          // the segment's table record
-  static constexpr int STAGE = (TBL_OFF + MT_TBLK + 1023) / 1024 * 1024;
+  static constexpr int STAGE = (TBL_OFF + TBLK + 1023) / 1024 * 1024;
   static constexpr int STAGES_OFF = MT_HDR;
   static constexpr int TB = MT_BLOCKS * R * MC * 4;        // one fold buffer: [block][R][MC]
-  static constexpr int TB_OFF = STAGES_OFF + MT_NS * STAGE;
+  static constexpr int TB_OFF = STAGES_OFF + NS * STAGE;
   static constexpr int BYTES = TB_OFF + 2 * TB;
   static constexpr int SMEM = BYTES + 1024;                // slack to align the base
   // the fold: each of the 32*TW fold threads owns FC columns of FRW rows
@@ -114,7 +122,7 @@ struct MtPlan {
 
 // mbarriers in the header: stage full/empty, fold buffer full/empty
 struct MtBars {
-  uint64_t full[MT_NS], empty[MT_NS];
+  uint64_t full[MT_NSMAX], empty[MT_NSMAX];
   uint64_t bfull[2], bempty[2];
 };
 
@@ -135,21 +143,72 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // word 2p, of word 2p + 1) * 2^(FOLD_E - o(j)).  The block sums add the
 // block's activations in the order of the dots (even and odd words serially,
 // then together) and scale by 2^(b-1).
-template <int BITS, bool FOLD>
-__global__ void __launch_bounds__(MT_TB_THREADS) mt_table_kernel(const __half* x, int M, int K, int NSEG,
-                                                                 unsigned char* tabs) {
-  constexpr int MC = MT_MC, CPW = 32 / BITS, HALF = CPW / 2;
+template <int BITS, bool FOLD, int MC, bool FUSED>
+__global__ void __launch_bounds__(MT_TB_THREADS * MC)
+    mt_table_kernel(const __half* x, const __half* r, const __half* gamma, float eps, __half* h_out, int M, int K,
+                    int NSEG, unsigned char* tabs) {
+  using RC = MtRec<MC>;
+  constexpr int CPW = 32 / BITS, HALF = CPW / 2;
   __shared__ __align__(16) __half xs[2 * MC * 256];       // [half][m][256]
-  __shared__ __align__(16) u64 rec[MT_TBLK / 8];
+  __shared__ __align__(16) u64 rec[RC::TBLK / 8];
+  extern __shared__ float nrm[];                           // fused: [MC][K/32] block sums, then [MC] inv
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // x comes from the previous kernel, and it may still read the workspace
+  // x (and r) come from the previous kernel, and it may still read the
+  // workspace or h_out
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int s = blockIdx.x, m0 = blockIdx.y * MC, tt = threadIdx.x;
-  for (int i = tt; i < MT_TBLK / 8; i += MT_TB_THREADS) rec[i] = 0ull;
-  for (int i = tt; i < MC * MT_KS / 8; i += MT_TB_THREADS) {
+  for (int i = tt; i < RC::TBLK / 8; i += MT_TB_THREADS * MC) rec[i] = 0ull;
+  if (FUSED) {
+    // the residual add + RMSNorm of the fused definition, per column: warp
+    // w takes column m0 + w, its lanes the block sums of squares of h =
+    // fp16(x + r) (each serial over its 32 elements), lane 0 their serial
+    // sum and inv = 1/sqrt(ss/K + eps) -- the same steps and order as the
+    // M = 1 prologue, so the normalised activations are the same values
+    const int NB = K / 32, w = tt >> 5, lane = tt & 31;
+    float* bsum = nrm + w * NB;
+    float* inv = nrm + MC * NB;
+    if (m0 + w < M) {
+      const __half* xc = x + (int64_t)(m0 + w) * K;
+      const __half* rc = r + (int64_t)(m0 + w) * K;
+      for (int b = lane; b < NB; b += 32) bsum[b] = block_sumsq(xc, rc, 32 * b, nullptr);
+      __syncwarp();
+      if (lane == 0) {
+        float ss = 0.0f;
+        for (int b = 0; b < NB; ++b) ss = __fadd_rn(ss, bsum[b]);
+        inv[w] = rms_inv(ss, K, eps);
+      }
+    }
+    __syncthreads();
+  }
+  for (int i = tt; i < MC * MT_KS / 8; i += MT_TB_THREADS * MC) {
     const int m = i / (MT_KS / 8), k = 8 * (i % (MT_KS / 8)), kk = s * MT_KS + k;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (m0 + m < M && kk < K) v = *reinterpret_cast<const uint4*>(x + (int64_t)(m0 + m) * K + kk);
+    if (m0 + m < M && kk < K) {
+      const int64_t o = (int64_t)(m0 + m) * K + kk;
+      if (FUSED) {
+        // y = fp16((h * inv) * gamma), and h itself to h_out (this segment
+        // of this chunk's columns)
+        const uint4 xv = ldg16(reinterpret_cast<const uint4*>(x + o));
+        const uint4 rv = ldg16(reinterpret_cast<const uint4*>(r + o));
+        const uint4 gv = ldg16(reinterpret_cast<const uint4*>(gamma + kk));
+        const float iv = nrm[MC * (K / 32) + m];
+        uint16_t hh[8], yy[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const __half h = add_h(h_of(xv, e), h_of(rv, e));
+          hh[e] = __half_as_ushort(h);
+          yy[e] = __half_as_ushort(norm_h(h, iv, h_of(gv, e)));
+        }
+        memcpy(&v, yy, 16);
+        if (h_out) {
+          uint4 hv;
+          memcpy(&hv, hh, 16);
+          *reinterpret_cast<uint4*>(h_out + o) = hv;
+        }
+      } else {
+        v = *reinterpret_cast<const uint4*>(x + o);
+      }
+    }
     *reinterpret_cast<uint4*>(xs + (k >> 8) * (MC * 256) + m * 256 + (k & 255)) = v;
   }
   __syncthreads();
@@ -167,7 +226,7 @@ __global__ void __launch_bounds__(MT_TB_THREADS) mt_table_kernel(const __half* x
   };
   // task (m, item, quarter): 8 steps of one item for one column, from two
   // 16-byte chunks of activations
-  for (int task = tt; task < MC * items * 4; task += MT_TB_THREADS) {
+  for (int task = tt; task < MC * items * 4; task += MT_TB_THREADS * MC) {
     const int m = task / (items * 4), iq = task % (items * 4), item = iq >> 2, q = iq & 3;
     const int hq = q & 1, blk = q >> 1;
     float A[8], Bv[8];
@@ -179,7 +238,7 @@ __global__ void __launch_bounds__(MT_TB_THREADS) mt_table_kernel(const __half* x
       chunk(m, a0, A);
       chunk(m, a0 + (BITS == 2 ? 16 : 8), Bv);
     }
-    u64* dst = rec + (size_t)item * MT_TITEM + q * MT_OCT + m;
+    u64* dst = rec + (size_t)item * RC::TITEM + q * RC::OCT + m;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       float v0, v1, sc;
@@ -202,8 +261,8 @@ __global__ void __launch_bounds__(MT_TB_THREADS) mt_table_kernel(const __half* x
     }
   }
   if (FOLD) {
-    float* ysum = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(rec) + MT_TAB);
-    for (int task = tt; task < MC * 2 * items; task += MT_TB_THREADS) {
+    float* ysum = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(rec) + RC::TAB);
+    for (int task = tt; task < MC * 2 * items; task += MT_TB_THREADS * MC) {
       const int m = task / (2 * items), bl = task % (2 * items);
       float y[32];
 #pragma unroll
@@ -224,21 +283,22 @@ __global__ void __launch_bounds__(MT_TB_THREADS) mt_table_kernel(const __half* x
     }
   }
   __syncthreads();
-  uint4* out = reinterpret_cast<uint4*>(tabs + ((size_t)blockIdx.y * NSEG + s) * MT_TBLK);
-  for (int i = tt; i < MT_TBLK / 16; i += MT_TB_THREADS) out[i] = reinterpret_cast<const uint4*>(rec)[i];
+  uint4* out = reinterpret_cast<uint4*>(tabs + ((size_t)blockIdx.y * NSEG + s) * RC::TBLK);
+  for (int i = tt; i < RC::TBLK / 16; i += MT_TB_THREADS * MC) out[i] = reinterpret_cast<const uint4*>(rec)[i];
 }
 
-template <int BITS, bool FOLD, int U>
-__global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
+template <int BITS, bool FOLD, int U, int MC_>
+__global__ void __launch_bounds__(MtLayout<BITS, U, MC_>::THREADS, 1)
     gemm_mt_kernel(GemvArgs a, MtPlan P, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales) {
-  using L = MtLayout<BITS, U>;
-  constexpr int R = L::R, MC = L::MC, CW = L::CW, UW = L::UW;
+  using L = MtLayout<BITS, U, MC_>;
+  using RC = MtRec<MC_>;
+  constexpr int R = L::R, MC = L::MC, CW = L::CW, UW = L::UW, NS = L::NS;
   constexpr int CPW = 32 / BITS, HALF = CPW / 2, WPB = 32 / CPW, NP = 16 / CPW;
   constexpr uint32_t MASK = (1u << BITS) - 1u;
   constexpr int CPI = BITS / 2;          // 16-byte chunks per item and row
   constexpr int IPB = 8 / CPI;           // items per 128-byte box
-  static_assert(MC == 4 && (L::FC == 4 || L::FC == 2 || L::FC == 1) &&
+  static_assert((MC == 4 || MC == 8) && (L::FC == 8 || L::FC == 4 || L::FC == 2 || L::FC == 1) &&
                     R * MC == 32 * L::TW * L::FC * L::FRW && L::TPG * L::FRW == R,
                 "tile shape");
 
@@ -253,7 +313,7 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
 
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
-    for (int s = 0; s < MT_NS; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&B->full[s], 1);
       mbar_init(&B->empty[s], CW);
     }
@@ -272,16 +332,16 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
   // ------------------------------------------------------------ copies --
   if (warp == CW + L::TW) {
     if (lane == 0) {
-      const uint32_t tx = (uint32_t)(L::NBOX * L::BOX + (perrow ? 0 : R * 32) + MT_TBLK);
+      const uint32_t tx = (uint32_t)(L::NBOX * L::BOX + (perrow ? 0 : R * 32) + RC::TBLK);
       int g = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < P.tiles && !stop; t += gridDim.x) {
         const int r0 = (t / P.CC) * R, c = t % P.CC;
-        const unsigned char* trec = P.tabs + (size_t)c * P.NSEG * MT_TBLK;
+        const unsigned char* trec = P.tabs + (size_t)c * P.NSEG * RC::TBLK;
         for (int s = 0; s < P.NSEG; ++s, ++g) {
-          const int slot = g % MT_NS;
-          if (g >= MT_NS &&
-              !mbar_wait_fast(&B->empty[slot], ((g / MT_NS) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) {
+          const int slot = g % NS;
+          if (g >= NS &&
+              !mbar_wait_fast(&B->empty[slot], ((g / NS) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err)) {
             stop = true;
             break;
           }
@@ -294,11 +354,11 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
 #pragma unroll
           for (int b = 0; b < L::NBOX; ++b) tma_2d(st + b * L::BOX, &tm_codes, s * 8 * BITS + 16 * b, r0, &B->full[slot]);
           if (!perrow) tma_2d(st + L::SC_OFF, &tm_scales, s * 16, r0, &B->full[slot]);
-          bulk_g2s(st + L::TBL_OFF, trec + (size_t)s * MT_TBLK, MT_TBLK, &B->full[slot]);
+          bulk_g2s(st + L::TBL_OFF, trec + (size_t)s * RC::TBLK, RC::TBLK, &B->full[slot]);
         }
       }
       // let every copy issued land before the CTA can exit
-      for (int j = (g > MT_NS ? g - MT_NS : 0); j < g; ++j) mbar_drain(&B->full[j % MT_NS], (j / MT_NS) & 1, err);
+      for (int j = (g > NS ? g - NS : 0); j < g; ++j) mbar_drain(&B->full[j % NS], (j / NS) & 1, err);
     }
     return;
   }
@@ -329,7 +389,18 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
 #pragma unroll
           for (int bl = 0; bl < MT_BLOCKS; ++bl)
             if (bl < 2 * items) {
-              if constexpr (FC == 4) {
+              if constexpr (FC == 8) {
+                const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
+                const float4 f2 = *reinterpret_cast<const float4*>(tb + bl * R * MC + 4);
+                acc[k][0] = __fadd_rn(acc[k][0], f.x);
+                acc[k][1] = __fadd_rn(acc[k][1], f.y);
+                acc[k][2] = __fadd_rn(acc[k][2], f.z);
+                acc[k][3] = __fadd_rn(acc[k][3], f.w);
+                acc[k][4] = __fadd_rn(acc[k][4], f2.x);
+                acc[k][5] = __fadd_rn(acc[k][5], f2.y);
+                acc[k][6] = __fadd_rn(acc[k][6], f2.z);
+                acc[k][7] = __fadd_rn(acc[k][7], f2.w);
+              } else if constexpr (FC == 4) {
                 const float4 f = *reinterpret_cast<const float4*>(tb + bl * R * MC);
                 acc[k][0] = __fadd_rn(acc[k][0], f.x);
                 acc[k][1] = __fadd_rn(acc[k][1], f.y);
@@ -376,9 +447,9 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
   int g = 0;
   for (int t = blockIdx.x; t < P.tiles; t += gridDim.x) {
     for (int s = 0; s < P.NSEG; ++s, ++g) {
-      const int slot = g % MT_NS, b = g & 1;
+      const int slot = g % NS, b = g & 1;
       const int items = min(MT_ITEMS, (a.K - s * MT_KS) / 64);
-      if (ok) ok = mbar_wait_fast(&B->full[slot], (g / MT_NS) & 1, abort_f, ERR_MT_TIMEOUT, err);
+      if (ok) ok = mbar_wait_fast(&B->full[slot], (g / NS) & 1, abort_f, ERR_MT_TIMEOUT, err);
       if (ok && g >= 2) ok = mbar_wait_fast(&B->bempty[b], ((g >> 1) - 1) & 1, abort_f, ERR_MT_TIMEOUT, err);
 
       // item `warp / CWI` of the segment for rows half `warp % CWI` of the
@@ -386,8 +457,8 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
       const int item = warp / L::CWI, rh = (warp % L::CWI) * UW;
       if (ok && item < items) {
         const unsigned char* st = sm + L::STAGES_OFF + slot * L::STAGE;
-        const u64* tabi = reinterpret_cast<const u64*>(st + L::TBL_OFF) + (size_t)item * MT_TITEM;
-        const float* ysum = reinterpret_cast<const float*>(st + L::TBL_OFF + MT_TAB);
+        const u64* tabi = reinterpret_cast<const u64*>(st + L::TBL_OFF) + (size_t)item * RC::TITEM;
+        const float* ysum = reinterpret_cast<const float*>(st + L::TBL_OFF + RC::TAB);
         float* tb = reinterpret_cast<float*>(sm + L::TB_OFF + b * L::TB);
         const unsigned char* cbox = st + (item / IPB) * L::BOX;
         const int ch0 = (item % IPB) * CPI;
@@ -430,7 +501,7 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
 #pragma unroll
                 for (int u = 0; u < UW; ++u) v[u] = ((j < HALF) ? lo[u] : hi[u]) & mm64;
                 const int tq = CPW * p + j;   // step 16*blk + tq
-                const u64* yk = tabi + (2 * blk + (tq >> 3)) * MT_OCT + (tq & 7) * MC;
+                const u64* yk = tabi + (2 * blk + (tq >> 3)) * RC::OCT + (tq & 7) * MC;
 #pragma unroll
                 for (int mm = 0; mm < MC; mm += 2) {
                   const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
@@ -443,8 +514,15 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
               }
             }
             const int bl = 2 * item + blk;
-            const float4 bS = *reinterpret_cast<const float4*>(ysum + bl * MC);
-            const float bs[4] = {bS.x, bS.y, bS.z, bS.w};
+            float bs[MC];
+#pragma unroll
+            for (int c4 = 0; c4 < MC; c4 += 4) {
+              const float4 bS = *reinterpret_cast<const float4*>(ysum + bl * MC + c4);
+              bs[c4] = bS.x;
+              bs[c4 + 1] = bS.y;
+              bs[c4 + 2] = bS.z;
+              bs[c4 + 3] = bS.w;
+            }
 #pragma unroll
             for (int u = 0; u < UW; ++u) {
               const float sc = __half2float(__ushort_as_half((uint16_t)(blk ? (scw[u] >> 16) : (scw[u] & 0xFFFFu))));
@@ -457,7 +535,10 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
                 if (!perrow) pb = __fmul_rn(pb, sc);
                 o[mm] = pb;
               }
-              *reinterpret_cast<float4*>(tb + (bl * R + lane + 32 * (rh + u)) * MC) = make_float4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+              for (int c4 = 0; c4 < MC; c4 += 4)
+                *reinterpret_cast<float4*>(tb + (bl * R + lane + 32 * (rh + u)) * MC + c4) =
+                    make_float4(o[c4], o[c4 + 1], o[c4 + 2], o[c4 + 3]);
             }
           }
         } else {
@@ -494,7 +575,7 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
                 v[u] = decode2(wa, wb, MASK << o, pk(offf, offf));
               }
               const int tk = wi * CPW + j;   // step
-              const u64* yk = tabi + (tk >> 3) * MT_OCT + (tk & 7) * MC;
+              const u64* yk = tabi + (tk >> 3) * RC::OCT + (tk & 7) * MC;
 #pragma unroll
               for (int mm = 0; mm < MC; mm += 2) {
                 const ulonglong2 y2 = *reinterpret_cast<const ulonglong2*>(yk + mm);
@@ -519,8 +600,13 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
               o0[mm] = perrow ? p0 : __fmul_rn(p0, s_lo);
               o1[mm] = perrow ? p1 : __fmul_rn(p1, s_hi);
             }
-            *reinterpret_cast<float4*>(tb + ((2 * item) * R + r) * MC) = make_float4(o0[0], o0[1], o0[2], o0[3]);
-            *reinterpret_cast<float4*>(tb + ((2 * item + 1) * R + r) * MC) = make_float4(o1[0], o1[1], o1[2], o1[3]);
+#pragma unroll
+            for (int c4 = 0; c4 < MC; c4 += 4) {
+              *reinterpret_cast<float4*>(tb + ((2 * item) * R + r) * MC + c4) =
+                  make_float4(o0[c4], o0[c4 + 1], o0[c4 + 2], o0[c4 + 3]);
+              *reinterpret_cast<float4*>(tb + ((2 * item + 1) * R + r) * MC + c4) =
+                  make_float4(o1[c4], o1[c4 + 1], o1[c4 + 2], o1[c4 + 3]);
+            }
           }
         }
       }
@@ -531,46 +617,6 @@ __global__ void __launch_bounds__(MtLayout<BITS, U>::THREADS, 1)
         mbar_arrive(&B->bfull[b]);
       }
     }
-  }
-}
-
-}  // namespace
-
-namespace {
-
-// The fused prologue for M >= 2 columns, one CTA per column: block sums of
-// squares of h (serial inside each 32-element block; h stored to h_out),
-// their serial sum, inv = 1/sqrt(ss/K + eps) in IEEE fp32 steps, and
-// yn = fp16((h * inv) * gamma).
-__global__ void __launch_bounds__(256) rms_prologue_kernel(GemvArgs a, __half* yn) {
-  extern __shared__ float bsum[];   // K/32 block sums
-  __shared__ float inv_sh;
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // x and r may come from the previous kernel, h_out may still be read by it
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int K = a.K, NB = K / 32, m = blockIdx.x;
-  const __half* x = a.x + (int64_t)m * K;
-  const __half* r = a.r + (int64_t)m * K;
-  __half* h_out = a.h_out ? a.h_out + (int64_t)m * K : nullptr;
-  for (int b = threadIdx.x; b < NB; b += blockDim.x) bsum[b] = block_sumsq(x, r, 32 * b, h_out);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float ss = 0.0f;
-    for (int b = 0; b < NB; ++b) ss = __fadd_rn(ss, bsum[b]);
-    inv_sh = rms_inv(ss, K, a.eps);
-  }
-  __syncthreads();
-  const float inv = inv_sh;
-  for (int k = 8 * threadIdx.x; k < K; k += 8 * blockDim.x) {
-    const uint4 xv = ldg16(reinterpret_cast<const uint4*>(x + k));
-    const uint4 rv = ldg16(reinterpret_cast<const uint4*>(r + k));
-    const uint4 gv = ldg16(reinterpret_cast<const uint4*>(a.gamma + k));
-    uint16_t yy[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) yy[e] = __half_as_ushort(norm_h(add_h(h_of(xv, e), h_of(rv, e)), inv, h_of(gv, e)));
-    uint4 out;
-    memcpy(&out, yy, 16);
-    *reinterpret_cast<uint4*>(yn + (int64_t)m * K + k) = out;
   }
 }
 
@@ -615,23 +661,21 @@ cudaError_t mt_launch(void (*kern)(KArgs...), dim3 grid, int threads, size_t sme
   return cudaGetLastError();
 }
 
-size_t mt_table_bytes(int M, int K) {
-  const size_t CC = (size_t)(M + MT_MC - 1) / MT_MC, NSEG = (size_t)(K + MT_KS - 1) / MT_KS;
-  return CC * NSEG * MT_TBLK;
+size_t mt_table_bytes(int M, int K, int MC) {
+  const size_t CC = (size_t)(M + MC - 1) / MC, NSEG = (size_t)(K + MT_KS - 1) / MT_KS;
+  return CC * NSEG * (size_t)(MC == 8 ? MtRec<8>::TBLK : MtRec<4>::TBLK);
 }
 
-size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
-
 // The table kernel, then the tiles on its records (a.ws: the records).
-template <int BITS, bool FOLD, int U>
+template <int BITS, bool FOLD, int U, int MC>
 int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
-  using L = MtLayout<BITS, U>;
-  constexpr int R = L::R, MC = L::MC;
-  auto kern = gemm_mt_kernel<BITS, FOLD, U>;
+  using L = MtLayout<BITS, U, MC>;
+  constexpr int R = L::R;
+  auto kern = gemm_mt_kernel<BITS, FOLD, U, MC>;
   static thread_local KernCache cache;
   const DevInfo& d = dev_info();
   if ((size_t)L::SMEM > (size_t)d.max_smem_optin) return QMV_ERR_UNSUPPORTED;
-  if (!a.ws || a.ws_bytes < mt_table_bytes(a.M, a.K)) return QMV_ERR_WORKSPACE;
+  if (!a.ws || a.ws_bytes < mt_table_bytes(a.M, a.K, MC)) return QMV_ERR_WORKSPACE;
   int occ = 0;
   cudaError_t e = prep_kernel(kern, cache, L::THREADS, L::SMEM, &occ);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
@@ -653,8 +697,19 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   P.tiles = (int)(((int64_t)a.N + R - 1) / R) * P.CC;
   P.NSEG = (a.K + MT_KS - 1) / MT_KS;
   P.tabs = reinterpret_cast<const unsigned char*>(a.ws);
-  e = mt_launch(mt_table_kernel<BITS, FOLD>, dim3(P.NSEG, P.CC), MT_TB_THREADS, 0, s, a.x, a.M, a.K, P.NSEG,
-                reinterpret_cast<unsigned char*>(a.ws));
+  if (a.fused) {
+    // the fused residual add + RMSNorm runs in the table kernel
+    const size_t nsm = ((size_t)MC * (a.K / 32) + MC) * sizeof(float);
+    auto tk = mt_table_kernel<BITS, FOLD, MC, true>;
+    if (nsm > 16 * 1024) e = cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)nsm);
+    if (e == cudaSuccess)
+      e = mt_launch(tk, dim3(P.NSEG, P.CC), MT_TB_THREADS * MC, nsm, s, a.x, a.r, a.gamma, a.eps, a.h_out, a.M, a.K,
+                    P.NSEG, reinterpret_cast<unsigned char*>(a.ws));
+  } else {
+    e = mt_launch(mt_table_kernel<BITS, FOLD, MC, false>, dim3(P.NSEG, P.CC), MT_TB_THREADS * MC, 0, s, a.x,
+                  (const __half*)nullptr, (const __half*)nullptr, 0.0f, (__half*)nullptr, a.M, a.K, P.NSEG,
+                  reinterpret_cast<unsigned char*>(a.ws));
+  }
   if (e == cudaSuccess) {
     const int grid = P.tiles < d.sms ? P.tiles : d.sms;
     e = mt_launch(kern, dim3(grid), L::THREADS, L::SMEM, s, a, P, tmc, tms);
@@ -663,75 +718,77 @@ int run_mt(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
   return QMV_OK;
 }
 
-// Estimated time of a row-tile height (U rows per lane), in SM cycles: whole
-// rounds of tiles over the SMs, times the segments per tile, times the
-// measured cost of one segment on GB300 (about 4500 cycles for 128 rows, 2900
-// for 64: a fixed part for the copies, tables, waits and block finishes plus
-// the paired FMAs, which scale with the rows; 32-row tiles are priced on the
-// same line).
-double mt_cost(int N, int M, int K, int U, int sms) {
+// The tile shapes built: rows per lane U and columns MC.  8-column tiles
+// share each code's mask between twice the paired FMAs; they fit shared
+// memory with two ring stages, for int2 at U <= 4 and for int4 and int8 at
+// U = 2.
+struct MtChoice {
+  int U, MC;
+};
+static bool mt_built(int bits, int U, int MC) {
+  if (MC == 4) return U == 1 || U == 2 || (U == 4 && bits != 8);
+  return U == 2 || (U == 4 && bits == 2);
+}
+
+// Estimated time of a tile shape, in SM cycles: whole rounds of tiles over
+// the SMs, times the segments per tile, times the measured cost of one
+// segment on GB300 (4 columns: about 4500 cycles for 128 rows, 2900 for 64,
+// 32-row tiles priced on the same line; 8 columns: twice the paired FMAs at
+// about 10 % better issue efficiency on the same fixed part).
+static double mt_cost(int N, int M, int K, int U, int MC, int sms) {
   const int R = 32 * U;
-  const int64_t tiles = (((int64_t)N + R - 1) / R) * ((M + MT_MC - 1) / MT_MC);
+  const int64_t tiles = (((int64_t)N + R - 1) / R) * ((M + MC - 1) / MC);
   const int64_t rounds = (tiles + sms - 1) / sms;
-  const double seg = 1300.0 + 25.0 * R;
+  const double seg = (MC == 4) ? 1300.0 + 25.0 * R : 1300.0 + 45.0 * R;
   return (double)rounds * ((K + MT_KS - 1) / MT_KS) * seg;
+}
+
+static MtChoice mt_choose(int N, int M, int K, int bits) {
+  const int sms = dev_info().sms;
+  MtChoice best{2, 4};
+  double bc = mt_cost(N, M, K, 2, 4, sms);
+  const MtChoice cand[] = {{4, 4}, {1, 4}, {2, 8}, {4, 8}};
+  for (const MtChoice& c : cand) {
+    if (!mt_built(bits, c.U, c.MC) || (c.MC == 8 && M < 5)) continue;
+    const double t = mt_cost(N, M, K, c.U, c.MC, sms);
+    if (t < bc) {
+      bc = t;
+      best = c;
+    }
+  }
+  return best;
 }
 
 template <int BITS, bool FOLD>
 int mt_bits(const GemvArgs& a, cudaStream_t s, cudaError_t* err) {
-  // rows per lane: 4 (not for int8: 16 words a row), 2, or 1 (32-row tiles,
-  // for matrices with too few 64-row tiles to cover the SMs), by the cost model
-  const int sms = dev_info().sms;
-  int best = 2;
-  double bc = mt_cost(a.N, a.M, a.K, 2, sms);
-  if (BITS != 8 && mt_cost(a.N, a.M, a.K, 4, sms) <= bc) {
-    best = 4;
-    bc = mt_cost(a.N, a.M, a.K, 4, sms);
+  const MtChoice c = mt_choose(a.N, a.M, a.K, BITS);
+  if (c.MC == 8) {
+    if constexpr (BITS == 2)
+      if (c.U == 4) return run_mt<BITS, FOLD, 4, 8>(a, s, err);
+    return run_mt<BITS, FOLD, 2, 8>(a, s, err);
   }
-  if (mt_cost(a.N, a.M, a.K, 1, sms) < bc) best = 1;
-  if (best == 1) return run_mt<BITS, FOLD, 1>(a, s, err);
+  if (c.U == 1) return run_mt<BITS, FOLD, 1, 4>(a, s, err);
   if constexpr (BITS != 8)
-    if (best == 4) return run_mt<BITS, FOLD, 4>(a, s, err);
-  return run_mt<BITS, FOLD, 2>(a, s, err);
+    if (c.U == 4) return run_mt<BITS, FOLD, 4, 4>(a, s, err);
+  return run_mt<BITS, FOLD, 2, 4>(a, s, err);
 }
 
 }  // namespace
 
 static int launch_mtile_plain(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err);
 
-size_t mt_workspace_bytes(int M, int K, bool fused) {
+size_t mt_workspace_bytes(int M, int N, int K, int bits, bool fused) {
+  (void)fused;   // the fused residual add + RMSNorm needs no scratch of its own
   if (M < 2 || K % 256 != 0) return 0;
-  return (fused ? round256((size_t)M * K * sizeof(__half)) : 0) + mt_table_bytes(M, K);
+  const MtChoice c = mt_choose(N, M, K, bits);
+  return mt_table_bytes(M, K, c.MC);
 }
 
 int launch_mtile(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {
   if (a.M < 2 || a.K % 256 != 0 || a.gather_rows || a.amax_ws) return QMV_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(a.x) & 15u) != 0) return QMV_ERR_UNSUPPORTED;
-  if (!a.ws || a.ws_bytes < mt_workspace_bytes(a.M, a.K, a.fused != 0)) return QMV_ERR_WORKSPACE;
-  if (!a.fused) return launch_mtile_plain(a, bits, s, err);
-  // fused prologue: the normalised activations into the front of the
-  // caller's workspace, then the tables and tiles on them
-  const size_t ysz = round256((size_t)a.M * a.K * sizeof(__half));
-  __half* yn = reinterpret_cast<__half*>(a.ws);
-  cudaError_t e = cudaSuccess;
-  const size_t psm = (size_t)(a.K / 32) * sizeof(float);
-  if (psm > 48 * 1024) {
-    e = cudaFuncSetAttribute(rms_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psm);
-  }
-  if (e == cudaSuccess) e = mt_launch(rms_prologue_kernel, dim3(a.M), 256, psm, s, a, yn);
-  if (e != cudaSuccess) {
-    *err = e;
-    return QMV_ERR_CUDA;
-  }
-  GemvArgs b = a;
-  b.x = yn;
-  b.fused = 0;
-  b.r = nullptr;
-  b.gamma = nullptr;
-  b.h_out = nullptr;
-  b.ws = reinterpret_cast<unsigned char*>(a.ws) + ysz;
-  b.ws_bytes = a.ws_bytes - ysz;
-  return launch_mtile_plain(b, bits, s, err);
+  if (!a.ws || a.ws_bytes < mt_workspace_bytes(a.M, a.N, a.K, bits, a.fused != 0)) return QMV_ERR_WORKSPACE;
+  return launch_mtile_plain(a, bits, s, err);
 }
 
 static int launch_mtile_plain(const GemvArgs& a, int bits, cudaStream_t s, cudaError_t* err) {

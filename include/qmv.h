@@ -131,9 +131,9 @@ QMV_API int qmv_pack_weights(qmv_pack *p, const int8_t *d_codes_in, const uint16
  *     split-K partial tiles when the chosen split needs more than the output
  *     itself, else 0.
  *   - every other M >= 2 (the CUDA-core M-column tiles): the activation
- *     tables, built once per call, ceil(M/4) * ceil(K/512) * 8960 bytes,
- *     after (fused = 1) the prologue's normalised activations, M x K fp16
- *     rounded up to 256 bytes.
+ *     tables, built once per call: per 512 codes, 8960 bytes per 4 columns
+ *     (ceil(M/4) * ceil(K/512) * 8960), or 17408 per 8 columns where the
+ *     library takes 8-column tiles (M >= 5), fused or not.
  * The size depends only on these arguments and the device's SM count, so one
  * workspace serves every later call with them.  Host only; 0 for invalid
  * arguments.
