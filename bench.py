@@ -15,7 +15,9 @@ K steps replay the token graph exactly K times, whatever K is.
 
 value = packed bytes of the K tokens / device time (CUDA events on the launch
 stream, max over ranks): effective GB/s.  `tok_per_s_equiv` = tokens / s.
-`step_ms` gives the median, p10 and p90 of the per-step times.  `e2e` is the
+`step_ms` gives the median, p10 and p90 of per-step times, taken from K
+further steps each between its own pair of events (the timed span itself has
+no events between its steps).  `e2e` is the
 same metric with the token's inputs (embedding row, residual) copied host ->
 device from pinned memory and the fp32 logits copied back inside every step.
 
@@ -561,11 +563,16 @@ def gpu_arm(args, rank, world, local):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with torch.cuda.stream(stream):
         t0.record(stream)
+        for _ in range(K):
+            g_tok.replay()
+        t1.record(stream)
+        # the per-step distribution from K more steps, each between its own
+        # pair of events (recording events between the replays slows the
+        # steps a little, so the timed span above has none)
         for a, b in ev:
             a.record(stream)
             g_tok.replay()
             b.record(stream)
-        t1.record(stream)
         # the dominant kernel's own launches: the 30 fused gate/up of the
         # token, same weights and buffers, right after the timed steps
         reps = max(3, K // 4)
