@@ -26,12 +26,15 @@
 //   warps 0..15: decode.  Thread t takes row t % 128, 32-code block
 //     (t / 128) % 2 and every second slab of the stage from t / 256: it turns
 //     the block into fp16 weights w = v*s (half2 magic decode, re-paired into
-//     natural k order) and writes them into the stage's 128-byte-swizzled
-//     K-major A sub-tile.  At the end they are the epilogue: tcgen05.ld of
-//     their TMEM lane quarter, a quarter of the tile's columns each.
-//   warp 17 (one thread): allocates the accumulator in tensor memory and
-//     issues tcgen05.mma (M=128, N=MT, K=16; four per slab), releasing each
-//     stage with tcgen05.commit on its mbarrier.
+//     natural k order) and stores them straight into tensor memory, the MMA's
+//     A operand (row = lane of its warp's lane quarter, two weights a
+//     column), so the weights never pass through shared memory.  At the end
+//     they are the epilogue: tcgen05.ld of their TMEM lane quarter, a
+//     quarter of the tile's columns each.
+//   warp 17 (one thread): allocates tensor memory (the accumulator and the
+//     A stages) and issues tcgen05.mma (A from tensor memory, B from shared
+//     memory; M=128, N=MT, K=16; four per slab), releasing each stage with
+//     tcgen05.commit on its mbarrier.
 // Every wait is bounded; a wait that runs out records an error code in this
 // file's device error word and the CTA winds down.
 #include <cuda.h>
@@ -48,6 +51,7 @@ namespace {
 constexpr uint32_t TC_SPIN = 1u << 22;
 constexpr int ERR_TC_TIMEOUT = 16;
 constexpr int RS = 4;          // K slabs per raw stage (256 codes)
+constexpr int TC_TMEM_COLS = 512;   // tensor-memory columns a CTA allocates (accumulator + A stages)
 constexpr int NDEC = 16;       // decode (and epilogue) warps
 constexpr int NSET = NDEC * 32 / 256;   // slabs of a stage decoded side by side
 constexpr int W_RAW = NDEC, W_MMA = NDEC + 1, W_B = NDEC + 2;   // role warps
@@ -196,11 +200,14 @@ template <int MT, int NST, int NRAW, int KSUB>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(TcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_x) {
-  constexpr int A_SUB = 128 * 128;                // 128 rows x 64 fp16
+  // the decoded weights (the MMA's A operand, 128 rows x 64 fp16 a slab) go
+  // to tensor memory: 32 columns a slab after the MT accumulator columns;
+  // only the activations (B) are staged in shared memory
   constexpr int B_SUB = MT * 128;                 // MT tokens x 64 fp16
-  constexpr int A_BYTES = KSUB * A_SUB;
   constexpr int B_BYTES = KSUB * B_SUB;
-  constexpr int STAGE = A_BYTES + B_BYTES;
+  constexpr int STAGE = B_BYTES;
+  constexpr uint32_t A_COL = MT;                  // first tensor-memory column of the A stages
+  static_assert(MT + NST * KSUB * 32 <= TC_TMEM_COLS, "A stages fit tensor memory");
   static_assert(RS % KSUB == 0, "a stage's slabs come from one raw stage");
   constexpr uint32_t IDESC = (1u << 4)               // D = f32
                              | ((uint32_t)(MT >> 3) << 17)  // N
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == W_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"((uint32_t)MT)
+                 "r"((uint32_t)TC_TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -281,8 +288,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_mbar_arrive_tx(&b_full[s], B_BYTES);
 #pragma unroll
         for (int u = 0; u < KSUB; ++u)
-          tc_tma2d_hint(tiles + s * STAGE + A_BYTES + u * B_SUB, &tm_x, (slab0 + i * KSUB + u) * 64, 0,
-                        &b_full[s], pol);
+          tc_tma2d_hint(tiles + s * STAGE + u * B_SUB, &tm_x, (slab0 + i * KSUB + u) * 64, 0, &b_full[s], pol);
         ++issued;
       }
       for (int i = (issued > NST ? issued - NST : 0); i < issued; ++i)
@@ -296,18 +302,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!tc_wait(&a_full[s], (i / NST) & 1, abort_f)) break;
         if (!tc_wait(&b_full[s], (i / NST) & 1, abort_f)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t abase = smem_u32(tiles + s * STAGE);
-        const uint32_t bbase = abase + A_BYTES;
+        const uint32_t bbase = smem_u32(tiles + s * STAGE);
+        const uint32_t acol = tmem + A_COL + (uint32_t)(s * KSUB * 32);
 #pragma unroll
         for (int kk = 0; kk < 4 * KSUB; ++kk) {
-          const uint64_t ad = sw128_desc(abase + (kk >> 2) * A_SUB + 32 * (kk & 3));
+          // A: 8 tensor-memory columns (16 fp16 a row) per K = 16 step
+          const uint32_t at = acol + (uint32_t)(kk * 8);
           const uint64_t bd = sw128_desc(bbase + (kk >> 2) * B_SUB + 32 * (kk & 3));
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
           asm volatile(
               "{\n\t.reg .pred p;\n\t"
               "setp.ne.u32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-              "l"(ad), "l"(bd), "r"(IDESC), "r"(acc)
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+              "r"(at), "l"(bd), "r"(IDESC), "r"(acc)
               : "memory");
         }
         asm volatile(
@@ -332,14 +339,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                              : 0u;
     for (int i = 0; i < nstage; ++i) {
       const int s = i % NST;
-      if (i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f)) break;
+      // every wait's outcome is made warp-uniform: the warp-wide tensor-memory
+      // stores below must be reached by all of its lanes or by none
+      if (__any_sync(0xFFFFFFFFu, i >= NST && !tc_wait(&empty[s], ((i / NST) - 1) & 1, abort_f))) break;
+      // the MMAs that read this A stage have completed (their commit)
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       bool ok = true;
 #pragma unroll 1
       for (int u = uset; u < KSUB; u += NSET) {
         const int sl = i * KSUB + u;   // slab
         const int j = sl / RS, rr = j % NRAW, sub = sl % RS;
         if (j != waited) {
-          if (!tc_wait(&raw_full[rr], (j / NRAW) & 1, abort_f)) {
+          if (__any_sync(0xFFFFFFFFu, !tc_wait(&raw_full[rr], (j / NRAW) & 1, abort_f))) {
             ok = false;
             break;
           }
@@ -351,14 +362,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!a.perrow)
           sb = *reinterpret_cast<const uint16_t*>(rb + RAW_CODES + row * (RS * 4) + sub * 4 + blk * 2);
         const __half2 s2 = u32_as_h2(sb | (sb << 16));
-        unsigned char* A = tiles + s * STAGE + u * A_SUB;
         const uint32_t words[2] = {cw.x, cw.y};
+        uint32_t o[16];   // the block's 32 weights in k order, two fp16 a word
 #pragma unroll
         for (int wj = 0; wj < 2; ++wj) {
-          const int wi = 2 * blk + wj;
           __half2 vp[8];
           decode_word<2>(words[wj], vp);   // vp[i] = (v_i, v_{i+8})
-          uint32_t o[8];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             // natural order: (v_2q, v_2q+1) and (v_8+2q, v_9+2q)
@@ -366,15 +375,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&vp[2 * q + 1]);
             const __half2 lo = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x5410)), s2);   // exact
             const __half2 hi = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x7632)), s2);
-            o[q] = *reinterpret_cast<const uint32_t*>(&lo);
-            o[4 + q] = *reinterpret_cast<const uint32_t*>(&hi);
+            o[8 * wj + q] = *reinterpret_cast<const uint32_t*>(&lo);
+            o[8 * wj + 4 + q] = *reinterpret_cast<const uint32_t*>(&hi);
           }
-          *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(A + sw128_off(row, 2 * wi + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
+        // row `row` is tensor-memory lane `row` (this warp's lane quarter);
+        // the block's 16 words go to its 16 columns of the slab
+        const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + A_COL +
+                               (uint32_t)((s * KSUB + u) * 32 + blk * 16);
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+            "%13, %14, %15, %16};" ::"r"(taddr),
+            "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]), "r"(o[8]),
+            "r"(o[9]), "r"(o[10]), "r"(o[11]), "r"(o[12]), "r"(o[13]), "r"(o[14]), "r"(o[15])
+            : "memory");
       }
       if (!ok) break;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // the stores are complete before the MMA thread may read them
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
         tc_mbar_arrive(&a_full[s]);
@@ -387,7 +406,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // --------------------------------------------------------- epilogue --
     // warp w reads TMEM lanes 32*(w%4) .. +31 (its lane quarter), columns of
     // its half of the tile's tokens
-    if (nstage > 0 && tc_wait(done, 0, abort_f)) {
+    if (nstage > 0 && __all_sync(0xFFFFFFFFu, tc_wait(done, 0, abort_f))) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int q4 = warp & 3;
       const int r = 32 * q4 + lane;
@@ -431,7 +450,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   if (warp == W_MMA) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)MT)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"((uint32_t)TC_TMEM_COLS)
                  : "memory");
   }
 }
@@ -498,8 +518,11 @@ bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t in
 
 template <int MT, int NST, int NRAW, int KSUB>
 static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s, cudaError_t* err) {
-  constexpr int STAGE = KSUB * (128 * 128 + MT * 128);
-  const size_t smem = 1024 + (size_t)NST * STAGE + (size_t)NRAW * RAW_BYTES + 256;
+  constexpr int STAGE = KSUB * MT * 128;
+  // at least 116 KB, so that one CTA runs per SM: each allocates all the
+  // tensor-memory columns it uses (accumulator + A stages, 512)
+  size_t smem = 1024 + (size_t)NST * STAGE + (size_t)NRAW * RAW_BYTES + 256;
+  if (smem < 116 * 1024) smem = 116 * 1024;
   static thread_local int set_dev = -1;
   auto kern = tc_gemm_kernel<MT, NST, NRAW, KSUB>;
   int dev = 0;
