@@ -209,6 +209,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   constexpr uint32_t A_COL = MT;                  // first tensor-memory column of the A stages
   static_assert(MT + NST * KSUB * 32 <= TC_TMEM_COLS, "A stages fit tensor memory");
   static_assert(RS % KSUB == 0, "a stage's slabs come from one raw stage");
+  // decode warps are at most NST - 1 stages apart; the raw stages they read
+  // must then differ by less than two trips round the raw ring, or a parity
+  // wait could match an older phase
+  static_assert((NST - 1) * KSUB / RS + 1 < 2 * NRAW, "raw ring too shallow for the decode spread");
   constexpr uint32_t IDESC = (1u << 4)               // D = f32
                              | ((uint32_t)(MT >> 3) << 17)  // N
                              | ((uint32_t)(128 >> 4) << 24);  // M
