@@ -11,7 +11,9 @@ output, as one CUDA graph with programmatic dependent launch:
   lm_head                                          int2 262144 x 2048, group 32
 = 1,274,941,440 packed bytes (codes + fp16 scales) per token, 122 launches.
 The weights (1.27 GB) are ten times the L2, so every step reads them from HBM.
-K steps replay the token graph exactly K times, whatever K is.
+Each step first copies its inputs (the embedding row and the residual, 8 KB)
+from their resident copy in HBM, so every token starts from the same finite
+state.  K steps replay the token graph exactly K times, whatever K is.
 
 value = packed bytes of the K tokens / device time (CUDA events on the launch
 stream, max over ranks): effective GB/s.  `tok_per_s_equiv` = tokens / s.
@@ -297,17 +299,25 @@ class Token:
         self.host_in = np.concatenate([synth.normal_f16(SEED, "tok.embed", (D_MODEL,)),
                                        synth.normal_f16(SEED, "tok.r", (D_MODEL,))])
         self.io.copy_(torch.from_numpy(self.host_in))
+        # a token's inputs as they sit in HBM before its step: every step
+        # starts from them (the residual stream does not carry over from the
+        # previous token; replaying on carried-over state drifts to inf/NaN)
+        self.io0 = self.io.clone()
         self.g1 = dev_f16(dev, "tok.g1", (D_MODEL,), mean=1.0, std=0.1)
         self.g2 = dev_f16(dev, "tok.g2", (D_MODEL,), mean=1.0, std=0.1)
         self.x, self.h, self.yq, self.yo = f16(D_MODEL), f16(D_MODEL), f16(2560), f16(D_MODEL)
         self.ygu = f16(2 * TOKEN_FF)
         self.logits = torch.empty(1, LM_HEAD[1], dtype=torch.float32, device=dev)
 
-    def run(self, stream):
+    def run(self, stream, fresh=True):
         """ple -> 30 x (fused qkv -> o -> fused gate/up -> down) -> lm_head:
-        122 launches, each reading the previous one's output."""
+        122 launches, each reading the previous one's output.  fresh: first
+        copy the token's inputs (embedding row, residual) from their resident
+        copy in HBM; without it the caller has just put them in place."""
         q = self.qmv
         F16, FAST = q.QMV_F16, q.QMV_FAST
+        if fresh:
+            self.io.copy_(self.io0)
         q.qmv_gemv(self.ple, self.e, y=self.x, y_dtype=F16, mode=FAST, stream=stream)
         for lay in self.layers:
             q.qmv_fused_rmsnorm_gemv(lay["qkv"], self.x, self.r, self.g1, EPS, h_out=self.h, y=self.yq,
@@ -585,6 +595,7 @@ def gpu_arm(args, rank, world, local):
     torch.cuda.synchronize()
     barrier()
     ck = clocks.stop()
+    logits_finite = bool(torch.isfinite(tok.logits).all().item())
     ms = t0.elapsed_time(t1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     dom_ms = d0.elapsed_time(d1) / (reps * TOKEN_LAYERS)
@@ -598,7 +609,7 @@ def gpu_arm(args, rank, world, local):
 
     def e2e_step():
         tok.io.copy_(pin, non_blocking=True)
-        tok.run(stream)
+        tok.run(stream, fresh=False)
         logits_host.copy_(tok.logits, non_blocking=True)
 
     g_e2e = capture(stream, e2e_step)
@@ -647,6 +658,7 @@ def gpu_arm(args, rank, world, local):
         "tok_per_s_equiv": round(world * K / (ms_max * 1e-3), 1),
         "step_ms": {k: (round(v, 5) if isinstance(v, float) else v) for k, v in st.items()},
         "gpu_launches": TOKEN_LAUNCHES * K,
+        "logits_finite": logits_finite,
         "roofline": {"bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": measured_traffic("gemv_m1_fused_int2_32768x2048"),
