@@ -364,6 +364,7 @@ def block_c2(qmv, dev, L=32):
               for li in range(L)]
     f16 = lambda n: torch.zeros(1, n, dtype=torch.float16, device=dev)
     b = dict(x=dev_f16(dev, "bench.x", (1, D_MODEL)), r=dev_f16(dev, "bench.r", (1, D_MODEL)),
+             x0=dev_f16(dev, "bench.x", (1, D_MODEL)), r0=dev_f16(dev, "bench.r", (1, D_MODEL)),
              g1=dev_f16(dev, "bench.g1", (D_MODEL,), mean=1.0, std=0.1),
              g2=dev_f16(dev, "bench.g2", (D_MODEL,), mean=1.0, std=0.1),
              h=f16(D_MODEL), y_qkv=f16(2560), y_o=f16(D_MODEL), y_gu=f16(2 * LAYER_FF))
@@ -378,6 +379,15 @@ def layer_ops(lay, b):
             ("gemv", lay["o"], b["y_qkv"][:, :D_MODEL], None, None, None, b["y_o"]),
             ("fused", lay["gateup"], b["y_o"], b["h"], b["g2"], b["r"], b["y_gu"]),
             ("gemv", lay["down"], b["y_gu"][:, :LAYER_FF], None, None, None, b["x"])]
+
+
+def fresh_inputs(b, stream):
+    """Restore the layers' inputs (x, r) from their resident copies on
+    `stream`, so that repeated runs start from the same finite state."""
+    import torch
+    with torch.cuda.stream(stream):
+        b["x"].copy_(b["x0"])
+        b["r"].copy_(b["r0"])
 
 
 def run_layer(qmv, lay, b, stream):
@@ -410,8 +420,8 @@ def chain_eager(qmv, dev, stream, layers, b, ch, reps):
     chain).  Microseconds per layer / per matvec, wall clock."""
     import torch
     L = len(layers)
-    sep = wall_us(lambda: [run_layer(qmv, lay, b, stream) for lay in layers], reps) / L
-    chn = wall_us(lambda: ch.run(stream), reps) / L
+    sep = wall_us(lambda: (fresh_inputs(b, stream), [run_layer(qmv, lay, b, stream) for lay in layers]), reps) / L
+    chn = wall_us(lambda: (fresh_inputs(b, stream), ch.run(stream)), reps) / L
     n = 64
     packs = [make_pack(qmv, dev, f"ce.{i}", 1024, 1024, 2, 32) for i in range(n)]
     x = dev_f16(dev, "ce.x", (1, 1024))
@@ -709,11 +719,11 @@ def side_blocks(qmv, dev, stream, args, world):
         L = len(layers)
         items = {}
         if "c2" in want:
-            items["c2"] = capture(stream, lambda: [run_layer(qmv, lay, b, stream) for lay in layers])
+            items["c2"] = capture(stream, lambda: (fresh_inputs(b, stream), [run_layer(qmv, lay, b, stream) for lay in layers]))
         ch = None
         if "chain" in want:
             ch = chain_layers(qmv, layers, b)
-            items["chain"] = capture(stream, lambda: ch.run(stream))
+            items["chain"] = capture(stream, lambda: (fresh_inputs(b, stream), ch.run(stream)))
         r = interleaved(stream, items, rounds)
         if "c2" in r:
             out["c2"] = dict(summ(r["c2"], L, LAYER_BYTES,
