@@ -17,15 +17,17 @@
 // second kernel adds the splits in split order, so the result never depends
 // on CTA timing).  A pipeline stage carries KSUB 64-code slabs (4 for MT =
 // 64, 2 for MT = 128): one hand-off between the roles per 64*KSUB codes.
+// The 16 decode warps form two groups that take alternate stages, so two
+// stages' decodes are in flight at once.
 // Roles:
 //   warp 16 (one thread): TMA of the packed codes and scales of the tile, 4
 //     K-slabs (256 codes) at a time, into a ring of raw stages.
 //   warp 18 (one thread): TMA of the activation sub-tiles of each stage's
 //     slabs straight into the MMA operand stage, with a 128-byte-swizzle
 //     tensor map (the K-major layout the MMA reads).
-//   warps 0..15: decode.  Thread t takes row t % 128, 32-code block
-//     (t / 128) % 2 and every second slab of the stage from t / 256: it turns
-//     the block into fp16 weights w = v*s (half2 magic decode, re-paired into
+//   warps 0..15: decode, in two groups of eight taking alternate stages.
+//     Thread t of a group takes row t % 128 and 32-code block (t / 128) % 2
+//     of every slab of its stage: it turns the block into fp16 weights w = v*s (half2 magic decode, re-paired into
 //     natural k order) and stores them straight into tensor memory, the MMA's
 //     A operand (row = lane of its warp's lane quarter, two weights a
 //     column), so the weights never pass through shared memory.  At the end
@@ -53,7 +55,7 @@ constexpr int ERR_TC_TIMEOUT = 16;
 constexpr int RS = 4;          // K slabs per raw stage (256 codes)
 constexpr int TC_TMEM_COLS = 512;   // tensor-memory columns a CTA allocates (accumulator + A stages)
 constexpr int NDEC = 16;       // decode (and epilogue) warps
-constexpr int NSET = NDEC * 32 / 256;   // slabs of a stage decoded side by side
+constexpr int NGRP = NDEC / 8;          // decode groups, each taking every NGRP-th stage
 constexpr int W_RAW = NDEC, W_MMA = NDEC + 1, W_B = NDEC + 2;   // role warps
 constexpr int TC_THREADS = 32 * (NDEC + 3);
 constexpr int RAW_CODES = 128 * RS * 16;   // bytes of codes per raw stage
@@ -148,8 +150,8 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
 
 }  // namespace
 
-// Raw-ring depth (slabs a raw stage) of the two tile shapes.
-constexpr int TC_RS_M64 = 2, TC_RS_M128 = 2;
+// Raw-ring depth (raw stages of RS slabs) of the two tile shapes.
+constexpr int TC_RS_M64 = 3, TC_RS_M128 = 3;
 
 // How K is split across CTAs: split K to balance the waves; the time is
 // about ceil(tiles * split / SMs) CTA-slots of 1/split of the work each; the
@@ -240,13 +242,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
-      tc_mbar_init(&a_full[s], NDEC);
+      tc_mbar_init(&a_full[s], NDEC / NGRP);
       tc_mbar_init(&b_full[s], 1);
       tc_mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < NRAW; ++r) {
       tc_mbar_init(&raw_full[r], 1);
-      tc_mbar_init(&raw_empty[r], NDEC);
+      // the decode groups whose stages read a raw stage each arrive once
+      tc_mbar_init(&raw_empty[r], (NDEC / NGRP) * (RS / KSUB < NGRP ? RS / KSUB : NGRP));
     }
     tc_mbar_init(done, 1);
     *abort_f = 0;
@@ -332,16 +335,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           : "memory");
     }
   } else {
-    // ---------------------------- decode (NDEC warps: row, block and slab) --
-    static_assert(KSUB % NSET == 0, "a stage's slabs split evenly over the decode sets");
+    // -------------------------- decode (NGRP groups of 8 warps, by stage) --
+    // group g decodes stages g, g + NGRP, ...: the groups' stages are in
+    // flight at once, each group's chain (raw wait, decode, tensor-memory
+    // store, its completion, the hand-off) overlapping the other's
+    const int grp = warp >> 3;
     const int row = threadIdx.x & 127;        // weight row of the tile
     const int blk = (threadIdx.x >> 7) & 1;   // which 32-code block of the slab
-    const int uset = threadIdx.x >> 8;        // which of the stage's slabs (every NSET-th)
     int waited = -1;                          // the last raw stage this thread waited for
     const uint32_t prs = a.perrow && n0 + row < a.N
                              ? (uint32_t)__half_as_ushort(__ldg(a.scales + n0 + row))
                              : 0u;
-    for (int i = 0; i < nstage; ++i) {
+    for (int i = grp; i < nstage; i += NGRP) {
       const int s = i % NST;
       // every wait's outcome is made warp-uniform: the warp-wide tensor-memory
       // stores below must be reached by all of its lanes or by none
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       bool ok = true;
 #pragma unroll 1
-      for (int u = uset; u < KSUB; u += NSET) {
+      for (int u = 0; u < KSUB; ++u) {
         const int sl = i * KSUB + u;   // slab
         const int j = sl / RS, rr = j % NRAW, sub = sl % RS;
         if (j != waited) {
@@ -401,9 +406,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         tc_mbar_arrive(&a_full[s]);
-        // the stage's last slab ends a raw stage (RS is a multiple of KSUB)
-        const int last = i * KSUB + KSUB - 1;
-        if (last % RS == RS - 1) tc_mbar_arrive(&raw_empty[(last / RS) % NRAW]);
+        // this group is done with a raw stage when its next stage reads another
+        const int j = (i * KSUB) / RS;
+        if (i + NGRP >= nstage || ((i + NGRP) * KSUB) / RS != j) tc_mbar_arrive(&raw_empty[j % NRAW]);
       }
     }
 
@@ -604,15 +609,13 @@ int launch_tc_gemm(const GemvArgs& g, int bits, cudaStream_t s, cudaError_t* err
   a.split = 1;
   a.slabs_per_split = g.K / 64;
   const int tiles = (g.N + 127) / 128;
-  // the raw ring (codes + scales, 4 slabs a stage) keeps about an HBM
-  // latency of weight data in flight; the decoded stages fill the rest
-  // stages of several 64-code slabs: the roles' hand-offs, not the data
-  // paths, set the pace (0.46 us a slab with every copy, decode and MMA
-  // removed), so a stage carries four slabs for M <= 64 (two stages of
-  // 96 KB) and two for M = 128 (three stages of 64 KB); a two-slab raw ring
-  // keeps a code and scale copy in flight
-  if (g.M <= 64) return run_tc<64, 2, TC_RS_M64, 4>(a, g, tiles, s, err);
-  return run_tc<128, 3, TC_RS_M128, 2>(a, g, tiles, s, err);
+  // stages of several 64-code slabs (smaller stages measured slower): four
+  // slabs for M <= 64, two for M = 128.  Only the activation tiles sit in
+  // shared memory (32 KB a stage), the decoded weights in tensor memory, so
+  // there are three stages at M <= 64 and six at M = 128 (the tensor-memory
+  // columns' limit), and three raw stages of codes and scales
+  if (g.M <= 64) return run_tc<64, 3, TC_RS_M64, 4>(a, g, tiles, s, err);
+  return run_tc<128, 6, TC_RS_M128, 2>(a, g, tiles, s, err);
 }
 
 }  // namespace qmv
