@@ -294,11 +294,11 @@ __host__ __device__ inline int tma_round16(int x) { return (x + 15) & ~15; }
 
 // ------------------------------------------------------ op-level pieces --
 
-// Codes per segment: the whole row up to 2048, else the largest multiple of
-// 256 up to 2048 that divides K.
-inline int tma_segment(int K) {
-  if (K <= 2048) return K;
-  for (int d = 8; d >= 1; --d)
+// Codes per segment: the whole row up to ks_max (2048 or 4096), else the
+// largest multiple of 256 up to ks_max that divides K.
+inline int tma_segment(int K, int ks_max = 2048) {
+  if (K <= ks_max) return K;
+  for (int d = ks_max / 256; d >= 1; --d)
     if ((K / 256) % d == 0) return 256 * d;
   return 256;
 }

@@ -25,6 +25,8 @@ SHAPES = [
     (2048, 2048, 8, 2048),    # per-row int8 projection
     (1, 64, 2, 32), (3, 128, 2, 128), (33, 96, 4, 32), (65, 160, 8, 32), (100, 5376, 4, 32),
     (37, 5376, 8, 5376), (19, 21504, 4, 32), (29, 14336, 2, 32), (5, 16384, 2, 32),
+    # few rows over a long K: 4096-code segments, a ragged last row group
+    (2047, 20480, 2, 32), (700, 16384, 4, 32),
 ]
 
 
