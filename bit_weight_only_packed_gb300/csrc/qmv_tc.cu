@@ -215,6 +215,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // must then differ by less than two trips round the raw ring, or a parity
   // wait could match an older phase
   static_assert((NST - 1) * KSUB / RS + 1 < 2 * NRAW, "raw ring too shallow for the decode spread");
+  // a decode group's wait for the MMAs of stage i - NST (A stage reuse) is a
+  // parity wait, which tells a phase only from the one before it: the
+  // group's previous wait (stage i - NGRP - NST) must already imply the
+  // completion of stage i - 2 * NST, i.e. NGRP <= NST
+  static_assert(NGRP <= NST, "more decode groups than A stages: the A-stage parity waits could alias");
   constexpr uint32_t IDESC = (1u << 4)               // D = f32
                              | ((uint32_t)(MT >> 3) << 17)  // N
                              | ((uint32_t)(128 >> 4) << 24);  // M
