@@ -220,6 +220,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // group's previous wait (stage i - NGRP - NST) must already imply the
   // completion of stage i - 2 * NST, i.e. NGRP <= NST
   static_assert(NGRP <= NST, "more decode groups than A stages: the A-stage parity waits could alias");
+  // likewise a decode warp's raw-stage wait: when it waits for raw stage j
+  // it has seen the MMAs of stage i - NST complete, so every raw stage up to
+  // (i - NST) * KSUB / RS has landed; raw stage j - NRAW (the previous phase
+  // of the same buffer) must be among them
+  static_assert(NST * KSUB <= NRAW * RS, "raw ring too shallow for the A ring: raw parity waits could alias");
   constexpr uint32_t IDESC = (1u << 4)               // D = f32
                              | ((uint32_t)(MT >> 3) << 17)  // N
                              | ((uint32_t)(128 >> 4) << 24);  // M
