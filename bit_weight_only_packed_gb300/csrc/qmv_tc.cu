@@ -55,12 +55,13 @@ constexpr int ERR_TC_TIMEOUT = 16;
 constexpr int RS = 4;          // K slabs per raw stage (256 codes)
 constexpr int TC_TMEM_COLS = 512;   // tensor-memory columns a CTA allocates (accumulator + A stages)
 constexpr int NDEC = 16;       // decode (and epilogue) warps
-constexpr int NGRP = NDEC / 8;          // decode groups, each taking every NGRP-th stage
 constexpr int W_RAW = NDEC, W_MMA = NDEC + 1, W_B = NDEC + 2;   // role warps
 constexpr int TC_THREADS = 32 * (NDEC + 3);
 constexpr int RAW_CODES = 128 * RS * 16;   // bytes of codes per raw stage
 constexpr int RAW_SC = 128 * RS * 4;       // bytes of scales per raw stage
 constexpr int RAW_BYTES = RAW_CODES + RAW_SC;
+static_assert(RS * 16 == 64, "a row of a raw stage's codes is one 64-byte swizzle span");
+static_assert(RAW_BYTES % 1024 == 0, "raw stages keep the swizzle's alignment");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -198,7 +199,7 @@ struct TcArgs {
 // KSUB 64-code slabs per pipeline stage: each stage holds KSUB weight
 // sub-tiles (128 rows x 64 fp16 each) and KSUB activation sub-tiles (MT x 64
 // fp16 each), so the roles hand a stage over once per 64*KSUB codes.
-template <int MT, int NST, int NRAW, int KSUB>
+template <int MT, int NST, int NRAW, int KSUB, int GW>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_gemm_kernel(TcArgs a, const __grid_constant__ CUtensorMap tm_codes,
                    const __grid_constant__ CUtensorMap tm_scales, const __grid_constant__ CUtensorMap tm_x) {
@@ -219,6 +220,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // parity wait, which tells a phase only from the one before it: the
   // group's previous wait (stage i - NGRP - NST) must already imply the
   // completion of stage i - 2 * NST, i.e. NGRP <= NST
+  static_assert(GW == 4 || GW == 8, "decode groups of 4 warps (both blocks a thread) or 8 (one)");
+  constexpr int NGRP = NDEC / GW;   // decode groups, each taking every NGRP-th stage
   static_assert(NGRP <= NST, "more decode groups than A stages: the A-stage parity waits could alias");
   // likewise a decode warp's raw-stage wait: when it waits for raw stage j
   // it has seen the MMAs of stage i - NST complete, so every raw stage up to
@@ -345,13 +348,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           : "memory");
     }
   } else {
-    // -------------------------- decode (NGRP groups of 8 warps, by stage) --
+    // ------------------------ decode (NGRP groups of GW warps, by stage) --
     // group g decodes stages g, g + NGRP, ...: the groups' stages are in
     // flight at once, each group's chain (raw wait, decode, tensor-memory
-    // store, its completion, the hand-off) overlapping the other's
-    const int grp = warp >> 3;
+    // store, its completion, the hand-off) overlapping the others'.  With
+    // 8-warp groups a thread decodes one 32-code block of its row of a slab,
+    // with 4-warp groups both.
+    const int grp = warp / GW;
     const int row = threadIdx.x & 127;        // weight row of the tile
-    const int blk = (threadIdx.x >> 7) & 1;   // which 32-code block of the slab
+    const int blk = GW == 8 ? (threadIdx.x >> 7) & 1 : 0;   // first 32-code block of the slab
+    constexpr int NB = GW == 8 ? 1 : 2;       // blocks a thread decodes
     int waited = -1;                          // the last raw stage this thread waited for
     const uint32_t prs = a.perrow && n0 + row < a.N
                              ? (uint32_t)__half_as_ushort(__ldg(a.scales + n0 + row))
@@ -376,38 +382,70 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           waited = j;
         }
         const unsigned char* rb = rawbuf + rr * RAW_BYTES;
-        const uint2 cw = *reinterpret_cast<const uint2*>(rb + row * (RS * 16) + sub * 16 + blk * 8);
-        uint32_t sb = prs;
-        if (!a.perrow)
-          sb = *reinterpret_cast<const uint16_t*>(rb + RAW_CODES + row * (RS * 4) + sub * 4 + blk * 2);
-        const __half2 s2 = u32_as_h2(sb | (sb << 16));
-        const uint32_t words[2] = {cw.x, cw.y};
-        uint32_t o[16];   // the block's 32 weights in k order, two fp16 a word
+        // the codes arrive 64-byte swizzled (offset bits 4..5 XOR bits 7..8):
+        // a thread's 8 (one block) or 16 bytes (both) of its 64-byte row
+        const uint32_t co = (uint32_t)(row * (RS * 16) + sub * 16 + blk * 8);
+        const unsigned char* cp = rb + (co ^ (((co >> 7) & 3u) << 4));
+        uint32_t words[2 * NB], sbb;
+        if constexpr (NB == 1) {
+          const uint2 cw = *reinterpret_cast<const uint2*>(cp);
+          words[0] = cw.x;
+          words[1] = cw.y;
+          sbb = a.perrow ? prs
+                         : *reinterpret_cast<const uint16_t*>(rb + RAW_CODES + row * (RS * 4) + sub * 4 + blk * 2);
+        } else {
+          const uint4 cw = *reinterpret_cast<const uint4*>(cp);
+          words[0] = cw.x;
+          words[1] = cw.y;
+          words[2] = cw.z;
+          words[3] = cw.w;
+          // block 0's scale in the low half, block 1's in the high half
+          sbb = a.perrow ? (prs | (prs << 16))
+                         : *reinterpret_cast<const uint32_t*>(rb + RAW_CODES + row * (RS * 4) + sub * 4);
+        }
+        uint32_t o[16 * NB];   // the blocks' weights in k order, two fp16 a word
 #pragma unroll
-        for (int wj = 0; wj < 2; ++wj) {
-          __half2 vp[8];
-          decode_word<2>(words[wj], vp);   // vp[i] = (v_i, v_{i+8})
+        for (int b = 0; b < NB; ++b) {
+          const uint32_t sb = (sbb >> (16 * b)) & 0xFFFFu;
+          const __half2 s2 = u32_as_h2(sb | (sb << 16));
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            // natural order: (v_2q, v_2q+1) and (v_8+2q, v_9+2q)
-            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&vp[2 * q]);
-            const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&vp[2 * q + 1]);
-            const __half2 lo = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x5410)), s2);   // exact
-            const __half2 hi = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x7632)), s2);
-            o[8 * wj + q] = *reinterpret_cast<const uint32_t*>(&lo);
-            o[8 * wj + 4 + q] = *reinterpret_cast<const uint32_t*>(&hi);
+          for (int wj = 0; wj < 2; ++wj) {
+            __half2 vp[8];
+            decode_word<2>(words[2 * b + wj], vp);   // vp[i] = (v_i, v_{i+8})
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              // natural order: (v_2q, v_2q+1) and (v_8+2q, v_9+2q)
+              const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&vp[2 * q]);
+              const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&vp[2 * q + 1]);
+              const __half2 lo = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x5410)), s2);   // exact
+              const __half2 hi = __hmul2(u32_as_h2(__byte_perm(a0, a1, 0x7632)), s2);
+              o[16 * b + 8 * wj + q] = *reinterpret_cast<const uint32_t*>(&lo);
+              o[16 * b + 8 * wj + 4 + q] = *reinterpret_cast<const uint32_t*>(&hi);
+            }
           }
         }
         // row `row` is tensor-memory lane `row` (this warp's lane quarter);
-        // the block's 16 words go to its 16 columns of the slab
+        // a block's 16 words go to its 16 columns of the slab
         const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + A_COL +
                                (uint32_t)((s * KSUB + u) * 32 + blk * 16);
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-            "%13, %14, %15, %16};" ::"r"(taddr),
-            "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]), "r"(o[8]),
-            "r"(o[9]), "r"(o[10]), "r"(o[11]), "r"(o[12]), "r"(o[13]), "r"(o[14]), "r"(o[15])
-            : "memory");
+        if constexpr (NB == 1) {
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+              "%13, %14, %15, %16};" ::"r"(taddr),
+              "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]), "r"(o[8]),
+              "r"(o[9]), "r"(o[10]), "r"(o[11]), "r"(o[12]), "r"(o[13]), "r"(o[14]), "r"(o[15])
+              : "memory");
+        } else {
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+              "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+              "%32};" ::"r"(taddr),
+              "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]), "r"(o[8]),
+              "r"(o[9]), "r"(o[10]), "r"(o[11]), "r"(o[12]), "r"(o[13]), "r"(o[14]), "r"(o[15]), "r"(o[16]),
+              "r"(o[17]), "r"(o[18]), "r"(o[19]), "r"(o[20]), "r"(o[21]), "r"(o[22]), "r"(o[23]), "r"(o[24]),
+              "r"(o[25]), "r"(o[26]), "r"(o[27]), "r"(o[28]), "r"(o[29]), "r"(o[30]), "r"(o[31])
+              : "memory");
+        }
       }
       if (!ok) break;
       // the stores are complete before the MMA thread may read them
@@ -535,7 +573,7 @@ bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT, int NST, int NRAW, int KSUB>
+template <int MT, int NST, int NRAW, int KSUB, int GW>
 static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s, cudaError_t* err) {
   constexpr int STAGE = KSUB * MT * 128;
   // at least 116 KB, so that one CTA runs per SM: each allocates all the
@@ -543,7 +581,7 @@ static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s
   size_t smem = 1024 + (size_t)NST * STAGE + (size_t)NRAW * RAW_BYTES + 256;
   if (smem < 116 * 1024) smem = 116 * 1024;
   static thread_local int set_dev = -1;
-  auto kern = tc_gemm_kernel<MT, NST, NRAW, KSUB>;
+  auto kern = tc_gemm_kernel<MT, NST, NRAW, KSUB, GW>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) { *err = e; return QMV_ERR_CUDA; }
@@ -558,7 +596,7 @@ static int run_tc(const TcArgs& a0, const GemvArgs& g, int tiles, cudaStream_t s
   // and columns past K are zero-filled.
   CUtensorMap tmc, tms, tmx;
   if (!enc2d(&tmc, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.codes, (uint64_t)g.K / 16, (uint64_t)g.N,
-             (uint64_t)g.K / 4, 4 * RS, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+             (uint64_t)g.K / 4, 4 * RS, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return QMV_ERR_UNSUPPORTED;
   if (g.perrow) {
     tms = tmc;   // unused
@@ -624,8 +662,8 @@ int launch_tc_gemm(const GemvArgs& g, int bits, cudaStream_t s, cudaError_t* err
   // shared memory (32 KB a stage), the decoded weights in tensor memory, so
   // there are three stages at M <= 64 and six at M = 128 (the tensor-memory
   // columns' limit), and three raw stages of codes and scales
-  if (g.M <= 64) return run_tc<64, 3, TC_RS_M64, 4>(a, g, tiles, s, err);
-  return run_tc<128, 6, TC_RS_M128, 2>(a, g, tiles, s, err);
+  if (g.M <= 64) return run_tc<64, 3, TC_RS_M64, 4, 8>(a, g, tiles, s, err);
+  return run_tc<128, 6, TC_RS_M128, 2, 4>(a, g, tiles, s, err);
 }
 
 }  // namespace qmv
