@@ -17,22 +17,26 @@
 // second kernel adds the splits in split order, so the result never depends
 // on CTA timing).  A pipeline stage carries KSUB 64-code slabs (4 for MT =
 // 64, 2 for MT = 128): one hand-off between the roles per 64*KSUB codes.
-// The 16 decode warps form two groups that take alternate stages, so two
-// stages' decodes are in flight at once.
+// The 16 decode warps form groups that take stages in turn, so several
+// stages' decodes are in flight at once: four groups of four warps at
+// MT = 128, two groups of eight at MT = 64 (a group's parity wait for the
+// reuse of an A stage needs groups <= A stages).
 // Roles:
-//   warp 16 (one thread): TMA of the packed codes and scales of the tile, 4
-//     K-slabs (256 codes) at a time, into a ring of raw stages.
+//   warp 16 (one thread): TMA of the packed codes (64-byte swizzle) and
+//     scales of the tile, 4 K-slabs (256 codes) at a time, into a ring of
+//     raw stages.
 //   warp 18 (one thread): TMA of the activation sub-tiles of each stage's
 //     slabs straight into the MMA operand stage, with a 128-byte-swizzle
 //     tensor map (the K-major layout the MMA reads).
-//   warps 0..15: decode, in two groups of eight taking alternate stages.
-//     Thread t of a group takes row t % 128 and 32-code block (t / 128) % 2
-//     of every slab of its stage: it turns the block into fp16 weights w = v*s (half2 magic decode, re-paired into
-//     natural k order) and stores them straight into tensor memory, the MMA's
-//     A operand (row = lane of its warp's lane quarter, two weights a
-//     column), so the weights never pass through shared memory.  At the end
-//     they are the epilogue: tcgen05.ld of their TMEM lane quarter, a
-//     quarter of the tile's columns each.
+//   warps 0..15: decode.  Thread t of a group takes row t % 128 of every
+//     slab of its stage, both 32-code blocks with four-warp groups, block
+//     (t / 128) % 2 with eight-warp groups: it turns them into fp16 weights
+//     w = v*s (half2 magic decode, re-paired into natural k order) and stores
+//     them straight into tensor memory, the MMA's A operand (row = lane of
+//     its warp's lane quarter, two weights a column), so the weights never
+//     pass through shared memory.  At the end they are the epilogue:
+//     tcgen05.ld of their TMEM lane quarter, a quarter of the tile's columns
+//     each.
 //   warp 17 (one thread): allocates tensor memory (the accumulator and the
 //     A stages) and issues tcgen05.mma (A from tensor memory, B from shared
 //     memory; M=128, N=MT, K=16; four per slab), releasing each stage with
