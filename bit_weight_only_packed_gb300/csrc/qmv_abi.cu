@@ -318,6 +318,78 @@ int qmv_pack_info(const qmv_pack* p, int* N, int* K, int* bits, int* group) {
   return QMV_OK;
 }
 
+// The saved-pack header (layout in qmv.h): little-endian fields written
+// byte by byte, so the format does not depend on the host's struct layout.
+static void put32(unsigned char* b, uint32_t v) {
+  for (int i = 0; i < 4; ++i) b[i] = (unsigned char)(v >> (8 * i));
+}
+static void put64(unsigned char* b, uint64_t v) {
+  for (int i = 0; i < 8; ++i) b[i] = (unsigned char)(v >> (8 * i));
+}
+static uint32_t get32(const unsigned char* b) {
+  uint32_t v = 0;
+  for (int i = 0; i < 4; ++i) v |= (uint32_t)b[i] << (8 * i);
+  return v;
+}
+static uint64_t get64(const unsigned char* b) {
+  uint64_t v = 0;
+  for (int i = 0; i < 8; ++i) v |= (uint64_t)b[i] << (8 * i);
+  return v;
+}
+static const char k_pack_magic[8] = {'Q', 'M', 'V', 'P', 'A', 'C', 'K', 0};
+
+int qmv_pack_header(const qmv_pack* p, void* header_out) {
+  if (!pack_ok(p) || !header_out) return QMV_ERR_INVALID_ARG;
+  unsigned char* b = (unsigned char*)header_out;
+  memset(b, 0, QMV_PACK_HEADER_BYTES);
+  memcpy(b, k_pack_magic, 8);
+  put32(b + 8, QMV_PACK_VERSION);
+  put32(b + 12, QMV_PACK_HEADER_BYTES);
+  put32(b + 16, (uint32_t)p->N);
+  put32(b + 20, (uint32_t)p->K);
+  put32(b + 24, (uint32_t)p->bits);
+  put32(b + 28, (uint32_t)p->group);
+  put64(b + 32, (uint64_t)p->codes_bytes);
+  put64(b + 40, (uint64_t)p->scales_bytes);
+  return QMV_OK;
+}
+
+int qmv_create_pack_from_header(qmv_pack** out, const void* header, size_t* codes_bytes,
+                                size_t* scales_bytes) {
+  if (!out) return QMV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!header) return QMV_ERR_INVALID_ARG;
+  const unsigned char* b = (const unsigned char*)header;
+  if (memcmp(b, k_pack_magic, 8) != 0 || get32(b + 12) != QMV_PACK_HEADER_BYTES)
+    return QMV_ERR_INVALID_ARG;
+  for (int i = 48; i < QMV_PACK_HEADER_BYTES; ++i)
+    if (b[i]) return QMV_ERR_INVALID_ARG;
+  if (get32(b + 8) != QMV_PACK_VERSION) return QMV_ERR_UNSUPPORTED;
+  const int N = (int)get32(b + 16), K = (int)get32(b + 20), bits = (int)get32(b + 24),
+            group = (int)get32(b + 28);
+  size_t cb = 0, sb = 0;
+  qmv_pack* p = nullptr;
+  const int st = qmv_create_pack(&p, N, K, bits, group, &cb, &sb);
+  if (st != QMV_OK) return st;
+  if (get64(b + 32) != (uint64_t)cb || get64(b + 40) != (uint64_t)sb) {
+    qmv_destroy_pack(p);
+    return QMV_ERR_SHAPE;
+  }
+  if (codes_bytes) *codes_bytes = cb;
+  if (scales_bytes) *scales_bytes = sb;
+  *out = p;
+  return QMV_OK;
+}
+
+int qmv_bind_packed(qmv_pack* p, void* d_codes, void* d_scales) {
+  if (!pack_ok(p) || !d_codes || !d_scales) return QMV_ERR_INVALID_ARG;
+  if (!aligned(d_codes, 16) || !aligned(d_scales, 16)) return QMV_ERR_ALIGNMENT;
+  p->d_codes = (const uint32_t*)d_codes;
+  p->d_scales = (const uint16_t*)d_scales;
+  p->bound = 1;
+  return QMV_OK;
+}
+
 int qmv_destroy_pack(qmv_pack* p) {
   if (!pack_ok(p)) return QMV_ERR_INVALID_ARG;
   p->magic = 0;

@@ -25,6 +25,7 @@ QMV_ERR_TIMEOUT = -6
 QMV_ERR_WORKSPACE = -7
 QMV_F32, QMV_F16 = 0, 1
 QMV_FAST, QMV_EXACT = 0, 1
+QMV_PACK_HEADER_BYTES, QMV_PACK_VERSION = 64, 1
 
 # every entry point declared in include/qmv.h, with its ctypes signature
 _P, _I, _F, _SZP = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.POINTER(ctypes.c_size_t)
@@ -39,6 +40,9 @@ SIGNATURES = {
     "qmv_pack_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
                            ctypes.POINTER(_I)]),
     "qmv_destroy_pack": (_I, [_P]),
+    "qmv_pack_header": (_I, [_P, _P]),
+    "qmv_create_pack_from_header": (_I, [ctypes.POINTER(_P), _P, _SZP, _SZP]),
+    "qmv_bind_packed": (_I, [_P, _P, _P]),
     "qmv_status_string": (ctypes.c_char_p, [_I]),
     "qmv_last_cuda_error": (_I, []),
     "qmv_device_error": (_I, [ctypes.POINTER(_I), _I]),
@@ -132,16 +136,44 @@ class Pack:
     """A packed weight matrix: the host descriptor plus the device buffers
     (allocated with torch) that hold the packed codes and scales."""
 
-    def __init__(self, N: int, K: int, bits: int, group: int):
+    def __init__(self, N: int, K: int, bits: int, group: int, header: bytes = None):
         h = _P()
         cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
-        _check("qmv_create_pack", _lib.qmv_create_pack(ctypes.byref(h), N, K, bits, group,
-                                                        ctypes.byref(cb), ctypes.byref(sb)))
+        if header is None:
+            _check("qmv_create_pack", _lib.qmv_create_pack(ctypes.byref(h), N, K, bits, group,
+                                                            ctypes.byref(cb), ctypes.byref(sb)))
+        else:
+            if len(header) != QMV_PACK_HEADER_BYTES:
+                raise ValueError(f"a pack header is {QMV_PACK_HEADER_BYTES} bytes, got {len(header)}")
+            buf = ctypes.create_string_buffer(bytes(header), QMV_PACK_HEADER_BYTES)
+            _check("qmv_create_pack_from_header", _lib.qmv_create_pack_from_header(
+                ctypes.byref(h), buf, ctypes.byref(cb), ctypes.byref(sb)))
         self.handle = h
+        if header is not None:
+            n, k, b, g = _I(), _I(), _I(), _I()
+            _check("qmv_pack_info", _lib.qmv_pack_info(h, ctypes.byref(n), ctypes.byref(k), ctypes.byref(b),
+                                                       ctypes.byref(g)))
+            N, K, bits, group = n.value, k.value, b.value, g.value
         self.N, self.K, self.bits, self.group = N, K, bits, group
         self.codes_bytes, self.scales_bytes = cb.value, sb.value
         self.words = None
         self.scales = None
+
+    @classmethod
+    def from_header(cls, header: bytes) -> "Pack":
+        """The pack described by a saved header (qmv_create_pack_from_header);
+        bind its reloaded buffers with bind_packed."""
+        return cls(0, 0, 0, 0, header=header)
+
+    def header(self) -> bytes:
+        return qmv_pack_header(self)
+
+    def bind_packed(self, words: torch.Tensor, scales: torch.Tensor):
+        """words, scales: device buffers holding the packed words and scales of
+        this shape (as pack_weights left them, e.g. reloaded from a file)."""
+        qmv_bind_packed(self, words, scales)
+        self.words, self.scales = words, scales
+        return self
 
     @property
     def packed_bytes(self) -> int:
@@ -310,6 +342,22 @@ def qmv_pack_info(p: Pack):
     _check("qmv_pack_info", _lib.qmv_pack_info(p.handle, ctypes.byref(n), ctypes.byref(k),
                                                ctypes.byref(b), ctypes.byref(g)))
     return n.value, k.value, b.value, g.value
+
+
+def qmv_pack_header(p: Pack) -> bytes:
+    buf = ctypes.create_string_buffer(QMV_PACK_HEADER_BYTES)
+    _check("qmv_pack_header", _lib.qmv_pack_header(p.handle, buf))
+    return buf.raw
+
+
+def qmv_create_pack_from_header(header: bytes) -> Pack:
+    return Pack.from_header(header)
+
+
+def qmv_bind_packed(p: Pack, d_codes, d_scales):
+    _need_bytes("d_codes", d_codes, p.codes_bytes)
+    _need_bytes("d_scales", d_scales, p.scales_bytes)
+    _check("qmv_bind_packed", _lib.qmv_bind_packed(p.handle, _dptr(d_codes), _dptr(d_scales)))
 
 
 def qmv_status_string(status: int) -> str:

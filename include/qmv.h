@@ -255,6 +255,42 @@ QMV_API int qmv_unpack_codes(const qmv_pack *p, int8_t *d_codes_out, void *strea
 /* qmv_pack_info -- read back a pack's shape (any out pointer may be NULL). */
 QMV_API int qmv_pack_info(const qmv_pack *p, int *N, int *K, int *bits, int *group);
 
+/*
+ * Saving and reloading packed weights.  A saved pack is its 64-byte header
+ * followed by the bytes of d_codes and of d_scales exactly as
+ * qmv_pack_weights wrote them (the caller copies them; the library does no
+ * file or host I/O).  Header, little-endian:
+ *   bytes  0..7   magic "QMVPACK" and a zero byte
+ *   bytes  8..11  uint32 layout version (QMV_PACK_VERSION: the packed-word
+ *                 layout of qmv_pack_weights; any other version is refused)
+ *   bytes 12..15  uint32 header size (64)
+ *   bytes 16..31  int32 N, K, bits, group
+ *   bytes 32..47  uint64 codes_bytes, scales_bytes
+ *   bytes 48..63  zero
+ */
+#define QMV_PACK_HEADER_BYTES 64
+#define QMV_PACK_VERSION 1
+
+/* qmv_pack_header -- write the header of pack p to header_out (64 bytes,
+ * host memory).  Errors: INVALID_ARG (p not a pack, header_out NULL).
+ * Host only. */
+QMV_API int qmv_pack_header(const qmv_pack *p, void *header_out);
+
+/* qmv_create_pack_from_header -- check a saved header and describe its pack,
+ * as qmv_create_pack would (codes_bytes, scales_bytes nullable).
+ * Errors: INVALID_ARG (NULL, wrong magic or header size, nonzero reserved
+ * bytes, bits/group not allowed), UNSUPPORTED (another layout version),
+ * SHAPE (shape not allowed, or byte counts that disagree with it).  Host only. */
+QMV_API int qmv_create_pack_from_header(qmv_pack **out, const void *header,
+                                        size_t *codes_bytes, size_t *scales_bytes);
+
+/* qmv_bind_packed -- bind device buffers that already hold packed words and
+ * scales (the output of qmv_pack_weights for this shape, e.g. reloaded from a
+ * saved pack), without packing.  d_codes, d_scales: device, 16-byte aligned,
+ * codes_bytes and scales_bytes long; the pack keeps them, as with
+ * qmv_pack_weights.  Errors: INVALID_ARG (NULL), ALIGNMENT.  Host only. */
+QMV_API int qmv_bind_packed(qmv_pack *p, void *d_codes, void *d_scales);
+
 /* qmv_destroy_pack -- free the host descriptor (never the device buffers). */
 QMV_API int qmv_destroy_pack(qmv_pack *p);
 

@@ -56,3 +56,36 @@ def test_device_generator_matches_host(bits):
     s2 = synth.scales(SEED, "gen", N, 64).numpy()
     assert np.array_equal(s1.view(np.uint16), s2.view(np.uint16))
     assert s2.min() >= np.float16(0.005) and s2.max() <= np.float16(0.02)
+
+
+@pytest.mark.parametrize("N,K,bits,group", [(300, 2048, 2, 32), (257, 5376, 4, 32), (65, 2048, 8, 2048)])
+def test_saved_pack_reloads_bit_exact(tmp_path, N, K, bits, group):
+    # save = header + the packed words and scales as the packer left them;
+    # reload into fresh device buffers, bind without packing, and the matvec
+    # is bit-identical to the original pack's (and to the oracle in exact mode)
+    from gpu_util import acts, bits_equal, first_diff, to_dev
+    q = qmv()
+    m = Mat(f"save{N}x{K}b{bits}", N, K, bits, group)
+    path = tmp_path / "w.qmvpack"
+    with open(path, "wb") as f:
+        f.write(m.pack.header())
+        f.write(m.pack.words.cpu().numpy().tobytes())
+        f.write(m.pack.scales.cpu().numpy().tobytes())
+    blob = path.read_bytes()
+    r = q.Pack.from_header(blob[:q.QMV_PACK_HEADER_BYTES])
+    assert (r.N, r.K, r.bits, r.group) == (N, K, bits, group)
+    assert len(blob) == q.QMV_PACK_HEADER_BYTES + r.codes_bytes + r.scales_bytes
+    off = q.QMV_PACK_HEADER_BYTES
+    words = torch.frombuffer(bytearray(blob[off:off + r.codes_bytes]), dtype=torch.int32).to(dev())
+    scales = torch.frombuffer(bytearray(blob[off + r.codes_bytes:]), dtype=torch.float16).to(dev())
+    r.bind_packed(words, scales)
+    x, _, _ = acts(f"save{N}x{K}", 1, K)
+    y0 = q.qmv_gemv(m.pack, to_dev(x), mode=q.QMV_EXACT)
+    y1 = q.qmv_gemv(r, to_dev(x), mode=q.QMV_EXACT)
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int32), y1.view(torch.int32))
+    codes, sc = m.host()
+    ref = oracle.gemv(codes, sc, group, x)
+    got = y1.cpu().numpy()
+    assert bits_equal(got, ref), first_diff(got, ref)
+    assert q.qmv_device_error(clear=True) == 0
