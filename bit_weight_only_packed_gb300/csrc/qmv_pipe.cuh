@@ -369,10 +369,108 @@ __device__ __forceinline__ float residual_blk(const uint32_t (&x)[16], const uin
 // receives h.  One round of global loads: x and r of a thread's block are
 // loaded together (gamma prefetched into L1 meanwhile), and the block's h
 // stays in registers.
+// The fused prologue with eight elements a thread, for K <= 8 * nt (whole
+// warps: tt = 0 .. nt-1 in warp order).  Every thread runs the same short
+// straight-line path once: a launch's prologue runs cold, at several cycles
+// per instruction, so its length, not its arithmetic, sets its time.  Lanes
+// 4j .. 4j+3 hold the four octets of one 32-code block; the block's serial
+// chains (its sum of squares over elements 0..31, and the folded form's two
+// activation sums) pass through them in element order by shuffles, so every
+// sum is formed in the same order as with one thread per block.
+template <int BITS, bool EXACT>
+__device__ __forceinline__ void build_table_octets(const GemvArgs& a, float* y2f, float* ysum, float* bsum,
+                                                   float* inv_sh, __half* h_out, int tt, int nt, int bar_id) {
+  constexpr int CPW = 32 / BITS;
+  const int K = a.K, NB = K / 32;
+  const int lane = tt & 31, base = lane & ~3, oq = lane & 3;
+  const bool live = 8 * tt < K;   // a block's four octets are all live or all not
+  const int e0 = live ? 8 * tt : 0;
+  const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + e0));
+  const uint4 rv = __ldg(reinterpret_cast<const uint4*>(a.r + e0));
+  const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + e0));
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, rw[4] = {rv.x, rv.y, rv.z, rv.w};
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  uint32_t hw[4];
+  float hf[8];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const __half2 xx = u32_as_h2(xw[w]), rr = u32_as_h2(rw[w]);
+    const __half lo = __float2half_rn(__fadd_rn(__low2float(xx), __low2float(rr)));
+    const __half hi = __float2half_rn(__fadd_rn(__high2float(xx), __high2float(rr)));
+    hf[2 * w] = __half2float(lo);
+    hf[2 * w + 1] = __half2float(hi);
+    hw[w] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+  float run = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (oq == k) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) run = __fmaf_rn(hf[e], hf[e], run);
+    }
+    run = __shfl_sync(0xffffffffu, run, base | k);
+  }
+  if (live) {
+    if (oq == 3) bsum[tt >> 2] = run;
+    if (h_out) *reinterpret_cast<uint4*>(h_out + e0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  }
+  named_bar(bar_id, nt);
+  if (tt == 0) {
+    // serial over the blocks, 16-byte loads issued ahead of the adds
+    float ss = 0.0f;
+    const float4* b4 = reinterpret_cast<const float4*>(bsum);
+#pragma unroll 4
+    for (int q = 0; q < NB / 4; ++q) {
+      const float4 v = b4[q];
+      ss = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(ss, v.x), v.y), v.z), v.w);
+    }
+    const float mean = __fdiv_rn(ss, (float)K);
+    *inv_sh = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
+  }
+  named_bar(bar_id, nt);
+  const float inv = *inv_sh;
+  uint32_t y[4];
+  float yf[8];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const __half2 hh = u32_as_h2(hw[w]), gg = u32_as_h2(gw[w]);
+    const __half yl = __float2half_rn(__fmul_rn(__fmul_rn(__low2float(hh), inv), __low2float(gg)));
+    const __half yh = __float2half_rn(__fmul_rn(__fmul_rn(__high2float(hh), inv), __high2float(gg)));
+    yf[2 * w] = __half2float(yl);
+    yf[2 * w + 1] = __half2float(yh);
+    y[w] = (uint32_t)__half_as_ushort(yl) | ((uint32_t)__half_as_ushort(yh) << 16);
+  }
+  if (live) store_y8<BITS, EXACT>(y2f, e0, y);
+  if (!EXACT) {
+    // the block's two activation sums (elements with (k / CPW) even, odd),
+    // each serially in k, through the block's octets in order
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (oq == k) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (((8 * k + e) / CPW) & 1)
+            s1 = __fadd_rn(s1, yf[e]);
+          else
+            s0 = __fadd_rn(s0, yf[e]);
+        }
+      }
+      s0 = __shfl_sync(0xffffffffu, s0, base | k);
+      s1 = __shfl_sync(0xffffffffu, s1, base | k);
+    }
+    if (live && oq == 3) ysum[tt >> 2] = __fmul_rn(__fadd_rn(s0, s1), (float)(1 << (BITS - 1)));
+  }
+}
+
 template <int BITS, bool FUSED, bool EXACT>
 __device__ __forceinline__ void build_table(const GemvArgs& a, float* y2f, float* ysum, float* bsum,
                                             float* inv_sh, __half* h_out, int tt, int nt, int bar_id) {
   const int K = a.K, NB = K / 32;
+  if (FUSED && K <= 8 * nt) {
+    build_table_octets<BITS, EXACT>(a, y2f, ysum, bsum, inv_sh, h_out, tt, nt, bar_id);
+    return;
+  }
   if (FUSED) {
     // pass 1: h and the block sums of squares (the block's h stays in
     // registers when every thread has at most one block; its gamma is
